@@ -1,0 +1,96 @@
+"""The five benchmark / parity workloads, with their synthetic input recipes.
+
+Shapes follow the four POPCORNBENCH transcript pages:
+
+* ``conv331_tiny`` / ``conv331``: Conv3d with a (3,3,1) kernel, the depth-1
+  case of "Kimi-K2.6 l1_p59" (scaled: Cin 16, Cout 64, 16x128x128x8 input).
+* ``convT_s2p1d2``: ConvTranspose3d 32->64, k3 s2 p1 d2 on a [16,32,16,32,32]
+  input ("Kimi-K2.6 l1_p77" test case).  The output is [16,64,33,65,65]: the
+  page's own output-size formula applied per axis (its 33^3 applies the depth
+  length to all three axes).
+* ``convT_bn_avgpool``: ConvTranspose3d 3->16, k3 s2 p1 + bias -> BatchNorm3d
+  (batch statistics, eps 1e-5, gamma 1, beta 0) -> AvgPool3d(2) twice on a
+  [64,3,32,32,32] input ("Kimi-K2.6 l2_p72").
+* ``conv_maxpool_lse_relu``: Conv3d 32->64, k3 s1 p1 + bias -> MaxPool3d(2,2)
+  -> logsumexp over channels -> ReLU on a [4,32,32,128,128] input
+  ("Kimi-K2.6 l2_p43").
+
+Inputs: x ~ N(0,1); weights and bias ~ U(-1/sqrt(fan_in), +1/sqrt(fan_in)).
+fan_in is Cin/G * kernel volume for the convolutions and for the
+ConvTranspose3d 32->64 workload (32*27, as its recipe states); for the
+ConvTranspose3d 3->16 workload, whose recipe gives no bound, it is PyTorch's
+default for that layer, weight.size(1) * kvol = 16*27.  Seeds: x 1000*i+1,
+w 1000*i+2, bias 1000*i+3 for workload i = 1..5.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import inputs
+
+
+@dataclass(frozen=True)
+class Workload:
+    index: int
+    name: str
+    op: str  # "conv3d" | "conv_transpose3d" | "convT_bn_avgpool" | "conv_maxpool_lse_relu"
+    x_shape: tuple
+    w_shape: tuple
+    bias: bool
+    stride: tuple = (1, 1, 1)
+    padding: tuple = (0, 0, 0)
+    dilation: tuple = (1, 1, 1)
+    output_padding: tuple = (0, 0, 0)
+    groups: int = 1
+    eps: float = 1e-5
+    desc: str = ""
+    fan_in: int = 0
+
+    @property
+    def transposed(self) -> bool:
+        return self.op in ("conv_transpose3d", "convT_bn_avgpool")
+
+    @property
+    def cout(self) -> int:
+        return self.w_shape[1] * self.groups if self.transposed else self.w_shape[0]
+
+    def make_inputs(self, x_dist: str = "normal"):
+        """(x, w, b) float32 arrays; b is None without bias."""
+        i = self.index
+        bound = 1.0 / math.sqrt(self.fan_in)
+        if x_dist == "normal":
+            x = inputs.normal(1000 * i + 1, self.x_shape)
+        else:  # "uniform01": torch.rand-style inputs used on the pages
+            x = inputs.uniform(1000 * i + 1, self.x_shape, 0.0, 1.0)
+        w = inputs.uniform(1000 * i + 2, self.w_shape, -bound, bound)
+        b = inputs.uniform(1000 * i + 3, (self.cout,), -bound, bound) if self.bias else None
+        return x, w, b
+
+    def kwargs(self) -> dict:
+        kw = dict(stride=self.stride, padding=self.padding, dilation=self.dilation,
+                  groups=self.groups)
+        if self.transposed:
+            kw["output_padding"] = self.output_padding
+        return kw
+
+
+WORKLOADS = [
+    Workload(1, "conv331_tiny", "conv3d", (2, 4, 16, 16, 4), (8, 4, 3, 3, 1), True,
+             fan_in=4 * 9, desc="Conv3d (3,3,1) tiny oracle check"),
+    Workload(2, "conv331", "conv3d", (16, 16, 128, 128, 8), (64, 16, 3, 3, 1), True,
+             fan_in=16 * 9, desc="Conv3d (3,3,1), depth axis acts as extra batch"),
+    Workload(3, "convT_s2p1d2", "conv_transpose3d", (16, 32, 16, 32, 32), (32, 64, 3, 3, 3),
+             False, stride=(2, 2, 2), padding=(1, 1, 1), dilation=(2, 2, 2),
+             fan_in=32 * 27, desc="ConvTranspose3d 32->64 k3 s2 p1 d2"),
+    Workload(4, "convT_bn_avgpool", "convT_bn_avgpool", (64, 3, 32, 32, 32), (3, 16, 3, 3, 3),
+             True, stride=(2, 2, 2), padding=(1, 1, 1), fan_in=16 * 27,
+             desc="ConvTranspose3d 3->16 k3 s2 p1 + BN(batch) + AvgPool3d(2) x2"),
+    Workload(5, "conv_maxpool_lse_relu", "conv_maxpool_lse_relu", (4, 32, 32, 128, 128),
+             (64, 32, 3, 3, 3), True, padding=(1, 1, 1), fan_in=32 * 27,
+             desc="Conv3d 32->64 k3 p1 + MaxPool3d(2) + logsumexp_c + ReLU"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
