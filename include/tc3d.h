@@ -1,0 +1,161 @@
+/*
+ * tc3d.h -- C ABI of the GB300 (sm_103a) 3-D convolution / transposed
+ * convolution library with fused epilogues.
+ *
+ * Operations (the four POPCORNBENCH transcript pages define them; cited by
+ * page title):
+ *   tc3d_conv3d_fwd            Conv3d forward, any stride / padding /
+ *                              dilation / groups, including the depth-1
+ *                              (k,k,1) kernel ("Kimi-K2.6 l1_p59": the
+ *                              direct-convolution formula with per-axis
+ *                              stride, padding and dilation).
+ *   tc3d_conv_transpose3d_fwd  ConvTranspose3d forward ("Kimi-K2.6 l1_p77":
+ *                              receive form -- output z takes tap k iff
+ *                              (z + p - d*k) is divisible by s and the
+ *                              quotient is a valid input index).
+ *   tc3d_conv_maxpool_lse_relu Conv3d -> MaxPool3d(2,2) -> logsumexp over the
+ *                              channel axis (keepdim) -> ReLU
+ *                              ("Kimi-K2.6 l2_p43", problem statement).
+ *   tc3d_convT_bn_avgpool      ConvTranspose3d -> BatchNorm3d with batch
+ *                              statistics (biased variance) -> AvgPool3d(2)
+ *                              -> AvgPool3d(2) ("Kimi-K2.6 l2_p72", problem
+ *                              statement; the two pools are one 4x4x4 pool
+ *                              by that page's pooling derivation).
+ *
+ * Common conventions for every entry point:
+ *  - Tensors are contiguous NCDHW fp32 in device memory.  Spatial axes are
+ *    positional (S0, S1, S2), S2 contiguous.  x: [N, Cin, S0, S1, S2].
+ *  - Conv weights: [Cout, Cin/groups, k0, k1, k2].  Transposed-conv weights:
+ *    [Cin, Cout/groups, k0, k1, k2] (PyTorch layouts).
+ *  - stride, pad, dilation, output_padding point to 3 host ints each
+ *    (per-axis values).  output_padding may be NULL (zeros) and must be
+ *    zeros for the convolutions; for transposed convolutions each entry
+ *    must be smaller than max(stride, dilation) of its axis.
+ *  - bias, gamma, beta may be NULL (meaning 0, 1, 0).
+ *  - workspace: caller-owned device memory of at least the size
+ *    tc3d_workspace_bytes reports for the same arguments, 256-byte aligned.
+ *    It holds the tensor-core-packed weights (and, for the fused BatchNorm,
+ *    the per-tile partial sums).  The library never allocates or frees
+ *    device memory and never frees caller pointers.
+ *  - All work is enqueued on `stream`; nothing synchronises.  Input and
+ *    output buffers must not overlap each other or the workspace.
+ *  - Return value: TC3D_OK (0) or a negative TC3D_ERR_* code.  Argument
+ *    errors are detected on the host before anything is launched and leave
+ *    y untouched.  TC3D_ERR_CUDA reports a launch failure.  A device-side
+ *    wait that ran out of time is reported by tc3d_last_device_error.
+ *  - Pointers to tensors must be 16-byte aligned (cudaMalloc gives 256).
+ */
+#ifndef TC3D_H
+#define TC3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TC3D_OK 0
+#define TC3D_ERR_NULL (-1)           /* a required pointer is NULL */
+#define TC3D_ERR_SHAPE (-2)          /* non-positive size or empty output */
+#define TC3D_ERR_GROUPS (-3)         /* Cin or Cout not divisible by groups */
+#define TC3D_ERR_OUTPUT_PADDING (-4) /* output_padding out of range */
+#define TC3D_ERR_ALIGN (-5)          /* tensor or workspace pointer misaligned */
+#define TC3D_ERR_WORKSPACE (-6)      /* workspace NULL or too small */
+#define TC3D_ERR_UNSUPPORTED (-7)    /* outside the implemented limits */
+#define TC3D_ERR_CUDA (-8)           /* a CUDA runtime call or launch failed */
+#define TC3D_ERR_DEVICE_TIMEOUT (-9) /* a device-side wait ran out of time */
+#define TC3D_ERR_DEVICE (-10)        /* current device is not sm_100-family */
+
+/* Operation selectors for the query functions. */
+#define TC3D_OP_CONV3D 0
+#define TC3D_OP_CONV_TRANSPOSE3D 1
+#define TC3D_OP_CONV_MAXPOOL_LSE_RELU 2
+#define TC3D_OP_CONVT_BN_AVGPOOL 3
+
+/* y[n,oc,o] = bias[oc] + sum_{ic in group(oc), k} w[oc,ic',k] *
+ *             x[n, ic, o*stride - pad + dilation*k]   (zero outside x)
+ * y: [N, Cout, O0, O1, O2], O = floor((S + 2p - d(k-1) - 1)/s) + 1. */
+int tc3d_conv3d_fwd(const float* x, const float* w, const float* bias, float* y, int N,
+                    int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                    const int stride[3], const int pad[3], const int dilation[3],
+                    const int output_padding[3], int groups, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
+/* y[n,oc,z] = bias[oc] + sum_{ic in group(oc), k : s | (z+p-d k)} w[ic,oc',k] *
+ *             x[n, ic, (z + p - d k)/s]   (terms with the quotient outside x dropped)
+ * y: [N, Cout, O0, O1, O2], O = (S-1)s - 2p + d(k-1) + output_padding + 1.
+ * Computed per output-parity class as dense sub-convolutions; classes with
+ * no tap hold the bias. */
+int tc3d_conv_transpose3d_fwd(const float* x, const float* w, const float* bias, float* y,
+                              int N, int Cin, int S0, int S1, int S2, int Cout, int k0,
+                              int k1, int k2, const int stride[3], const int pad[3],
+                              const int dilation[3], const int output_padding[3], int groups,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* c = conv3d (as tc3d_conv3d_fwd); m = MaxPool3d(2,2) of c (floor mode);
+ * y[n,0,q] = max(0, logsumexp_oc m[n,oc,q]).
+ * y: [N, 1, floor(O0/2), floor(O1/2), floor(O2/2)].  The conv output never
+ * leaves the chip. */
+int tc3d_conv_maxpool_lse_relu(const float* x, const float* w, const float* bias, float* y,
+                               int N, int Cin, int S0, int S1, int S2, int Cout, int k0,
+                               int k1, int k2, const int stride[3], const int pad[3],
+                               const int dilation[3], const int output_padding[3], int groups,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* t = conv_transpose3d (as above); per channel c, mean and biased variance
+ * of t over (N, all O0*O1*O2 positions); b = (t - mean)/sqrt(var + eps) *
+ * gamma[c] + beta[c]; y = AvgPool3d(2)(AvgPool3d(2)(b)), floor mode.
+ * y: [N, Cout, floor(floor(O0/2)/2), ...].  eps >= 0. */
+int tc3d_convT_bn_avgpool(const float* x, const float* w, const float* bias, const float* gamma,
+                          const float* beta, float eps, float* y, int N, int Cin, int S0,
+                          int S1, int S2, int Cout, int k0, int k1, int k2,
+                          const int stride[3], const int pad[3], const int dilation[3],
+                          const int output_padding[3], int groups, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/* Host-only queries (no device work).  op is a TC3D_OP_* selector; the
+ * remaining arguments are those of the matching entry point.  Both validate
+ * the arguments exactly as the entry point does. */
+int tc3d_workspace_bytes(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0,
+                         int k1, int k2, const int stride[3], const int pad[3],
+                         const int dilation[3], const int output_padding[3], int groups,
+                         size_t* bytes);
+
+/* out_dims[5] receives the dims of y (integer-exact). */
+int tc3d_out_shape(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
+                   int k2, const int stride[3], const int pad[3], const int dilation[3],
+                   const int output_padding[3], int groups, int64_t out_dims[5]);
+
+/* Writes a JSON description of the launch plan (row grid, parity classes,
+ * tap tables, tiles, chunking, shared-memory budget) into buf (NUL
+ * terminated, truncated to buflen).  Returns the status of the plan. */
+int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0,
+                       int k1, int k2, const int stride[3], const int pad[3],
+                       const int dilation[3], const int output_padding[3], int groups,
+                       char* buf, size_t buflen);
+
+/* Synchronises `stream`, then returns TC3D_ERR_DEVICE_TIMEOUT if any kernel
+ * of this library on the current device gave up on a bounded wait since the
+ * last call (and clears that flag), TC3D_ERR_CUDA on a CUDA error, else
+ * TC3D_OK. */
+int tc3d_last_device_error(cudaStream_t stream);
+
+/* Sets the time limit of every device-side wait (default 2 s).  A value of
+ * 0 restores the default.  Affects launches made after the call. */
+void tc3d_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the bounded-wait path: launches one CTA that waits on an
+ * mbarrier nobody arrives on, for at most timeout_ns, then returns.
+ * Returns the value tc3d_last_device_error gives afterwards (expected:
+ * TC3D_ERR_DEVICE_TIMEOUT). */
+int tc3d_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* tc3d_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TC3D_H */

@@ -153,6 +153,12 @@ def _geom(x, w):
     return N, Cin, S0, S1, S2, k0, k1, k2
 
 
+def _check_w(x, w, groups, transposed):
+    ok = w.shape[0] == x.shape[1] if transposed else w.shape[1] * groups == x.shape[1]
+    if not ok or w.ndim != 5 or x.ndim != 5:
+        raise ValueError(f"weight {w.shape} does not fit input {x.shape} with groups={groups}")
+
+
 def _check(rc, what):
     if rc != 0:
         raise ValueError(f"oracle {what}: invalid arguments")
@@ -164,6 +170,7 @@ def conv3d(x, w, b=None, stride=1, padding=0, dilation=1, groups=1, nthreads=Non
     w, wp = _d(w)
     b, bp = _d(b)
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, False)
     Cout = w.shape[0]
     shp = conv_out_shape(x.shape, w.shape, stride, padding, dilation)
     if min(shp) <= 0:
@@ -182,6 +189,7 @@ def conv3d_at(x, w, b, idx, stride=1, padding=0, dilation=1, groups=1, nthreads=
     b, bp = _d(b)
     idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, False)
     out = np.empty(idx.shape, np.float64)
     _check(_load().oracle_conv3d_at(xp, wp, bp, N, Cin, S0, S1, S2, w.shape[0], k0, k1, k2,
                                     _i3(stride), _i3(padding), _i3(dilation), groups,
@@ -197,6 +205,7 @@ def conv_transpose3d(x, w, b=None, stride=1, padding=0, dilation=1, output_paddi
     w, wp = _d(w)
     b, bp = _d(b)
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
     shp = convT_out_shape(x.shape, w.shape, stride, padding, dilation, output_padding, groups)
     if min(shp) <= 0:
         raise ValueError("empty convT output")
@@ -215,6 +224,7 @@ def conv_transpose3d_at(x, w, b, idx, stride=1, padding=0, dilation=1, output_pa
     b, bp = _d(b)
     idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
     out = np.empty(idx.shape, np.float64)
     _check(_load().oracle_conv_transpose3d_at(
         xp, wp, bp, N, Cin, S0, S1, S2, w.shape[1] * groups, k0, k1, k2, _i3(stride),
@@ -230,6 +240,7 @@ def conv_transpose3d_scatter(x, w, b=None, stride=1, padding=0, dilation=1,
     w, wp = _d(w)
     b, bp = _d(b)
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
     shp = convT_out_shape(x.shape, w.shape, stride, padding, dilation, output_padding, groups)
     y = np.empty(shp, np.float64)
     _check(_load().oracle_conv_transpose3d_scatter(
@@ -295,6 +306,7 @@ def convT_bn_avgpool(x, w, b=None, gamma=None, beta=None, eps=1e-5, stride=1, pa
     g, gp = _d(gamma)
     be, bep = _d(beta)
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
     shp = convT_out_shape(x.shape, w.shape, stride, padding, dilation, output_padding, groups)
     out_shape = shp[:2] + tuple(o // 2 // 2 for o in shp[2:])
     y = np.empty(out_shape, np.float64)
@@ -315,6 +327,7 @@ def convT_bn_avgpool_at(x, w, b, idx, gamma=None, beta=None, eps=1e-5, stride=1,
     be, bep = _d(beta)
     idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
     Cout = w.shape[1] * groups
     out = np.empty(idx.shape, np.float64)
     mean = np.empty(Cout, np.float64)
@@ -334,6 +347,7 @@ def conv_maxpool_lse_relu(x, w, b=None, stride=1, padding=0, dilation=1, groups=
     w, wp = _d(w)
     b, bp = _d(b)
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, False)
     shp = conv_out_shape(x.shape, w.shape, stride, padding, dilation)
     y = np.empty((N, 1) + tuple(o // 2 for o in shp[2:]), np.float64)
     _check(_load().oracle_conv_maxpool_lse_relu(
@@ -350,6 +364,7 @@ def conv_maxpool_lse_relu_at(x, w, b, idx, stride=1, padding=0, dilation=1, grou
     b, bp = _d(b)
     idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
     N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, False)
     out = np.empty(idx.shape, np.float64)
     _check(_load().oracle_conv_maxpool_lse_relu_at(
         xp, wp, bp, N, Cin, S0, S1, S2, w.shape[0], k0, k1, k2, _i3(stride), _i3(padding),

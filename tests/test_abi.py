@@ -1,0 +1,228 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol, and
+its host-side logic (output shapes, argument validation, the transposed
+convolution's parity classes and tap tables) is exact.  No device calls."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import transposed_conv_epilogues_gb300 as tc
+from transposed_conv_epilogues_gb300 import build as tcbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tcbuild.build()
+    return tc.load()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "tc3d.h")).read()
+    return sorted(set(re.findall(r"\b(tc3d_[A-Za-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert set(declared) == set(tc.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in range(-10, 1):
+        assert tc.status_string(st) not in ("", "unknown status")
+    assert tc.status_string(-99) == "unknown status"
+
+
+# --------------------------------------------------------------------------
+# output shapes agree with the oracle's independent size formulas
+# --------------------------------------------------------------------------
+def test_out_shapes_vs_oracle(lib, oracle):
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        S = tuple(int(v) for v in rng.integers(1, 12, 3))
+        k = tuple(int(v) for v in rng.integers(1, 5, 3))
+        s = tuple(int(v) for v in rng.integers(1, 4, 3))
+        p = tuple(int(v) for v in rng.integers(0, 3, 3))
+        d = tuple(int(v) for v in rng.integers(1, 4, 3))
+        G = int(rng.choice([1, 2]))
+        xs, wc, wt = (2, 2 * G) + S, (2 * G, 2) + k, (2 * G, 3) + k
+        ref = oracle.conv_out_shape(xs, wc, s, p, d)
+        if min(ref) > 0:
+            assert tc.out_shape(0, xs, wc, s, p, d, 0, G) == ref
+            if min(ref[2:]) >= 2:
+                assert tc.out_shape(2, xs, wc, s, p, d, 0, G) == (2, 1) + tuple(
+                    o // 2 for o in ref[2:])
+        else:
+            with pytest.raises(tc.Tc3dError):
+                tc.out_shape(0, xs, wc, s, p, d, 0, G)
+        op = tuple(int(rng.integers(0, max(a, b))) for a, b in zip(s, d))
+        reft = oracle.convT_out_shape(xs, wt, s, p, d, op, G)
+        if min(reft) > 0:
+            assert tc.out_shape(1, xs, wt, s, p, d, op, G) == reft
+            if min(reft[2:]) >= 4:
+                assert tc.out_shape(3, xs, wt, s, p, d, op, G) == reft[:2] + tuple(
+                    o // 4 for o in reft[2:])
+
+
+def test_workload_shapes(lib):
+    from transposed_conv_epilogues_gb300.workloads import WORKLOADS
+    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3}
+    expect = {1: (2, 8, 14, 14, 4), 2: (16, 64, 126, 126, 8), 3: (16, 64, 33, 65, 65),
+              4: (64, 16, 15, 15, 15), 5: (4, 1, 16, 64, 64)}
+    for wl in WORKLOADS:
+        assert tc.out_shape(ops[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
+                            wl.dilation, wl.output_padding, wl.groups) == expect[wl.index]
+
+
+# --------------------------------------------------------------------------
+# argument validation happens on the host, before any device work
+# --------------------------------------------------------------------------
+def _call(lib, fn, ptrs, geom, ws=256):
+    dummy = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    return fn(*ptrs, *geom, dummy if ws else None, ctypes.c_size_t(ws), None)
+
+
+def _geom(N=1, Cin=2, S=(4, 4, 4), Cout=2, k=(3, 3, 3), s=(1, 1, 1), p=(0, 0, 0), d=(1, 1, 1),
+          op=(0, 0, 0), G=1):
+    I3 = ctypes.c_int * 3
+    return (N, Cin, *S, Cout, *k, I3(*s), I3(*p), I3(*d), I3(*op), G)
+
+
+@pytest.mark.parametrize("name", ["tc3d_conv3d_fwd", "tc3d_conv_transpose3d_fwd",
+                                  "tc3d_conv_maxpool_lse_relu"])
+def test_argument_errors(lib, name):
+    fn = getattr(lib, name)
+    P = ctypes.c_void_p
+    ok = (P(256), P(512), None, P(1024))
+    assert _call(lib, fn, (None, P(512), None, P(1024)), _geom()) == tc.TC3D_ERR_NULL
+    assert _call(lib, fn, (P(256), None, None, P(1024)), _geom()) == tc.TC3D_ERR_NULL
+    assert _call(lib, fn, (P(256), P(512), None, None), _geom()) == tc.TC3D_ERR_NULL
+    assert _call(lib, fn, ok, _geom(N=0)) == tc.TC3D_ERR_SHAPE
+    assert _call(lib, fn, ok, _geom(S=(4, -1, 4))) == tc.TC3D_ERR_SHAPE
+    assert _call(lib, fn, ok, _geom(s=(1, 0, 1))) == tc.TC3D_ERR_SHAPE
+    assert _call(lib, fn, ok, _geom(Cin=3, G=2)) == tc.TC3D_ERR_GROUPS
+    assert _call(lib, fn, ok, _geom(Cout=3, G=2, Cin=2)) == tc.TC3D_ERR_GROUPS
+    assert _call(lib, fn, ok, _geom(k=(17, 1, 1), S=(20, 4, 4))) == tc.TC3D_ERR_UNSUPPORTED
+    assert _call(lib, fn, (P(258), P(512), None, P(1024)), _geom()) == tc.TC3D_ERR_ALIGN
+    assert _call(lib, fn, ok, _geom(), ws=0) == tc.TC3D_ERR_WORKSPACE
+    if name == "tc3d_conv_transpose3d_fwd":
+        assert _call(lib, fn, ok, _geom(s=(2, 2, 2), op=(2, 0, 0))) == tc.TC3D_ERR_OUTPUT_PADDING
+        assert _call(lib, fn, ok, _geom(s=(2, 1, 1), d=(3, 1, 1), op=(2, 0, 0))) != \
+            tc.TC3D_ERR_OUTPUT_PADDING  # op < max(stride, dilation) is allowed
+    else:
+        assert _call(lib, fn, ok, _geom(op=(1, 0, 0))) == tc.TC3D_ERR_OUTPUT_PADDING
+        assert _call(lib, fn, ok, _geom(S=(2, 4, 4))) == tc.TC3D_ERR_SHAPE  # empty output
+    if name == "tc3d_conv_maxpool_lse_relu":
+        assert _call(lib, fn, ok, _geom(S=(3, 4, 4))) == tc.TC3D_ERR_SHAPE  # pool of 1 -> 0
+
+
+def test_convT_bn_avgpool_argument_errors(lib):
+    fn = lib.tc3d_convT_bn_avgpool
+    P = ctypes.c_void_p
+    dummy = P(256)
+
+    def call(geom, eps=1e-5, ws=256, x=P(256)):
+        return fn(x, P(512), None, None, None, ctypes.c_float(eps), P(1024), *geom,
+                  dummy if ws else None, ctypes.c_size_t(ws), None)
+
+    assert call(_geom(S=(2, 2, 2), s=(2, 2, 2), p=(1, 1, 1))) == tc.TC3D_ERR_SHAPE  # 3 -> 0
+    assert call(_geom(), x=None) == tc.TC3D_ERR_NULL
+    assert call(_geom(s=(2, 2, 2)), ws=0) == tc.TC3D_ERR_WORKSPACE
+    assert call(_geom(s=(2, 2, 2)), eps=-1.0) == tc.TC3D_ERR_SHAPE
+
+
+def test_workspace_bytes(lib):
+    for op in range(4):
+        n = tc.workspace_bytes(op, (2, 4, 9, 9, 9), (4, 4, 3, 3, 3), 2 if op % 2 else 1, 1)
+        assert n >= 256 and n % 256 == 0
+
+
+# --------------------------------------------------------------------------
+# parity classes and tap tables of the plan, against brute force and the pages
+# --------------------------------------------------------------------------
+def _axis_tables(s, p, d, k):
+    plan = tc.plan_describe(1, (1, 1, 8, 1, 1), (1, 1, k, 1, 1), (s, 1, 1), (p, 0, 0),
+                            (d, 1, 1), 0, 1)
+    assert plan["status"] == 0
+    return plan, plan["axes"][0]
+
+
+@pytest.mark.parametrize("s,p,d,k", list(itertools.product(range(1, 5), range(0, 4),
+                                                           range(1, 5), range(1, 5))))
+def test_parity_tables_brute_force(lib, s, p, d, k):
+    plan, ax = _axis_tables(s, p, d, k)
+    u = ax["u"]
+    # brute force: class r, tap kk contributes iff s | (r + p - d kk); offset (r+p-d kk)/s
+    expect = {}
+    for r in range(s):
+        taps = {}
+        for kk in range(k):
+            t = r + p - d * kk
+            if t % s == 0:
+                taps[t // s] = kk
+        if taps:
+            expect[r] = taps
+    assert ax["classes"] == sorted(expect)
+    assert sorted(u) == sorted({uu for t in expect.values() for uu in t})
+    for ri, r in enumerate(ax["classes"]):
+        got = {u[t]: kk for t, kk in enumerate(ax["kidx"][ri]) if kk >= 0}
+        assert got == expect[r]
+    assert plan["nEmpty"] == s - len(expect)
+
+
+def _golden_pairs(name):
+    rows = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if f[0] == "total_pairs":
+            continue
+        rows[int(f[0])] = set() if f[1] == "none" else {tuple(int(v) for v in t.split(","))
+                                                         for t in f[1:]}
+    return rows
+
+
+@pytest.mark.parametrize("name,L,s,p,d", [("convT_taps_s2p1d2k3_L16.txt", 16, 2, 1, 2),
+                                          ("convT_taps_s2p1d1k3_L32.txt", 32, 2, 1, 1)])
+def test_parity_tables_match_pages(lib, name, L, s, p, d):
+    plan, ax = _axis_tables(s, p, d, 3)
+    u = ax["u"]
+    for z, pairs in _golden_pairs(name).items():
+        m, r = divmod(z, s)
+        got = set()
+        if r in ax["classes"]:
+            ri = ax["classes"].index(r)
+            for t, kk in enumerate(ax["kidx"][ri]):
+                if kk >= 0 and 0 <= m + u[t] < L:
+                    got.add((m + u[t], kk))
+        assert got == pairs, (z, got, pairs)
+
+
+def test_plans_of_workloads(lib):
+    """Structural facts of the five workloads' plans."""
+    from transposed_conv_epilogues_gb300.workloads import BY_NAME
+    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3}
+
+    def plan(n):
+        wl = BY_NAME[n]
+        return tc.plan_describe(ops[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
+                                wl.dilation, wl.output_padding, wl.groups)
+
+    c3 = plan("convT_s2p1d2")  # only the all-odd class has taps: 1 of 8, 27 taps
+    assert c3["nR"] == 1 and c3["nEmpty"] == 7 and c3["M"] == [16, 32, 32]
+    assert all(ax["classes"] == [1] and sorted(ax["kidx"][0]) == [0, 1, 2] for ax in c3["axes"])
+    c4 = plan("convT_bn_avgpool")
+    assert c4["fused"] == 1 and c4["nR"] == 8 and c4["M"] == [32, 32, 32]
+    c5 = plan("conv_maxpool_lse_relu")
+    assert c5["Q"] == [2, 2, 8] and c5["n_tile"] == 64
+    for n in BY_NAME:
+        pl = plan(n)
+        assert pl["status"] == 0 and pl["smem_bytes"] <= 227 * 1024

@@ -1,0 +1,276 @@
+"""GPU parity tests: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: |gpu - oracle| <= 1e-4 + 1e-4 * |oracle| for every compared element
+(3xTF32 products accumulated in fp32; the tolerance is the one the workloads
+are specified with), and exact integer shapes.  Small cases compare every
+output; the full-size workloads compare sampled outputs that the oracle
+evaluates one by one.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from transposed_conv_epilogues_gb300 import inputs
+from transposed_conv_epilogues_gb300.workloads import BY_NAME
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-4
+RTOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def tc():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from transposed_conv_epilogues_gb300 import build
+    build.build()
+    import transposed_conv_epilogues_gb300 as t
+    t.load()
+    return t
+
+
+def _dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def check(gpu, ref, what=""):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.argmax(np.where(bad, err - bound, -np.inf))
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at "
+                             f"{np.unravel_index(i, ref.shape)}: gpu {gpu.flat[i]!r} "
+                             f"oracle {ref.flat[i]!r}")
+
+
+def make(xs, ws, cout, bias=True, seed=7, xdist="normal"):
+    x = (inputs.normal(seed, xs) if xdist == "normal"
+         else inputs.uniform(seed, xs, 0.0, 1.0))
+    fan = int(np.prod(ws[1:]))
+    bound = 1.0 / np.sqrt(fan)
+    w = inputs.uniform(seed + 1, ws, -bound, bound)
+    b = inputs.uniform(seed + 2, (cout,), -bound, bound) if bias else None
+    return x, w, b
+
+
+# --------------------------------------------------------------------------
+# small cases: every output compared
+# --------------------------------------------------------------------------
+CONV_CASES = [
+    # x shape, w shape, stride, pad, dil, groups, bias
+    ((2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1, 1, 1, True),
+    ((2, 4, 11, 9, 13), (6, 2, 3, 2, 3), (2, 1, 2), (1, 0, 2), (1, 2, 1), 2, True),
+    ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, 1, 1, 1, True),         # (k,k,1), pad on k=1 axis
+    ((1, 6, 7, 8, 9), (40, 6, 1, 1, 1), 1, 0, 1, 1, False),          # k = 1
+    ((1, 4, 6, 6, 8), (200, 4, 3, 1, 3), 1, (1, 0, 1), 1, 1, True),  # 2 column blocks
+    ((2, 8, 7, 9, 8), (8, 2, 3, 3, 3), 1, 1, 1, 4, True),            # groups 4
+    ((1, 3, 13, 12, 16), (5, 3, 5, 3, 5), (1, 2, 1), 2, 2, 1, True),  # k5 dil 2
+    ((3, 17, 6, 5, 20), (9, 17, 2, 3, 2), 1, 0, 1, 1, True),         # Cin 17: 2 chunks
+]
+
+
+@pytest.mark.parametrize("case", CONV_CASES)
+def test_conv3d_small(tc, case):
+    xs, ws, s, p, d, G, bias = case
+    x, w, b = make(xs, ws, ws[0], bias)
+    y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), s, p, d, G).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, s, p, d, G), f"conv3d {case}")
+
+
+CONVT_CASES = [
+    # x shape, w shape, stride, pad, dil, output_padding, groups, bias
+    ((2, 6, 5, 7, 8), (6, 10, 3, 3, 3), 2, 1, 2, 0, 1, False),
+    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, True),
+    ((2, 4, 5, 6, 7), (4, 3, 3, 2, 4), (3, 2, 1), (1, 0, 2), (1, 2, 1), (2, 1, 0), 2, True),
+    ((1, 5, 6, 7, 8), (5, 6, 3, 3, 3), 1, 1, 1, 0, 1, True),
+    ((2, 3, 3, 4, 4), (3, 5, 2, 2, 2), 4, 0, 1, (3, 0, 2), 1, True),  # many empty classes
+    ((1, 2, 4, 5, 6), (2, 3, 1, 3, 2), (2, 3, 2), (0, 1, 1), (1, 1, 2), (1, 2, 0), 1, True),
+]
+
+
+@pytest.mark.parametrize("case", CONVT_CASES)
+def test_conv_transpose3d_small(tc, case):
+    xs, ws, s, p, d, op, G, bias = case
+    x, w, b = make(xs, ws, ws[1] * G, bias)
+    y = tc.conv_transpose3d_fwd(_dev(x), _dev(w), _dev(b), s, p, d, op, G).cpu().numpy()
+    check(y, orc.conv_transpose3d(x, w, b, s, p, d, op, G), f"convT {case}")
+
+
+LSE_CASES = [
+    ((2, 5, 8, 10, 16), (12, 5, 3, 3, 3), 1, 1, 1, 1),
+    ((1, 4, 9, 11, 13), (40, 2, 3, 3, 3), 1, 1, 1, 2),     # groups: running LSE across blocks
+    ((2, 3, 13, 12, 18), (6, 3, 3, 3, 3), (2, 1, 2), 1, 1, 1),  # stride, odd extents
+    ((1, 2, 6, 6, 8), (300, 2, 3, 3, 3), 1, 1, 1, 1),       # Cout 300: two column blocks
+    ((1, 4, 7, 9, 10), (8, 4, 3, 3, 1), 1, (1, 1, 0), (1, 2, 1), 1),
+]
+
+
+@pytest.mark.parametrize("case", LSE_CASES)
+def test_conv_maxpool_lse_relu_small(tc, case):
+    xs, ws, s, p, d, G = case
+    x, w, b = make(xs, ws, ws[0], True)
+    b = b - 0.3  # push some LSE values below zero so the ReLU matters
+    y = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), s, p, d, G).cpu().numpy()
+    check(y, orc.conv_maxpool_lse_relu(x, w, b, s, p, d, G), f"pool-lse {case}")
+
+
+BN_CASES = [
+    # x shape, w shape, stride, pad, dil, output_padding, groups, gamma/beta
+    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # fused
+    ((2, 7, 9, 8, 10), (7, 5, 3, 3, 3), 2, 1, 1, (0, 1, 1), 1, True),  # fused, ragged
+    ((2, 4, 6, 7, 8), (4, 3, 3, 3, 3), 2, 1, 1, 0, 2, True),          # fused, groups
+    ((2, 3, 9, 5, 6), (3, 4, 3, 3, 3), (1, 2, 2), 1, 1, 0, 1, True),  # unfused: stride 1 axis
+    ((2, 3, 6, 6, 6), (3, 4, 3, 3, 3), 2, 1, 2, 0, 1, True),          # unfused: dilation 2
+]
+
+
+@pytest.mark.parametrize("case", BN_CASES)
+def test_convT_bn_avgpool_small(tc, case):
+    xs, ws, s, p, d, op, G, affine = case
+    cout = ws[1] * G
+    x, w, b = make(xs, ws, cout, True)
+    g = inputs.uniform(99, (cout,), 0.5, 1.5) if affine else None
+    be = inputs.uniform(98, (cout,), -0.5, 0.5) if affine else None
+    y = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), _dev(g), _dev(be), 1e-5, s, p, d, op,
+                            G).cpu().numpy()
+    check(y, orc.convT_bn_avgpool(x, w, b, g, be, 1e-5, s, p, d, op, G), f"bn-pool {case}")
+
+
+def test_uniform01_inputs(tc):
+    """torch.rand-style inputs (all positive) as on the pages."""
+    x, w, b = make((2, 6, 9, 8, 12), (8, 6, 3, 3, 3), 8, True, seed=31, xdist="uniform01")
+    check(tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), 1, 1).cpu().numpy(),
+          orc.conv3d(x, w, b, 1, 1), "conv uniform01")
+    xt, wt, bt = make((2, 3, 6, 6, 6), (3, 16, 3, 3, 3), 16, True, seed=41, xdist="uniform01")
+    check(tc.convT_bn_avgpool(_dev(xt), _dev(wt), _dev(bt), None, None, 1e-5, 2, 1)
+          .cpu().numpy(), orc.convT_bn_avgpool(xt, wt, bt, None, None, 1e-5, 2, 1),
+          "bn-pool uniform01")
+
+
+# --------------------------------------------------------------------------
+# edge cases
+# --------------------------------------------------------------------------
+def test_misaligned_input_uses_plain_loads(tc):
+    """x starting 4 bytes past a 16-byte boundary cannot be a TMA source; the
+    plain-load producer must give the same result."""
+    x, w, b = make((2, 4, 6, 7, 8), (5, 4, 3, 3, 3), 5)
+    buf = torch.zeros(x.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(x.ravel()).cuda()
+    xv = buf[1:].view(x.shape)
+    assert xv.data_ptr() % 16 != 0
+    y = tc.conv3d_fwd(xv, _dev(w), _dev(b), 1, 1).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, 1, 1), "misaligned x")
+
+
+def test_guard_bands_untouched(tc):
+    x, w, b = make((2, 6, 5, 7, 8), (6, 10, 3, 3, 3), 10)
+    shp = tc.out_shape(1, x.shape, w.shape, 2, 1, 2)
+    n = int(np.prod(shp))
+    G = 4096
+    buf = torch.full((n + 2 * G,), 12345.0, dtype=torch.float32, device="cuda")
+    out = buf[G:G + n].view(shp)
+    tc.conv_transpose3d_fwd(_dev(x), _dev(w), _dev(b), 2, 1, 2, out=out)
+    h = buf.cpu().numpy()
+    assert np.all(h[:G] == 12345.0) and np.all(h[G + n:] == 12345.0)
+    check(out.cpu().numpy(), orc.conv_transpose3d(x, w, b, 2, 1, 2), "guarded convT")
+
+
+def test_deterministic_repeat(tc):
+    x, w, b = make((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 16)
+    a1 = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), None, None, 1e-5, 2, 1)
+    a2 = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), None, None, 1e-5, 2, 1)
+    assert torch.equal(a1, a2)
+    x, w, b = make((2, 5, 8, 10, 16), (12, 5, 3, 3, 3), 12)
+    c1 = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), 1, 1)
+    c2 = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), 1, 1)
+    assert torch.equal(c1, c2)
+
+
+def test_error_leaves_output_untouched(tc):
+    x, w, b = make((1, 4, 6, 6, 8), (4, 4, 3, 3, 3), 4)
+    y = torch.full(tc.out_shape(0, x.shape, w.shape, 1, 1), 7.0, device="cuda")
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tc.Tc3dError) as e:
+        tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), 1, 1, out=y, workspace=small)
+    assert e.value.status == tc.TC3D_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+
+
+def test_bounded_wait_reports_timeout(tc):
+    """A wait on an mbarrier nobody arrives on gives up after its limit and
+    the host sees TC3D_ERR_DEVICE_TIMEOUT; the context stays usable."""
+    assert tc.selftest_wait_timeout(20_000_000) == tc.TC3D_ERR_DEVICE_TIMEOUT
+    assert tc.last_device_error() == tc.TC3D_OK
+    x, w, b = make((1, 3, 5, 6, 8), (4, 3, 3, 3, 3), 4)
+    check(tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), 1, 1).cpu().numpy(),
+          orc.conv3d(x, w, b, 1, 1), "after timeout")
+    assert tc.last_device_error() == tc.TC3D_OK
+
+
+# --------------------------------------------------------------------------
+# the five workloads at full size (sampled outputs)
+# --------------------------------------------------------------------------
+def _wl(name):
+    wl = BY_NAME[name]
+    x, w, b = wl.make_inputs()
+    return wl, x, w, b
+
+
+def test_workload_conv331_tiny_full(tc):
+    wl, x, w, b = _wl("conv331_tiny")
+    y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), **wl.kwargs()).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, **wl.kwargs()), wl.name)
+
+
+def test_workload_conv331_sampled(tc):
+    wl, x, w, b = _wl("conv331")
+    y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), **wl.kwargs()).cpu().numpy().ravel()
+    idx = inputs.sample_indices(202, y.size, 20000)
+    idx = np.concatenate([idx, [0, y.size - 1]])
+    check(y[idx], orc.conv3d_at(x, w, b, idx, **wl.kwargs()), wl.name)
+
+
+def test_workload_convT_s2p1d2_sampled(tc):
+    wl, x, w, b = _wl("convT_s2p1d2")
+    y = tc.conv_transpose3d_fwd(_dev(x), _dev(w), None, **wl.kwargs()).cpu().numpy()
+    assert y.shape == (16, 64, 33, 65, 65)
+    # outputs with any even coordinate belong to classes without taps: exactly 0
+    odd = np.zeros(y.shape[2:], bool)
+    odd[1::2, 1::2, 1::2] = True
+    assert np.all(y[:, :, ~odd] == 0.0)
+    flat = y.ravel()
+    idx = inputs.sample_indices(303, flat.size, 20000)
+    idx = np.concatenate([idx, [0, flat.size - 1]])
+    check(flat[idx], orc.conv_transpose3d_at(x, w, None, idx, **wl.kwargs()), wl.name)
+
+
+def test_workload_convT_bn_avgpool_sampled(tc):
+    wl, x, w, b = _wl("convT_bn_avgpool")
+    y = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), None, None, wl.eps,
+                            **wl.kwargs()).cpu().numpy()
+    assert y.shape == (64, 16, 15, 15, 15)
+    flat = y.ravel()
+    idx = inputs.sample_indices(404, flat.size, 3000)
+    ref = orc.convT_bn_avgpool_at(x, w, b, idx, None, None, wl.eps, **wl.kwargs())
+    check(flat[idx], ref, wl.name)
+    # BatchNorm with gamma 1, beta 0: each channel of the pooled output has
+    # mean ~ 0 (pooling averages whole windows of the normalised tensor)
+    assert np.all(np.abs(y.mean(axis=(0, 2, 3, 4))) < 0.05)
+
+
+def test_workload_conv_maxpool_lse_relu_sampled(tc):
+    wl, x, w, b = _wl("conv_maxpool_lse_relu")
+    y = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), **wl.kwargs()).cpu().numpy()
+    assert y.shape == (4, 1, 16, 64, 64)
+    flat = y.ravel()
+    idx = inputs.sample_indices(505, flat.size, 1500)
+    idx = np.concatenate([idx, [0, flat.size - 1]])
+    check(flat[idx], orc.conv_maxpool_lse_relu_at(x, w, b, idx, **wl.kwargs()), wl.name)
+    # logsumexp over 64 channels >= their max, so ReLU rarely clips here
+    assert np.all(flat >= 0.0)

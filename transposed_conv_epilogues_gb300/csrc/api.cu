@@ -1,0 +1,537 @@
+// api.cu -- the C ABI (include/tc3d.h): argument checks, plans, tensor-map
+// encoding and the launches of one call, all enqueued on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tc3d.h"
+#include "engine.cuh"
+#include "plan.h"
+
+using namespace tc3d;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceState {
+  bool init = false;
+  int status = TC3D_OK;
+  int sm_count = 0;
+  int* err = nullptr;  // device address of the error word
+  bool smem_set[3] = {false, false, false};
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TC3D_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = TC3D_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = TC3D_ERR_DEVICE;  // the kernels are built for sm_103a only
+    } else if (error_flag_address(&d.err) != cudaSuccess) {
+      d.status = TC3D_ERR_CUDA;
+    }
+    if (!g_encode && d.status == TC3D_OK) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  *out = &d;
+  return d.status;
+}
+
+Problem make_problem(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
+                     int k2, const int stride[3], const int pad[3], const int dil[3],
+                     const int out_pad[3], int groups) {
+  Problem pb;
+  pb.op = op;
+  pb.N = N;
+  pb.Cin = Cin;
+  pb.S[0] = S0;
+  pb.S[1] = S1;
+  pb.S[2] = S2;
+  pb.Cout = Cout;
+  pb.k[0] = k0;
+  pb.k[1] = k1;
+  pb.k[2] = k2;
+  for (int a = 0; a < 3; ++a) {
+    pb.stride[a] = stride ? stride[a] : 1;
+    pb.pad[a] = pad ? pad[a] : 0;
+    pb.dil[a] = dil ? dil[a] : 1;
+    pb.out_pad[a] = out_pad ? out_pad[a] : 0;
+  }
+  pb.groups = groups;
+  return pb;
+}
+
+int plan_for(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+             const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
+             int groups, Plan* pl) {
+  if (!stride || !pad || !dil) return TC3D_ERR_NULL;
+  Problem pb = make_problem(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad,
+                            groups);
+  return make_plan(pb, pl);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int set_smem(DeviceState* d, int epi) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!d->smem_set[epi]) {
+    if (engine_set_smem(epi, kMaxSmem) != cudaSuccess) return TC3D_ERR_CUDA;
+    d->smem_set[epi] = true;
+  }
+  return TC3D_OK;
+}
+
+void fill_params(const Plan& pl, EngineParams* ep) {
+  std::memset(ep, 0, sizeof(*ep));
+  const Problem& pb = pl.pb;
+  ep->timeout_ns = g_timeout_ns.load();
+  ep->N = pb.N;
+  ep->C = pb.Cin;
+  ep->Cout = pb.Cout;
+  ep->G = pb.groups;
+  ep->cin_g = pl.cin_g;
+  ep->cout_g = pl.cout_g;
+  for (int a = 0; a < 3; ++a) {
+    ep->S[a] = pb.S[a];
+    ep->O[a] = (int)pl.O[a];
+    ep->P[a] = (int)pl.P[a];
+    ep->M[a] = pl.M[a];
+    ep->s_in[a] = pl.s_in[a];
+    ep->s_out[a] = pl.s_out[a];
+    ep->u_min[a] = pl.u_min[a];
+    ep->nU[a] = pl.nU[a];
+    for (int t = 0; t < kMaxAxisTaps; ++t) ep->u_rel[a][t] = pl.u_rel[a][t];
+    ep->nRaxis[a] = pl.nRaxis[a];
+    int mask = 0;
+    for (int i = 0; i < pl.nRaxis[a]; ++i) {
+      ep->r_axis[a][i] = pl.r_axis[a][i];
+      mask |= 1 << pl.r_axis[a][i];
+    }
+    ep->cls_mask[a] = mask;
+    ep->Q[a] = pl.Q[a];
+    ep->Pq[a] = pl.Pq[a];
+    ep->T[a] = pl.T[a];
+    ep->ntile[a] = pl.ntile[a];
+    ep->box[a] = pl.box[a];
+  }
+  ep->nUtot = pl.nU[0] * pl.nU[1] * pl.nU[2];
+  ep->nR = pl.nR;
+  ep->nEmpty = pl.nEmpty;
+  ep->ocb = pl.ocb;
+  ep->n_tile = pl.n_tile;
+  ep->nb_per_group = pl.nb_per_group;
+  ep->n_colblocks = pl.n_colblocks;
+  ep->n_acc = pl.n_acc;
+  ep->dbuf = pl.dbuf;
+  ep->a_stages = pl.a_stages;
+  ep->tiles = (int)pl.tiles;
+  ep->cin_chunk = pl.cin_chunk;
+  ep->n_chunks = pl.n_chunks;
+  ep->k_chunk = pl.k_chunk;
+  ep->ksteps_chunk = pl.ksteps_chunk;
+  ep->raw_stages = pl.raw_stages;
+  ep->raw_stage_bytes = (unsigned)pl.raw_stage_bytes;
+  ep->b_resident = pl.b_resident;
+  ep->b_stages = pl.b_stages;
+  ep->b_stage_bytes = (unsigned)pl.b_stage_bytes;
+  const SmemLayout L = smem_layout(pl);
+  ep->sm_raw = (unsigned)L.raw;
+  ep->sm_b = (unsigned)L.b;
+  ep->sm_ktab = (unsigned)L.ktab;
+  ep->sm_misc = (unsigned)L.misc;
+  ep->sm_bar = (unsigned)L.bar;
+}
+
+// Encode the 5-D tensor map over x, or leave use_tma = 0 (plain-load producer)
+// when x or its strides break TMA's 16-byte rules.
+void encode_xmap(const Plan& pl, const float* x, EngineParams* ep) {
+  const Problem& pb = pl.pb;
+  ep->use_tma = 0;
+  if (!g_encode || !aligned(x, 16) || (pb.S[2] % 4) != 0) return;
+  cuuint64_t dims[5] = {(cuuint64_t)pb.S[2], (cuuint64_t)pb.S[1], (cuuint64_t)pb.S[0],
+                        (cuuint64_t)pb.Cin, (cuuint64_t)pb.N};
+  cuuint64_t strides[4];
+  strides[0] = (cuuint64_t)pb.S[2] * 4;
+  strides[1] = strides[0] * pb.S[1];
+  strides[2] = strides[1] * pb.S[0];
+  strides[3] = strides[2] * pb.Cin;
+  for (int i = 0; i < 4; ++i)
+    if (strides[i] >= (1ull << 40)) return;
+  cuuint32_t box[5] = {(cuuint32_t)pl.box[2], (cuuint32_t)pl.box[1], (cuuint32_t)pl.box[0],
+                       (cuuint32_t)pl.cin_chunk, 1};
+  for (int i = 0; i < 5; ++i)
+    if (box[i] == 0 || box[i] > 256) return;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(&ep->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float*>(x),
+                        dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) ep->use_tma = 1;
+}
+
+int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cudaStream_t st) {
+  PackParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.w = w;
+  pp.out = wpack;
+  pp.transposed = pl.transposed;
+  pp.cin_g = pl.cin_g;
+  pp.cout_g = pl.cout_g;
+  for (int a = 0; a < 3; ++a) {
+    pp.k[a] = pl.pb.k[a];
+    pp.nU[a] = pl.nU[a];
+    pp.nRaxis[a] = pl.nRaxis[a];
+    for (int r = 0; r < kMaxClassesAxis; ++r)
+      for (int t = 0; t < kMaxAxisTaps; ++t) pp.kidx[a][r][t] = pl.kidx[a][r][t];
+  }
+  pp.nUtot = pl.nU[0] * pl.nU[1] * pl.nU[2];
+  pp.nR = pl.nR;
+  pp.ocb = pl.ocb;
+  pp.n_tile = pl.n_tile;
+  pp.nb_per_group = pl.nb_per_group;
+  pp.n_colblocks = pl.n_colblocks;
+  pp.cin_chunk = pl.cin_chunk;
+  pp.n_chunks = pl.n_chunks;
+  pp.k_chunk = pl.k_chunk;
+  pp.ksteps_chunk = pl.ksteps_chunk;
+  pp.total = pl.ws_wpack_bytes / 4;
+  long long blocks = (pp.total + 255) / 256;
+  if (blocks > (long long)sm_count * 8) blocks = (long long)sm_count * 8;
+  return pack_launch(pp, (unsigned)blocks, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
+}
+
+int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cudaStream_t st) {
+  if (!pl.fill_slab) return TC3D_OK;
+  const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
+  int zlo[3];
+  for (int a = 0; a < 3; ++a) zlo[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
+  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count * 4, st) ==
+                 cudaSuccess
+             ? TC3D_OK
+             : TC3D_ERR_CUDA;
+}
+
+int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, const float* bias,
+                  float* y, float2* partials, DeviceState* d, cudaStream_t st) {
+  if (pl.tiles == 0) return TC3D_OK;
+  EngineParams ep;
+  fill_params(pl, &ep);
+  ep.x = x;
+  ep.wpack = wpack;
+  ep.bias = bias;
+  ep.y = y;
+  ep.partials = partials;
+  ep.err = d->err;
+  encode_xmap(pl, x, &ep);
+  const unsigned grid = (unsigned)std::min<int64_t>(pl.tiles, d->sm_count);
+  int rc = set_smem(d, epi);
+  if (rc) return rc;
+  return engine_launch(epi, ep, grid, (size_t)pl.smem_bytes, st) == cudaSuccess ? TC3D_OK
+                                                                               : TC3D_ERR_CUDA;
+}
+
+int common_checks(const float* x, const float* w, const float* y, const float* bias,
+                  const void* ws, size_t ws_bytes, const Plan& pl) {
+  if (!x || !w || !y) return TC3D_ERR_NULL;
+  if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
+    return TC3D_ERR_ALIGN;
+  if (!ws || ws_bytes < (size_t)pl.ws_total) return TC3D_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return TC3D_ERR_ALIGN;
+  return TC3D_OK;
+}
+
+int run(int op, const float* x, const float* w, const float* bias, const float* gamma,
+        const float* beta, float eps, float* y, int N, int Cin, int S0, int S1, int S2, int Cout,
+        int k0, int k1, int k2, const int stride[3], const int pad[3], const int dil[3],
+        const int out_pad[3], int groups, void* ws, size_t ws_bytes, cudaStream_t st) {
+  Plan pl;
+  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
+                    &pl);
+  if (rc) return rc;
+  if (op == OP_CONVT_BN_POOL && !(eps >= 0.0f)) return TC3D_ERR_SHAPE;
+  rc = common_checks(x, w, y, bias, ws, ws_bytes, pl);
+  if (rc) return rc;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return TC3D_ERR_ALIGN;
+  DeviceState* d = nullptr;
+  rc = device_state(&d);
+  if (rc) return rc;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
+  rc = launch_pack(pl, w, wpack, d->sm_count, st);
+  if (rc) return rc;
+  if (op != OP_CONVT_BN_POOL) {
+    rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
+    if (rc) return rc;
+    return launch_fill(pl, bias, y, d, st);
+  }
+
+  float2* stat = reinterpret_cast<float2*>(wsb + pl.ws_stat_off);
+  const long long pvol = (long long)pl.P[0] * pl.P[1] * pl.P[2];
+  const unsigned blocks =
+      (unsigned)std::min<long long>((pl.y_elems + 255) / 256, (long long)d->sm_count * 8);
+  if (pl.fused) {
+    float2* part = reinterpret_cast<float2*>(wsb + pl.ws_part_off);
+    rc = launch_engine(pl, EPI_BN_POOL, x, wpack, bias, y, part, d, st);
+    if (rc) return rc;
+    const double count = (double)N * (double)pl.O[0] * (double)pl.O[1] * (double)pl.O[2];
+    if (bn_stats_f2_launch(part, (int)pl.tiles, bias, gamma, beta, count, eps, Cout, stat, st) !=
+            cudaSuccess ||
+        bn_apply_launch(y, pl.y_elems, pvol, Cout, stat, blocks, st) != cudaSuccess)
+      return TC3D_ERR_CUDA;
+  } else {
+    float* full = reinterpret_cast<float*>(wsb + pl.ws_full_off);
+    double* part2 = reinterpret_cast<double*>(wsb + pl.ws_part_off);
+    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st);
+    if (rc) return rc;
+    rc = launch_fill(pl, bias, full, d, st);
+    if (rc) return rc;
+    const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
+    const int P[3] = {(int)pl.P[0], (int)pl.P[1], (int)pl.P[2]};
+    if (bn_unfused_launch(full, y, part2, N, Cout, O, P, gamma, beta, eps, stat, blocks, st) !=
+        cudaSuccess)
+      return TC3D_ERR_CUDA;
+  }
+  return TC3D_OK;
+}
+
+void append(std::string& s, const char* fmt, long long v) {
+  char b[96];
+  snprintf(b, sizeof(b), fmt, v);
+  s += b;
+}
+
+std::string describe(const Plan& pl) {
+  std::string s = "{";
+  append(s, "\"status\": %lld", pl.status);
+  if (pl.status == TC3D_OK) {
+    auto arr3 = [&](const char* name, const long long v0, long long v1, long long v2) {
+      char b[160];
+      snprintf(b, sizeof(b), ", \"%s\": [%lld, %lld, %lld]", name, v0, v1, v2);
+      s += b;
+    };
+    arr3("O", pl.O[0], pl.O[1], pl.O[2]);
+    arr3("P", pl.P[0], pl.P[1], pl.P[2]);
+    arr3("M", pl.M[0], pl.M[1], pl.M[2]);
+    arr3("s_in", pl.s_in[0], pl.s_in[1], pl.s_in[2]);
+    arr3("s_out", pl.s_out[0], pl.s_out[1], pl.s_out[2]);
+    arr3("u_min", pl.u_min[0], pl.u_min[1], pl.u_min[2]);
+    arr3("Q", pl.Q[0], pl.Q[1], pl.Q[2]);
+    arr3("Pq", pl.Pq[0], pl.Pq[1], pl.Pq[2]);
+    arr3("T", pl.T[0], pl.T[1], pl.T[2]);
+    arr3("box", pl.box[0], pl.box[1], pl.box[2]);
+    // per-axis offsets u (absolute) and tap tables kidx[class][offset]
+    s += ", \"axes\": [";
+    for (int a = 0; a < 3; ++a) {
+      if (a) s += ", ";
+      s += "{\"u\": [";
+      for (int t = 0; t < pl.nU[a]; ++t) {
+        if (t) s += ", ";
+        append(s, "%lld", pl.u_rel[a][t] + pl.u_min[a]);
+      }
+      s += "], \"classes\": [";
+      for (int r = 0; r < pl.nRaxis[a]; ++r) {
+        if (r) s += ", ";
+        append(s, "%lld", pl.r_axis[a][r]);
+      }
+      s += "], \"kidx\": [";
+      for (int r = 0; r < pl.nRaxis[a]; ++r) {
+        if (r) s += ", ";
+        s += "[";
+        for (int t = 0; t < pl.nU[a]; ++t) {
+          if (t) s += ", ";
+          append(s, "%lld", pl.kidx[a][r][t]);
+        }
+        s += "]";
+      }
+      s += "]}";
+    }
+    s += "]";
+    append(s, ", \"epi\": %lld", pl.epi);
+    append(s, ", \"fused\": %lld", pl.fused);
+    append(s, ", \"nR\": %lld", pl.nR);
+    append(s, ", \"nEmpty\": %lld", pl.nEmpty);
+    append(s, ", \"fill_slab\": %lld", pl.fill_slab);
+    append(s, ", \"xslack\": %lld", pl.xslack);
+    append(s, ", \"ocb\": %lld", pl.ocb);
+    append(s, ", \"n_tile\": %lld", pl.n_tile);
+    append(s, ", \"n_colblocks\": %lld", pl.n_colblocks);
+    append(s, ", \"n_acc\": %lld", pl.n_acc);
+    append(s, ", \"dbuf\": %lld", pl.dbuf);
+    append(s, ", \"a_stages\": %lld", pl.a_stages);
+    append(s, ", \"tiles\": %lld", pl.tiles);
+    append(s, ", \"cin_chunk\": %lld", pl.cin_chunk);
+    append(s, ", \"n_chunks\": %lld", pl.n_chunks);
+    append(s, ", \"k_chunk\": %lld", pl.k_chunk);
+    append(s, ", \"ksteps_chunk\": %lld", pl.ksteps_chunk);
+    append(s, ", \"raw_stages\": %lld", pl.raw_stages);
+    append(s, ", \"raw_stage_bytes\": %lld", pl.raw_stage_bytes);
+    append(s, ", \"b_resident\": %lld", pl.b_resident);
+    append(s, ", \"b_stages\": %lld", pl.b_stages);
+    append(s, ", \"b_stage_bytes\": %lld", pl.b_stage_bytes);
+    append(s, ", \"smem_bytes\": %lld", pl.smem_bytes);
+    append(s, ", \"ws_total\": %lld", pl.ws_total);
+    append(s, ", \"y_elems\": %lld", pl.y_elems);
+  }
+  s += "}";
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tc3d_conv3d_fwd(const float* x, const float* w, const float* bias, float* y, int N, int Cin,
+                    int S0, int S1, int S2, int Cout, int k0, int k1, int k2, const int stride[3],
+                    const int pad[3], const int dilation[3], const int output_padding[3],
+                    int groups, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return run(OP_CONV, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout, k0, k1, k2,
+             stride, pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
+}
+
+int tc3d_conv_transpose3d_fwd(const float* x, const float* w, const float* bias, float* y, int N,
+                              int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                              const int stride[3], const int pad[3], const int dilation[3],
+                              const int output_padding[3], int groups, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  return run(OP_CONVT, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout, k0, k1,
+             k2, stride, pad, dilation, output_padding, groups, workspace, workspace_bytes,
+             stream);
+}
+
+int tc3d_conv_maxpool_lse_relu(const float* x, const float* w, const float* bias, float* y, int N,
+                               int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                               const int stride[3], const int pad[3], const int dilation[3],
+                               const int output_padding[3], int groups, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  return run(OP_CONV_POOL_LSE, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout,
+             k0, k1, k2, stride, pad, dilation, output_padding, groups, workspace,
+             workspace_bytes, stream);
+}
+
+int tc3d_convT_bn_avgpool(const float* x, const float* w, const float* bias, const float* gamma,
+                          const float* beta, float eps, float* y, int N, int Cin, int S0, int S1,
+                          int S2, int Cout, int k0, int k1, int k2, const int stride[3],
+                          const int pad[3], const int dilation[3], const int output_padding[3],
+                          int groups, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  return run(OP_CONVT_BN_POOL, x, w, bias, gamma, beta, eps, y, N, Cin, S0, S1, S2, Cout, k0, k1,
+             k2, stride, pad, dilation, output_padding, groups, workspace, workspace_bytes,
+             stream);
+}
+
+int tc3d_workspace_bytes(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
+                         int k2, const int stride[3], const int pad[3], const int dilation[3],
+                         const int output_padding[3], int groups, size_t* bytes) {
+  if (!bytes) return TC3D_ERR_NULL;
+  Plan pl;
+  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                    output_padding, groups, &pl);
+  if (rc) return rc;
+  *bytes = (size_t)pl.ws_total;
+  return TC3D_OK;
+}
+
+int tc3d_out_shape(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
+                   int k2, const int stride[3], const int pad[3], const int dilation[3],
+                   const int output_padding[3], int groups, int64_t out_dims[5]) {
+  if (!out_dims) return TC3D_ERR_NULL;
+  Plan pl;
+  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                    output_padding, groups, &pl);
+  if (rc) return rc;
+  out_dims[0] = N;
+  if (op == OP_CONV || op == OP_CONVT) {
+    out_dims[1] = Cout;
+    for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.O[a];
+  } else {
+    out_dims[1] = op == OP_CONV_POOL_LSE ? 1 : Cout;
+    for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.P[a];
+  }
+  return TC3D_OK;
+}
+
+int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
+                       int k2, const int stride[3], const int pad[3], const int dilation[3],
+                       const int output_padding[3], int groups, char* buf, size_t buflen) {
+  Plan pl;
+  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                    output_padding, groups, &pl);
+  if (rc == TC3D_ERR_NULL) pl.status = rc;
+  if (buf && buflen) {
+    std::string s = describe(pl);
+    size_t n = std::min(buflen - 1, s.size());
+    std::memcpy(buf, s.data(), n);
+    buf[n] = 0;
+  }
+  return rc;
+}
+
+int tc3d_last_device_error(cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TC3D_ERR_CUDA;
+  int flag = 0, zero = 0;
+  if (cudaMemcpy(&flag, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TC3D_ERR_CUDA;
+  if (flag && cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return TC3D_ERR_CUDA;
+  return flag ? TC3D_ERR_DEVICE_TIMEOUT : TC3D_OK;
+}
+
+void tc3d_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+int tc3d_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  if (wait_timeout_launch(d->err, timeout_ns, stream) != cudaSuccess) return TC3D_ERR_CUDA;
+  return tc3d_last_device_error(stream);
+}
+
+const char* tc3d_status_string(int status) {
+  switch (status) {
+    case TC3D_OK: return "ok";
+    case TC3D_ERR_NULL: return "a required pointer is NULL";
+    case TC3D_ERR_SHAPE: return "non-positive size or empty output";
+    case TC3D_ERR_GROUPS: return "channels not divisible by groups";
+    case TC3D_ERR_OUTPUT_PADDING: return "output_padding out of range";
+    case TC3D_ERR_ALIGN: return "misaligned pointer";
+    case TC3D_ERR_WORKSPACE: return "workspace missing or too small";
+    case TC3D_ERR_UNSUPPORTED: return "outside the implemented limits";
+    case TC3D_ERR_CUDA: return "CUDA runtime error";
+    case TC3D_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
+    case TC3D_ERR_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

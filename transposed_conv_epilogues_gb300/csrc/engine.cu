@@ -1,0 +1,1019 @@
+// engine.cu -- the implicit-GEMM convolution engine for sm_103a.
+//
+// One persistent CTA per SM walks its share of tiles.  A tile is n_acc
+// accumulators of 128 rows (see plan.cpp for what a row is); every
+// accumulator is a 128 x n_tile fp32 block in tensor memory (TMEM).  Per
+// tile, per column block and per channel chunk:
+//
+//   warp 0  (raw producer)   one TMA box load of the raw fp32 input region
+//                            the tile's rows read (zero fill = padding)
+//   warp 1  (B producer)     bulk copies of pre-packed weight K-steps
+//                            (resident in shared memory when they fit)
+//   warps 7..14 (conversion) gather, for each K-step of 8 (channel, tap)
+//                            pairs and each row, x and x - trunc_tf32(x) from
+//                            the raw box and store them to TMEM (A operand)
+//   warp 2  (MMA)            tcgen05.mma kind::tf32, A from TMEM, B from
+//                            shared memory: D += A.Bw + A.Blo + Alo.Bw
+//                            (3xTF32: the tensor core reads the top 19 bits
+//                            of each fp32 operand, so x itself is the "hi"
+//                            part and only the low parts are formed)
+//   warps 3..6 (epilogue)    tcgen05.ld of D and the fused epilogue
+//
+// Every mbarrier wait is bounded; on time-out the CTA sets an error word and
+// all roles return, TMEM is freed, the kernel exits.
+#include "engine.cuh"
+#include "ptx.cuh"
+
+namespace tc3d {
+
+// Set to 1 by any CTA whose bounded wait ran out; read and cleared by the host.
+__device__ int g_tc3d_error = 0;
+
+cudaError_t error_flag_address(int** addr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(addr), g_tc3d_error);
+}
+
+namespace {
+
+struct Bars {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t raw_full(int i) const { return base + 8u * i; }
+  __device__ __forceinline__ uint32_t raw_empty(int i) const { return base + 24u + 8u * i; }
+  __device__ __forceinline__ uint32_t b_full(int i) const { return base + 48u + 8u * i; }
+  __device__ __forceinline__ uint32_t b_empty(int i) const { return base + 176u + 8u * i; }
+  __device__ __forceinline__ uint32_t a_full(int i) const { return base + 304u + 8u * i; }
+  __device__ __forceinline__ uint32_t a_empty(int i) const { return base + 432u + 8u * i; }
+  __device__ __forceinline__ uint32_t d_full(int i) const { return base + 560u + 8u * i; }
+  __device__ __forceinline__ uint32_t d_empty(int i) const { return base + 576u + 8u * i; }
+  __device__ __forceinline__ uint32_t epi(int i) const { return base + 592u + 8u * i; }
+};
+constexpr unsigned kBarTmemSlot = 608;
+constexpr unsigned kBarAbort = 612;
+
+struct TileCoord {
+  int n;
+  int o[3];
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const EngineParams& p, int t) {
+  TileCoord c;
+  const int b2 = t % p.ntile[2];
+  t /= p.ntile[2];
+  const int b1 = t % p.ntile[1];
+  t /= p.ntile[1];
+  const int b0 = t % p.ntile[0];
+  c.n = t / p.ntile[0];
+  c.o[0] = b0 * p.T[0];
+  c.o[1] = b1 * p.T[1];
+  c.o[2] = b2 * p.T[2];
+  return c;
+}
+
+// local row coordinates of (accumulator a, lane quarter q, lane l)
+__device__ __forceinline__ void row_local(const EngineParams& p, int a, int q, int l, int (&t)[3]) {
+  const int j = a * 4 + q;
+  const int p0 = j / (p.Pq[1] * p.Pq[2]);
+  const int p1 = (j / p.Pq[2]) % p.Pq[1];
+  const int p2 = j % p.Pq[2];
+  const int l0 = l / (p.Q[1] * p.Q[2]);
+  const int l1 = (l / p.Q[2]) % p.Q[1];
+  const int l2 = l % p.Q[2];
+  t[0] = p0 * p.Q[0] + l0;
+  t[1] = p1 * p.Q[1] + l1;
+  t[2] = p2 * p.Q[2] + l2;
+}
+
+__device__ __forceinline__ void raise_abort(const EngineParams& p, volatile int* abortf) {
+  *abortf = 1;
+  atomicExch(p.err, 1);
+}
+
+__device__ __forceinline__ float tf32_trunc(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// Sum 16 values over all 32 lanes; lane ends with the total of value index
+// 8*b4 + 4*b3 + 2*b2 + b1 (b = lane bits).
+__device__ __forceinline__ float reduce_scatter16_sum(const float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = b4 ? v[i] : v[i + 8];
+    const float keep = b4 ? v[i + 8] : v[i];
+    w8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b3 ? w8[i] : w8[i + 4];
+    const float keep = b3 ? w8[i + 4] : w8[i];
+    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b2 ? w4[i] : w4[i + 2];
+    const float keep = b2 ? w4[i + 2] : w4[i];
+    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const float send = b1 ? w2[0] : w2[1];
+  const float keep = b1 ? w2[1] : w2[0];
+  const float w1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
+}
+
+// Reduce 16 values over the 8 lanes of a 2x2x2 pool window (lane bits 0, 3,
+// 4) with op; lane ends with 2 values of index 8*b0 + 4*b3 + 2*b4 + {0,1}.
+template <bool MAX>
+__device__ __forceinline__ void reduce_scatter16_window(const float (&v)[16], int lane,
+                                                        float (&out)[2]) {
+  float w8[8], w4[4];
+  const bool b0 = lane & 1, b3 = lane & 8, b4 = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = b0 ? v[i] : v[i + 8];
+    const float keep = b0 ? v[i + 8] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 1);
+    w8[i] = MAX ? fmaxf(keep, r) : keep + r;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b3 ? w8[i] : w8[i + 4];
+    const float keep = b3 ? w8[i + 4] : w8[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 8);
+    w4[i] = MAX ? fmaxf(keep, r) : keep + r;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b4 ? w4[i] : w4[i + 2];
+    const float keep = b4 ? w4[i + 2] : w4[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+    out[i] = MAX ? fmaxf(keep, r) : keep + r;
+  }
+}
+
+}  // namespace
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngineParams p) {
+  extern __shared__ uint8_t smem_dyn[];
+  const uint32_t s_unaligned = smem_u32(smem_dyn);
+  const uint32_t sbase = (s_unaligned + 1023u) & ~1023u;
+  uint8_t* gbase = smem_dyn + (sbase - s_unaligned);
+  const Bars bars{sbase + p.sm_bar};
+  volatile int* abortf = reinterpret_cast<volatile int*>(gbase + p.sm_bar + kBarAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + p.sm_bar + kBarTmemSlot);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t tmo = p.timeout_ns;
+
+  // ---------------- set-up ----------------
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxRawStages; ++i) {
+      mbar_init(bars.raw_full(i), 1);
+      mbar_init(bars.raw_empty(i), kNumConvWarps);
+    }
+    for (int i = 0; i < kMaxBStages; ++i) {
+      mbar_init(bars.b_full(i), 1);
+      mbar_init(bars.b_empty(i), 1);
+    }
+    for (int i = 0; i < kMaxAStages; ++i) {
+      mbar_init(bars.a_full(i), 4);
+      mbar_init(bars.a_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.d_full(i), 1);
+      mbar_init(bars.d_empty(i), kNumEpiWarps);
+      mbar_init(bars.epi(i), kNumEpiWarps);
+    }
+    *abortf = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(sbase + p.sm_bar + kBarTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpRaw && lane == 0 && p.use_tma) prefetch_tensormap(&p.xmap);
+  {
+    // GEMM-K table of one channel chunk: raw-box offset of (channel, tap) pair k
+    int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
+    const int bvol = p.box[0] * p.box[1] * p.box[2];
+    for (int k = threadIdx.x; k < p.ksteps_chunk * 8; k += kThreads) {
+      int off = 0;
+      if (k < p.k_chunk) {
+        const int c = k / p.nUtot, t = k % p.nUtot;
+        const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
+        off = c * bvol + (p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2];
+      }
+      ktab[k] = off;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int dcols = p.n_acc * p.n_tile;  // columns of one D buffer
+  const uint32_t a_col0 = (uint32_t)(p.dbuf * dcols);
+
+  // ================= raw-input producer =================
+  if (warp == kWarpRaw) {
+    const int bvol = p.box[0] * p.box[1] * p.box[2];
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+      if (*abortf) break;
+      const TileCoord tc = decode_tile(p, tile);
+      const int zc = p.s_in[0] * tc.o[0] + p.u_min[0];
+      const int yc = p.s_in[1] * tc.o[1] + p.u_min[1];
+      const int xc = (p.s_in[2] * tc.o[2] + p.u_min[2]) & ~3;
+      bool ok = true;
+      for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+        const int g = cb / p.nb_per_group;
+        for (int c = 0; c < p.n_chunks; ++c, ++it) {
+          const int stage = it % p.raw_stages;
+          ok = mbar_wait(bars.raw_empty(stage), ((it / p.raw_stages) & 1) ^ 1, tmo, abortf);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            if (lane == 0) raise_abort(p, abortf);
+            break;
+          }
+          const int ch0 = g * p.cin_g + c * p.cin_chunk;
+          const uint32_t dst = sbase + p.sm_raw + stage * p.raw_stage_bytes;
+          if (p.use_tma) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bars.raw_full(stage), (uint32_t)(p.cin_chunk * bvol * 4));
+              tma_load_5d(dst, &p.xmap, xc, yc, zc, ch0, tc.n, bars.raw_full(stage));
+            }
+          } else {
+            float* d = reinterpret_cast<float*>(gbase + p.sm_raw + stage * p.raw_stage_bytes);
+            const int total = p.cin_chunk * bvol;
+            const long long s12 = (long long)p.S[1] * p.S[2];
+            for (int e = lane; e < total; e += 32) {
+              int r = e;
+              const int i2 = r % p.box[2];
+              r /= p.box[2];
+              const int i1 = r % p.box[1];
+              r /= p.box[1];
+              const int i0 = r % p.box[0];
+              const int cl = r / p.box[0];
+              const int gx = xc + i2, gy = yc + i1, gz = zc + i0, ch = ch0 + cl;
+              float v = 0.f;
+              if (ch < p.C && gx >= 0 && gx < p.S[2] && gy >= 0 && gy < p.S[1] && gz >= 0 &&
+                  gz < p.S[0])
+                v = __ldg(p.x + (((long long)tc.n * p.C + ch) * p.S[0] + gz) * s12 +
+                          (long long)gy * p.S[2] + gx);
+              d[e] = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.raw_full(stage));
+          }
+        }
+      }
+      if (!ok) break;
+    }
+  }
+  // ================= weight producer =================
+  else if (warp == kWarpB) {
+    if (lane == 0) {
+      if (p.b_resident) {
+        mbar_arrive_expect_tx(bars.b_full(0), p.b_stages * p.b_stage_bytes);
+        for (int s = 0; s < p.b_stages; ++s)
+          bulk_g2s(sbase + p.sm_b + s * p.b_stage_bytes,
+                   p.wpack + (size_t)s * (p.b_stage_bytes / 4), p.b_stage_bytes, bars.b_full(0));
+      } else {
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+          for (int cb = 0; cb < p.n_colblocks && ok; ++cb)
+            for (int c = 0; c < p.n_chunks && ok; ++c)
+              for (int j = 0; j < p.ksteps_chunk; ++j, ++it) {
+                const int stage = it % p.b_stages;
+                if (!mbar_wait(bars.b_empty(stage), ((it / p.b_stages) & 1) ^ 1, tmo, abortf)) {
+                  raise_abort(p, abortf);
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(bars.b_full(stage), p.b_stage_bytes);
+                const size_t src =
+                    (((size_t)cb * p.n_chunks + c) * p.ksteps_chunk + j) * (p.b_stage_bytes / 4);
+                bulk_g2s(sbase + p.sm_b + stage * p.b_stage_bytes, p.wpack + src, p.b_stage_bytes,
+                         bars.b_full(stage));
+              }
+        }
+      }
+    }
+  }
+  // ================= MMA issuer =================
+  else if (warp == kWarpMMA) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_tf32(128, (uint32_t)p.n_tile);
+      const uint32_t lo_off = (uint32_t)p.n_tile * 32u;  // Blo follows Bw in a stage
+      bool ok = true;
+      if (p.b_resident) {
+        ok = mbar_wait(bars.b_full(0), 0, tmo, abortf);
+        if (!ok) raise_abort(p, abortf);
+      }
+      int it_k = 0, it_a = 0, it_d = 0;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
+          const int dslot = it_d % p.dbuf;
+          if (!mbar_wait(bars.d_empty(dslot), ((it_d / p.dbuf) & 1) ^ 1, tmo, abortf)) {
+            raise_abort(p, abortf);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_base = tmem_base + (uint32_t)(dslot * dcols);
+          bool first = true;
+          for (int c = 0; c < p.n_chunks && ok; ++c) {
+            for (int j = 0; j < p.ksteps_chunk; ++j, ++it_k) {
+              uint32_t b_addr;
+              int bstage = 0;
+              if (p.b_resident) {
+                b_addr = sbase + p.sm_b + (uint32_t)(c * p.ksteps_chunk + j) * p.b_stage_bytes;
+              } else {
+                bstage = it_k % p.b_stages;
+                if (!mbar_wait(bars.b_full(bstage), (it_k / p.b_stages) & 1, tmo, abortf)) {
+                  raise_abort(p, abortf);
+                  ok = false;
+                  break;
+                }
+                b_addr = sbase + p.sm_b + (uint32_t)bstage * p.b_stage_bytes;
+              }
+              const uint64_t bw = smem_desc_noswz(b_addr, 128, 256);
+              const uint64_t blo = smem_desc_noswz(b_addr + lo_off, 128, 256);
+              for (int a = 0; a < p.n_acc; ++a, ++it_a) {
+                const int as = it_a % p.a_stages;
+                if (!mbar_wait(bars.a_full(as), (it_a / p.a_stages) & 1, tmo, abortf)) {
+                  raise_abort(p, abortf);
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t a_tm = tmem_base + a_col0 + (uint32_t)as * 16u;
+                const uint32_t d_tm = d_base + (uint32_t)(a * p.n_tile);
+                mma_tf32_ts(d_tm, a_tm, bw, idesc, first ? 0u : 1u);  // x . w
+                mma_tf32_ts(d_tm, a_tm, blo, idesc, 1u);              // x . w_lo
+                mma_tf32_ts(d_tm, a_tm + 8, bw, idesc, 1u);           // x_lo . w
+                mma_commit(bars.a_empty(as));
+              }
+              if (!ok) break;
+              if (!p.b_resident) mma_commit(bars.b_empty(bstage));
+              first = false;
+            }
+          }
+          if (!ok) break;
+          mma_commit(bars.d_full(dslot));
+        }
+      }
+    }
+  }
+  // ================= conversion warps =================
+  else if (warp >= kWarpConv0) {
+    const int cw = warp - kWarpConv0;
+    const int half = cw >> 2;
+    const int q = warp & 3;
+    const int* ktab = reinterpret_cast<const int*>(gbase + p.sm_ktab);
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int it_raw = 0, it_a = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(p, tile);
+      const int xs = p.s_in[2] * tc.o[2] + p.u_min[2];
+      const int xshift = xs - (xs & ~3);
+      int row_off[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        int t[3];
+        row_local(p, a < p.n_acc ? a : 0, q, lane, t);
+        row_off[a] = ((p.s_in[0] * t[0]) * p.box[1] + p.s_in[1] * t[1]) * p.box[2] +
+                     p.s_in[2] * t[2] + xshift;
+      }
+      for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+        for (int c = 0; c < p.n_chunks && ok; ++c, ++it_raw) {
+          const int rstage = it_raw % p.raw_stages;
+          ok = mbar_wait(bars.raw_full(rstage), (it_raw / p.raw_stages) & 1, tmo, abortf);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            if (lane == 0) raise_abort(p, abortf);
+            break;
+          }
+          const float* raw =
+              reinterpret_cast<const float*>(gbase + p.sm_raw + rstage * p.raw_stage_bytes);
+          const int cin_valid = min(p.cin_chunk, p.cin_g - c * p.cin_chunk);
+          const int valid_k = cin_valid * p.nUtot;
+          for (int j = 0; j < p.ksteps_chunk && ok; ++j) {
+            const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
+            const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
+            const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+            const int kbase = j * 8;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              if (a >= p.n_acc) break;
+              const int s = it_a++;
+              if ((s & 1) != half) continue;
+              const int as = s % p.a_stages;
+              ok = mbar_wait(bars.a_empty(as), ((s / p.a_stages) & 1) ^ 1, tmo, abortf);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                if (lane == 0) raise_abort(p, abortf);
+                break;
+              }
+              tc_fence_after();
+              const float* rp = raw + row_off[a];
+              uint32_t v[16];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float xv = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
+                v[e] = __float_as_uint(xv);
+                v[8 + e] = __float_as_uint(xv - tf32_trunc(xv));
+              }
+              tmem_st16(tmem_base + lane_addr + a_col0 + (uint32_t)as * 16u, v);
+              tmem_wait_st();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bars.a_full(as));
+            }
+          }
+          __syncwarp();
+          if (ok && lane == 0) mbar_arrive(bars.raw_empty(rstage));
+        }
+      }
+    }
+  }
+  // ================= epilogue warps =================
+  else {
+    const int q = warp & 3;
+    const int ew = warp - kWarpEpi0;  // 0..3
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    const long long ovol = (long long)p.O[0] * p.O[1] * p.O[2];
+    const long long o12 = (long long)p.O[1] * p.O[2];
+    int it_d = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(p, tile);
+      // per accumulator: row coordinates of this lane
+      int m[4][3];
+      bool rvalid[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        int t[3];
+        row_local(p, a < p.n_acc ? a : 0, q, lane, t);
+        rvalid[a] = true;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          m[a][i] = tc.o[i] + t[i];
+          rvalid[a] = rvalid[a] && m[a][i] < p.M[i];
+        }
+      }
+      // pool-LSE running state per accumulator (channels this lane holds)
+      float lse_m[4], lse_s[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        lse_m[a] = -INFINITY;
+        lse_s[a] = 0.f;
+      }
+      for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
+        const int g = cb / p.nb_per_group, nb = cb % p.nb_per_group;
+        const int oc0 = g * p.cout_g + nb * p.ocb;
+        const int ocb_valid = min(p.ocb, p.cout_g - nb * p.ocb);
+        const int dslot = it_d % p.dbuf;
+        ok = mbar_wait(bars.d_full(dslot), (it_d / p.dbuf) & 1, tmo, abortf);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          if (lane == 0) raise_abort(p, abortf);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dbase = tmem_base + lane_addr + (uint32_t)(dslot * dcols);
+
+        if constexpr (EPI == EPI_STORE) {
+#pragma unroll 1
+          for (int a = 0; a < p.n_acc; ++a) {
+            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+            int mm[3];
+            bool rv = false;
+#pragma unroll
+            for (int aa = 0; aa < 4; ++aa)
+              if (aa == a) {
+                mm[0] = m[aa][0];
+                mm[1] = m[aa][1];
+                mm[2] = m[aa][2];
+                rv = rvalid[aa];
+              }
+            const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1], zb2 = p.s_out[2] * mm[2];
+            const long long ybase = (long long)tc.n * p.Cout * ovol + (long long)zb0 * o12 +
+                                    (long long)zb1 * p.O[2] + zb2;
+            const bool plain = p.nR == 1 && p.nEmpty == 0;
+            for (int cc = 0; cc < p.n_tile; cc += 16) {
+              uint32_t v[16];
+              tmem_ld16(taddr + (uint32_t)cc, v);
+              tmem_wait_ld();
+              if (!rv) continue;
+              if (plain) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                  const int oc_l = cc + jj;
+                  if (oc_l < ocb_valid) {
+                    const int oc = oc0 + oc_l;
+                    const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+                    p.y[ybase + (long long)oc * ovol] = __uint_as_float(v[jj]) + b;
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                  const int col = cc + jj;
+                  const int oc_l = col / p.nR, ri = col - oc_l * p.nR;
+                  if (oc_l < ocb_valid) {
+                    const int oc = oc0 + oc_l;
+                    const int ri2 = ri % p.nRaxis[2];
+                    const int ri1 = (ri / p.nRaxis[2]) % p.nRaxis[1];
+                    const int ri0 = ri / (p.nRaxis[1] * p.nRaxis[2]);
+                    const int r0 = p.r_axis[0][ri0], r1 = p.r_axis[1][ri1], r2 = p.r_axis[2][ri2];
+                    if (zb0 + r0 < p.O[0] && zb1 + r1 < p.O[1] && zb2 + r2 < p.O[2]) {
+                      const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+                      p.y[ybase + (long long)oc * ovol + (long long)r0 * o12 +
+                          (long long)r1 * p.O[2] + r2] = __uint_as_float(v[jj]) + b;
+                    }
+                  }
+                }
+                if (p.nEmpty > 0) {
+                  // classes without a tap hold the bias; each channel is written
+                  // by the chunk holding its last column
+                  for (int oc_l = cc / p.nR; oc_l * p.nR <= cc + 15; ++oc_l) {
+                    const int last = oc_l * p.nR + p.nR - 1;
+                    if (last < cc || last > cc + 15 || oc_l >= ocb_valid) continue;
+                    const int oc = oc0 + oc_l;
+                    const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+                    for (int r0 = 0; r0 < p.s_out[0]; ++r0)
+                      for (int r1 = 0; r1 < p.s_out[1]; ++r1)
+                        for (int r2 = 0; r2 < p.s_out[2]; ++r2) {
+                          if (((p.cls_mask[0] >> r0) & 1) && ((p.cls_mask[1] >> r1) & 1) &&
+                              ((p.cls_mask[2] >> r2) & 1))
+                            continue;
+                          if (zb0 + r0 < p.O[0] && zb1 + r1 < p.O[1] && zb2 + r2 < p.O[2])
+                            p.y[ybase + (long long)oc * ovol + (long long)r0 * o12 +
+                                (long long)r1 * p.O[2] + r2] = b;
+                        }
+                  }
+                }
+              }
+            }
+          }
+        } else if constexpr (EPI == EPI_POOL_LSE) {
+          // rows of a quarter are a 2x2x2 block of 2x2x8 positions: lanes
+          // {l, l^1, l^8, l^16} .. form one MaxPool3d(2) window
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            if (a >= p.n_acc) break;
+            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+            const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
+            for (int cc = 0; cc < p.n_tile; cc += 16) {
+              uint32_t u[16];
+              tmem_ld16(taddr + (uint32_t)cc, u);
+              tmem_wait_ld();
+              float v[16], mx[2];
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(u[jj]);
+              reduce_scatter16_window<true>(v, lane, mx);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int oc_l = cc + bsel + h;
+                if (oc_l < ocb_valid) {
+                  const float val = mx[h] + (p.bias ? __ldg(p.bias + oc0 + oc_l) : 0.f);
+                  const float nm = fmaxf(lse_m[a], val);
+                  lse_s[a] = lse_s[a] * expf(lse_m[a] - nm) + expf(val - nm);
+                  lse_m[a] = nm;
+                }
+              }
+            }
+          }
+          if (cb == p.n_colblocks - 1) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              if (a >= p.n_acc) break;
+              float mm = lse_m[a], ss = lse_s[a];
+#pragma unroll
+              for (int sh = 0; sh < 3; ++sh) {
+                const int x = sh == 0 ? 1 : (sh == 1 ? 8 : 16);
+                const float om = __shfl_xor_sync(0xffffffffu, mm, x);
+                const float os = __shfl_xor_sync(0xffffffffu, ss, x);
+                const float nm = fmaxf(mm, om);
+                ss = (ss > 0.f ? ss * expf(mm - nm) : 0.f) + (os > 0.f ? os * expf(om - nm) : 0.f);
+                mm = nm;
+              }
+              const int w0 = m[a][0] >> 1, w1 = m[a][1] >> 1, w2 = m[a][2] >> 1;
+              if ((lane & 0x19) == 0 && w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2]) {
+                const float l = mm + logf(ss);
+                p.y[(((long long)tc.n * p.P[0] + w0) * p.P[1] + w1) * p.P[2] + w2] = fmaxf(l, 0.f);
+              }
+            }
+          }
+        } else {  // EPI_BN_POOL: stride-2 transposed conv, 8 classes per row (oc-major columns)
+          float s1[16], s2[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            s1[i] = 0.f;
+            s2[i] = 0.f;
+          }
+          const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
+#pragma unroll 1
+          for (int a = 0; a < p.n_acc; ++a) {
+            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+            int mm[3];
+            bool rv = false;
+#pragma unroll
+            for (int aa = 0; aa < 4; ++aa)
+              if (aa == a) {
+                mm[0] = m[aa][0];
+                mm[1] = m[aa][1];
+                mm[2] = m[aa][2];
+                rv = rvalid[aa];
+              }
+            // class r = 4 r0 + 2 r1 + r2 lies inside the output iff 2m + r < O
+            uint32_t vmask = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const bool in = rv && 2 * mm[0] + (r >> 2) < p.O[0] &&
+                              2 * mm[1] + ((r >> 1) & 1) < p.O[1] && 2 * mm[2] + (r & 1) < p.O[2];
+              vmask |= (in ? 1u : 0u) << r;
+            }
+            float ps[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ps[i] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {  // 16 columns = 2 channels x 8 classes
+              if (cc * 16 >= p.n_tile) break;
+              uint32_t u[16];
+              tmem_ld16(taddr + (uint32_t)(cc * 16), u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                float sum = 0.f, a1 = 0.f, a2 = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const float v = __uint_as_float(u[h * 8 + r]);
+                  sum += v;
+                  const float vm = ((vmask >> r) & 1) ? v : 0.f;
+                  a1 += vm;
+                  a2 = fmaf(vm, vm, a2);
+                }
+                ps[2 * cc + h] = sum;
+                s1[2 * cc + h] += a1;
+                s2[2 * cc + h] += a2;
+              }
+            }
+            // pooled sums over the 8 rows of each 4x4x4 window
+            float pw[2];
+            reduce_scatter16_window<false>(ps, lane, pw);
+            const int w0 = mm[0] >> 1, w1 = mm[1] >> 1, w2 = mm[2] >> 1;
+            if (w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2]) {
+              // lanes of a window group hold different channel pairs
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int oc_l = bsel + h;
+                if (oc_l < ocb_valid) {
+                  const int oc = oc0 + oc_l;
+                  const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+                  p.y[(((long long)tc.n * p.Cout + oc) * p.P[0] + w0) * p.P[1] * p.P[2] +
+                      (long long)w1 * p.P[2] + w2] = pw[h] * (1.0f / 64.0f) + b;
+                }
+              }
+            }
+          }
+          // BatchNorm partial sums of this tile: all lanes, then all 4 warps
+          const float t1 = reduce_scatter16_sum(s1, lane);
+          const float t2 = reduce_scatter16_sum(s2, lane);
+          float2* red = reinterpret_cast<float2*>(gbase + p.sm_misc) + (it_d & 1) * 64;
+          const int idx = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
+                          ((lane >> 1) & 1);
+          if ((lane & 1) == 0) red[ew * 16 + idx] = make_float2(t1, t2);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.epi(it_d & 1));
+          if (ew == 0) {
+            ok = mbar_wait(bars.epi(it_d & 1), (it_d >> 1) & 1, tmo, abortf);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              if (lane == 0) raise_abort(p, abortf);
+              break;
+            }
+            if (lane < ocb_valid) {
+              float2 acc = red[lane];
+#pragma unroll
+              for (int w = 1; w < kNumEpiWarps; ++w) {
+                acc.x += red[w * 16 + lane].x;
+                acc.y += red[w * 16 + lane].y;
+              }
+              p.partials[(size_t)(oc0 + lane) * p.tiles + tile] = acc;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.d_empty(dslot));
+      }
+    }
+  }
+
+  // ---------------- tear-down ----------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMMA) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template __global__ void engine_kernel<EPI_STORE>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_POOL_LSE>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_BN_POOL>(const __grid_constant__ EngineParams p);
+
+// ---------------------------------------------------------------------------
+// weight pre-pack: W -> [colblock][chunk][kstep][w | w_lo][n_tile x 8] in the
+// tensor core's K-major, no-swizzle layout (8-row x 16-byte core matrices;
+// the two K-halves of a row group 128 bytes apart, row groups 256 apart).
+// ---------------------------------------------------------------------------
+__global__ void pack_weights_kernel(const __grid_constant__ PackParams p) {
+  const long long per_step = 2LL * p.n_tile * 8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.total;
+       i += (long long)gridDim.x * blockDim.x) {
+    long long r = i;
+    const int e = (int)(r % 8);
+    r /= 8;
+    const int nrow = (int)(r % p.n_tile);
+    r /= p.n_tile;
+    const int hl = (int)(r % 2);
+    r /= 2;
+    const int j = (int)(r % p.ksteps_chunk);
+    r /= p.ksteps_chunk;
+    const int c = (int)(r % p.n_chunks);
+    const int cb = (int)(r / p.n_chunks);
+    const int g = cb / p.nb_per_group, nb = cb % p.nb_per_group;
+    float w = 0.f;
+    const int oc_l = nrow / p.nR, ri = nrow % p.nR;
+    const int k = j * 8 + e;
+    const int c_l = k / p.nUtot, t = k % p.nUtot;
+    const int icl = c * p.cin_chunk + c_l;
+    const int ocg = nb * p.ocb + oc_l;  // output channel within the group
+    if (oc_l < p.ocb && ocg < p.cout_g && k < p.k_chunk && icl < p.cin_g) {
+      const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
+      const int ri0 = ri / (p.nRaxis[1] * p.nRaxis[2]), ri1 = (ri / p.nRaxis[2]) % p.nRaxis[1],
+                ri2 = ri % p.nRaxis[2];
+      const int k0 = p.kidx[0][ri0][t0], k1 = p.kidx[1][ri1][t1], k2 = p.kidx[2][ri2][t2];
+      if (k0 >= 0 && k1 >= 0 && k2 >= 0) {
+        const long long tap = ((long long)k0 * p.k[1] + k1) * p.k[2] + k2;
+        const long long kvol = (long long)p.k[0] * p.k[1] * p.k[2];
+        long long widx;
+        if (!p.transposed)  // [Cout, Cin/G, k]
+          widx = ((long long)(g * p.cout_g + ocg) * p.cin_g + icl) * kvol + tap;
+        else  // [Cin, Cout/G, k]
+          widx = ((long long)(g * p.cin_g + icl) * p.cout_g + ocg) * kvol + tap;
+        w = __ldg(p.w + widx);
+      }
+    }
+    const float v = hl == 0 ? w : w - __uint_as_float(__float_as_uint(w) & 0xFFFFE000u);
+    const long long blk = i / per_step;  // (cb, c, j) block
+    const int off = (nrow / 8) * 64 + (e / 4) * 32 + (nrow % 8) * 4 + (e % 4);
+    p.out[blk * per_step + (long long)hl * p.n_tile * 8 + off] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// BatchNorm finalize (second pass of the two-pass grid reduction)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void block_sum2(double& a, double& b) {
+  __shared__ double sa[256], sb[256];
+  sa[threadIdx.x] = a;
+  sb[threadIdx.x] = b;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) {
+      sa[threadIdx.x] += sa[threadIdx.x + s];
+      sb[threadIdx.x] += sb[threadIdx.x + s];
+    }
+    __syncthreads();
+  }
+  a = sa[0];
+  b = sb[0];
+}
+
+// partials of bias-free values per (channel, tile); mean adds the bias back
+__global__ void __launch_bounds__(256) bn_stats_f2_kernel(const float2* part, int nparts,
+                                                          const float* bias, const float* gamma,
+                                                          const float* beta, double count,
+                                                          float eps, int Cout, float2* stat) {
+  const int c = blockIdx.x;
+  double s1 = 0.0, s2 = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += 256) {
+    const float2 v = part[(size_t)c * nparts + i];
+    s1 += v.x;
+    s2 += v.y;
+  }
+  block_sum2(s1, s2);
+  if (threadIdx.x == 0) {
+    const double mean_a = s1 / count;
+    double var = s2 / count - mean_a * mean_a;
+    if (var < 0.0) var = 0.0;
+    const double mean = mean_a + (bias ? (double)bias[c] : 0.0);
+    const double g = gamma ? (double)gamma[c] : 1.0, be = beta ? (double)beta[c] : 0.0;
+    const double scale = g / sqrt(var + (double)eps);
+    stat[c] = make_float2((float)scale, (float)(be - mean * scale));
+  }
+}
+
+// unfused path: per (n, c) slice sums of the full transposed-conv output
+__global__ void __launch_bounds__(256) bn_slice_sums_kernel(const float* t, long long slice,
+                                                            float2* /*unused*/, double* out2) {
+  const float* s = t + (long long)blockIdx.x * slice;
+  double a = 0.0, b = 0.0;
+  for (long long i = threadIdx.x; i < slice; i += 256) {
+    const double v = s[i];
+    a += v;
+    b += v * v;
+  }
+  block_sum2(a, b);
+  if (threadIdx.x == 0) {
+    out2[2 * blockIdx.x] = a;
+    out2[2 * blockIdx.x + 1] = b;
+  }
+}
+
+// part2: [N][Cout] double pairs (slice order n-major)
+__global__ void __launch_bounds__(256) bn_stats_d2_kernel(const double* part2, int nparts,
+                                                          const float* gamma, const float* beta,
+                                                          double count, float eps, int Cout,
+                                                          float2* stat) {
+  const int c = blockIdx.x;
+  double s1 = 0.0, s2 = 0.0;
+  for (int n = threadIdx.x; n < nparts; n += 256) {
+    s1 += part2[2 * ((size_t)n * Cout + c)];
+    s2 += part2[2 * ((size_t)n * Cout + c) + 1];
+  }
+  block_sum2(s1, s2);
+  if (threadIdx.x == 0) {
+    const double mean = s1 / count;
+    double var = s2 / count - mean * mean;
+    if (var < 0.0) var = 0.0;
+    const double g = gamma ? (double)gamma[c] : 1.0, be = beta ? (double)beta[c] : 0.0;
+    const double scale = g / sqrt(var + (double)eps);
+    stat[c] = make_float2((float)scale, (float)(be - mean * scale));
+  }
+}
+
+__global__ void bn_apply_kernel(float* y, long long n, long long inner, int Cout,
+                                const float2* stat) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)((i / inner) % Cout);
+    const float2 s = stat[c];
+    y[i] = fmaf(y[i], s.x, s.y);
+  }
+}
+
+// unfused path: y = scale * mean of the 4x4x4 window + shift
+__global__ void bn_pool4_kernel(const float* t, float* y, int N, int Cout, int O0, int O1, int O2,
+                                int P0, int P1, int P2, const float2* stat) {
+  const long long total = (long long)N * Cout * P0 * P1 * P2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    long long r = i;
+    const int q2 = (int)(r % P2);
+    r /= P2;
+    const int q1 = (int)(r % P1);
+    r /= P1;
+    const int q0 = (int)(r % P0);
+    r /= P0;
+    const int c = (int)(r % Cout);
+    const float* s = t + r * (long long)O0 * O1 * O2;
+    float acc = 0.f;
+    for (int a = 0; a < 4; ++a)
+      for (int b = 0; b < 4; ++b)
+        for (int e = 0; e < 4; ++e)
+          acc += s[((long long)(4 * q0 + a) * O1 + (4 * q1 + b)) * O2 + 4 * q2 + e];
+    const float2 st = stat[c];
+    y[i] = fmaf(acc * (1.0f / 64.0f), st.x, st.y);
+  }
+}
+
+// three disjoint boxes: z0 >= zlo0 | z0 < zlo0, z1 >= zlo1 | z0 < zlo0, z1 < zlo1, z2 >= zlo2
+__global__ void fill_slab_kernel(float* y, const float* bias, int N, int Cout, int O0, int O1,
+                                 int O2, int zl0, int zl1, int zl2) {
+  const long long nA = (long long)(O0 - zl0) * O1 * O2;
+  const long long nB = (long long)zl0 * (O1 - zl1) * O2;
+  const long long nC = (long long)zl0 * zl1 * (O2 - zl2);
+  const long long per = nA + nB + nC;
+  const long long total = per * N * Cout;
+  const long long ovol = (long long)O0 * O1 * O2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long nc = i / per;
+    long long r = i % per;
+    int z0, z1, z2;
+    if (r < nA) {
+      z2 = (int)(r % O2);
+      r /= O2;
+      z1 = (int)(r % O1);
+      z0 = zl0 + (int)(r / O1);
+    } else if (r < nA + nB) {
+      r -= nA;
+      z2 = (int)(r % O2);
+      r /= O2;
+      z1 = zl1 + (int)(r % (O1 - zl1));
+      z0 = (int)(r / (O1 - zl1));
+    } else {
+      r -= nA + nB;
+      z2 = zl2 + (int)(r % (O2 - zl2));
+      r /= (O2 - zl2);
+      z1 = (int)(r % zl1);
+      z0 = (int)(r / zl1);
+    }
+    const int c = (int)(nc % Cout);
+    y[nc * ovol + ((long long)z0 * O1 + z1) * O2 + z2] = bias ? bias[c] : 0.f;
+  }
+}
+
+__global__ void wait_timeout_kernel(int* err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, timeout_ns, nullptr)) atomicExch(err, 1);
+}
+
+// ---------------------------------------------------------------------------
+// host-side launch wrappers
+// ---------------------------------------------------------------------------
+cudaError_t engine_set_smem(int epi, int bytes) {
+  switch (epi) {
+    case EPI_STORE:
+      return cudaFuncSetAttribute(engine_kernel<EPI_STORE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    case EPI_POOL_LSE:
+      return cudaFuncSetAttribute(engine_kernel<EPI_POOL_LSE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    default:
+      return cudaFuncSetAttribute(engine_kernel<EPI_BN_POOL>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  }
+}
+
+cudaError_t engine_launch(int epi, const EngineParams& p, unsigned grid, size_t smem,
+                          cudaStream_t st) {
+  switch (epi) {
+    case EPI_STORE:
+      engine_kernel<EPI_STORE><<<grid, kThreads, smem, st>>>(p);
+      break;
+    case EPI_POOL_LSE:
+      engine_kernel<EPI_POOL_LSE><<<grid, kThreads, smem, st>>>(p);
+      break;
+    default:
+      engine_kernel<EPI_BN_POOL><<<grid, kThreads, smem, st>>>(p);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t pack_launch(const PackParams& pp, unsigned blocks, cudaStream_t st) {
+  pack_weights_kernel<<<blocks, 256, 0, st>>>(pp);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_stats_f2_launch(const float2* part, int nparts, const float* bias,
+                               const float* gamma, const float* beta, double count, float eps,
+                               int Cout, float2* stat, cudaStream_t st) {
+  bn_stats_f2_kernel<<<Cout, 256, 0, st>>>(part, nparts, bias, gamma, beta, count, eps, Cout,
+                                           stat);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_apply_launch(float* y, long long n, long long inner, int Cout, const float2* stat,
+                            unsigned blocks, cudaStream_t st) {
+  bn_apply_kernel<<<blocks, 256, 0, st>>>(y, n, inner, Cout, stat);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N, int Cout,
+                              const int O[3], const int P[3], const float* gamma,
+                              const float* beta, float eps, float2* stat, unsigned blocks,
+                              cudaStream_t st) {
+  const long long slice = (long long)O[0] * O[1] * O[2];
+  bn_slice_sums_kernel<<<(unsigned)(N * Cout), 256, 0, st>>>(full, slice, nullptr, part2);
+  const double count = (double)N * (double)slice;
+  bn_stats_d2_kernel<<<Cout, 256, 0, st>>>(part2, N, gamma, beta, count, eps, Cout, stat);
+  bn_pool4_kernel<<<blocks, 256, 0, st>>>(full, y, N, Cout, O[0], O[1], O[2], P[0], P[1], P[2],
+                                          stat);
+  return cudaGetLastError();
+}
+
+cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
+                             const int zlo[3], unsigned blocks, cudaStream_t st) {
+  fill_slab_kernel<<<blocks, 256, 0, st>>>(y, bias, N, Cout, O[0], O[1], O[2], zlo[0], zlo[1],
+                                           zlo[2]);
+  return cudaGetLastError();
+}
+
+cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_ns, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace tc3d

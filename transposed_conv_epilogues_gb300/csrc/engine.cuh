@@ -1,0 +1,103 @@
+// engine.cuh -- launch parameters shared by the host launcher and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace tc3d {
+
+// Warp roles of the implicit-GEMM kernel (one CTA per SM, 15 warps).
+constexpr int kWarpRaw = 0;     // TMA (or plain-load) producer of raw input boxes
+constexpr int kWarpB = 1;       // bulk-copy producer of packed weight K-steps
+constexpr int kWarpMMA = 2;     // TMEM allocator + single-thread tcgen05.mma issuer
+constexpr int kWarpEpi0 = 3;    // 4 epilogue warps (TMEM lane quarter = warp % 4)
+constexpr int kNumEpiWarps = 4;
+constexpr int kWarpConv0 = 7;   // 8 conversion warps: raw fp32 -> (x, x - trunc(x)) in TMEM
+constexpr int kNumConvWarps = 8;
+constexpr int kNumWarps = 15;
+constexpr int kThreads = kNumWarps * 32;
+
+constexpr int kMaxRawStages = 3;
+constexpr int kMaxBStages = 16;
+constexpr int kMaxAStages = 16;
+
+struct EngineParams {
+  CUtensorMap xmap;  // 5-D map over x (dims S2, S1, S0, C, N), used when use_tma
+  const float* x;
+  const float* wpack;
+  const float* bias;
+  float* y;
+  float2* partials;  // BN-pool: [Cout][tiles] (sum, sum of squares) of bias-free values
+  int* err;
+  unsigned long long timeout_ns;
+  int use_tma;
+
+  int N, C, Cout, G, cin_g, cout_g;
+  int S[3];
+  int O[3];
+  int P[3];
+  int M[3], s_in[3], s_out[3], u_min[3];
+  int nU[3], nUtot;
+  int u_rel[3][kMaxAxisTaps];
+  int nR, nRaxis[3], nEmpty;
+  int r_axis[3][kMaxClassesAxis];
+  int cls_mask[3];  // per axis: bit r set iff class r has a tap
+
+  int ocb, n_tile, nb_per_group, n_colblocks;
+  int n_acc, dbuf, a_stages;
+  int Q[3], Pq[3], T[3], ntile[3];
+  int tiles;
+
+  int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
+  int box[3];
+  int raw_stages;
+  unsigned raw_stage_bytes;
+  int b_resident, b_stages;
+  unsigned b_stage_bytes;
+
+  // dynamic shared-memory layout (offsets from the 1024-aligned base)
+  unsigned sm_raw, sm_b, sm_ktab, sm_misc, sm_bar;
+};
+
+struct PackParams {
+  const float* w;
+  float* out;
+  int transposed;
+  int cin_g, cout_g;
+  int k[3];
+  int nUtot, nU[3];
+  int nR, nRaxis[3];
+  int kidx[3][kMaxClassesAxis][kMaxAxisTaps];
+  int ocb, n_tile, nb_per_group, n_colblocks;
+  int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
+  long long total;  // floats in the packed buffer
+};
+
+// host-side launch wrappers (engine.cu; kernels are launched from the
+// translation unit that defines them)
+cudaError_t engine_set_smem(int epi, int bytes);
+cudaError_t engine_launch(int epi, const EngineParams& p, unsigned grid, size_t smem,
+                          cudaStream_t st);
+cudaError_t pack_launch(const PackParams& pp, unsigned blocks, cudaStream_t st);
+cudaError_t bn_stats_f2_launch(const float2* part, int nparts, const float* bias,
+                               const float* gamma, const float* beta, double count, float eps,
+                               int Cout, float2* stat, cudaStream_t st);
+cudaError_t bn_apply_launch(float* y, long long n, long long inner, int Cout, const float2* stat,
+                            unsigned blocks, cudaStream_t st);
+cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N, int Cout,
+                              const int O[3], const int P[3], const float* gamma,
+                              const float* beta, float eps, float2* stat, unsigned blocks,
+                              cudaStream_t st);
+// bias (or 0) into the outputs at z_a >= zlo[a] for any axis a (outputs of
+// rows past the GEMM row grid; all of them in classes without taps)
+cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
+                             const int zlo[3], unsigned blocks, cudaStream_t st);
+cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_ns, cudaStream_t st);
+
+// device address of the library's error word on the current device
+cudaError_t error_flag_address(int** addr);
+
+}  // namespace tc3d

@@ -1,0 +1,387 @@
+// plan.cpp -- host-side planning for the implicit-GEMM engine.
+//
+// The convolution and the transposed convolution are both cast as one GEMM
+// over "rows".  For a convolution a row is an output position o; its GEMM-K
+// entries are (input channel, tap) pairs read at input position
+// o*stride - pad + dilation*k (direct-convolution formula of the page
+// "Kimi-K2.6 l1_p59").  For a transposed convolution a row is a block of
+// stride^3 outputs z = stride*m + r, one per output-parity class r.  For a
+// fixed class r along an axis, tap k contributes iff (r + p - d*k) is a
+// multiple of s, and then reads input m + (r + p - d*k)/s ("Kimi-K2.6
+// l1_p77", receive-form derivation; "Kimi-K2.6 l2_p72", per-position tap
+// table).  So every class is a dense stride-1 sub-convolution over m, and
+// all classes of a row read inputs m + u for u in the union U of their
+// offsets.  The GEMM-N axis holds (output channel, non-empty class) pairs;
+// the packed weight of pair (class r, offset u) is W[k] with
+// k = (r + p - s*u)/d when that is an integer tap, else 0.  No zero-inserted
+// input is ever formed.
+#include "plan.h"
+
+#include <algorithm>
+#include <cstring>
+
+#include "../../include/tc3d.h"
+
+namespace tc3d {
+
+static int64_t floor_div(int64_t a, int64_t b) {
+  int64_t q = a / b;
+  if ((a % b != 0) && ((a < 0) != (b < 0))) --q;
+  return q;
+}
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+int64_t conv_len(int64_t L, int k, int s, int p, int d) {
+  if (L <= 0 || k <= 0 || s <= 0 || p < 0 || d <= 0) return 0;
+  int64_t span = L + 2 * (int64_t)p - (int64_t)d * (k - 1) - 1;
+  if (span < 0) return 0;
+  return span / s + 1;
+}
+
+int64_t convT_len(int64_t L, int k, int s, int p, int d, int op) {
+  if (L <= 0 || k <= 0 || s <= 0 || p < 0 || d <= 0 || op < 0) return 0;
+  int64_t o = (L - 1) * s - 2 * (int64_t)p + (int64_t)d * (k - 1) + op + 1;
+  return o > 0 ? o : 0;
+}
+
+static int validate(const Problem& pb, bool transposed) {
+  if (pb.N <= 0 || pb.Cin <= 0 || pb.Cout <= 0) return TC3D_ERR_SHAPE;
+  for (int a = 0; a < 3; ++a) {
+    if (pb.S[a] <= 0 || pb.k[a] <= 0 || pb.stride[a] <= 0 || pb.dil[a] <= 0 || pb.pad[a] < 0)
+      return TC3D_ERR_SHAPE;
+  }
+  if (pb.groups <= 0 || pb.Cin % pb.groups || pb.Cout % pb.groups) return TC3D_ERR_GROUPS;
+  for (int a = 0; a < 3; ++a) {
+    if (!transposed) {
+      if (pb.out_pad[a] != 0) return TC3D_ERR_OUTPUT_PADDING;
+    } else {
+      if (pb.out_pad[a] < 0 || pb.out_pad[a] >= std::max(pb.stride[a], pb.dil[a]))
+        return TC3D_ERR_OUTPUT_PADDING;
+    }
+  }
+  return TC3D_OK;
+}
+
+// largest x misalignment (in elements, 0..3) of the raw box start
+// s_in2 * T2 * b + u_min2 over tiles b; the start is rounded down to 16 bytes
+static int x_slack(const Plan& pl, int t2) {
+  int mx = 0;
+  for (int b = 0; b < 4; ++b) {
+    int64_t v = (int64_t)pl.s_in[2] * t2 * b + pl.u_min[2];
+    mx = std::max(mx, (int)(((v % 4) + 4) % 4));
+  }
+  return mx;
+}
+
+// per-axis raw-box extent for a tile extent t (rows)
+static int box_extent(const Plan& pl, int a, int t) {
+  int64_t e = (int64_t)pl.s_in[a] * (t - 1) + (pl.u_max[a] - pl.u_min[a]) + 1;
+  if (a == 2) e = round_up(e + x_slack(pl, t), 4);
+  return (int)std::min<int64_t>(e, 1 << 30);
+}
+
+static int ilog2(int v) {
+  int r = 0;
+  while ((1 << (r + 1)) <= v) ++r;
+  return r;
+}
+
+SmemLayout smem_layout(const Plan& pl) {
+  SmemLayout L;
+  L.raw = 0;
+  L.b = L.raw + (int64_t)pl.raw_stages * pl.raw_stage_bytes;
+  L.ktab = L.b + (int64_t)pl.b_stages * pl.b_stage_bytes;
+  L.misc = L.ktab + round_up((int64_t)pl.ksteps_chunk * 32, 1024);
+  L.bar = L.misc + 4096;
+  // + 1024 for the barriers and 1024 of slack to align the dynamic base
+  L.total = L.bar + 1024 + 1024;
+  // one CTA per SM: the kernel owns all 512 TMEM columns
+  L.total = std::max<int64_t>(L.total, 120 * 1024);
+  return L;
+}
+
+int make_plan(const Problem& pb_in, Plan* out) {
+  Plan pl;
+  std::memset(&pl, 0, sizeof(pl));
+  pl.pb = pb_in;
+  const Problem& pb = pl.pb;
+  const bool transposed = pb.op == OP_CONVT || pb.op == OP_CONVT_BN_POOL;
+  pl.transposed = transposed;
+  pl.status = TC3D_OK;
+  auto fail = [&](int st) {
+    pl.status = st;
+    *out = pl;
+    return st;
+  };
+  if (pb.op < OP_CONV || pb.op > OP_CONVT_BN_POOL) return fail(TC3D_ERR_UNSUPPORTED);
+  int st = validate(pb, transposed);
+  if (st) return fail(st);
+  pl.cin_g = pb.Cin / pb.groups;
+  pl.cout_g = pb.Cout / pb.groups;
+
+  // ---- output and pooled extents
+  for (int a = 0; a < 3; ++a) {
+    pl.O[a] = transposed ? convT_len(pb.S[a], pb.k[a], pb.stride[a], pb.pad[a], pb.dil[a],
+                                     pb.out_pad[a])
+                         : conv_len(pb.S[a], pb.k[a], pb.stride[a], pb.pad[a], pb.dil[a]);
+    if (pl.O[a] <= 0) return fail(TC3D_ERR_SHAPE);
+    if (pl.O[a] > (1 << 30)) return fail(TC3D_ERR_UNSUPPORTED);
+  }
+  int64_t ovol = pl.O[0] * pl.O[1] * pl.O[2];
+  if (pb.op == OP_CONV || pb.op == OP_CONVT) {
+    pl.y_elems = (int64_t)pb.N * pb.Cout * ovol;
+    pl.epi = EPI_STORE;
+  } else if (pb.op == OP_CONV_POOL_LSE) {
+    for (int a = 0; a < 3; ++a) {
+      pl.P[a] = pl.O[a] / 2;
+      if (pl.P[a] <= 0) return fail(TC3D_ERR_SHAPE);
+    }
+    pl.y_elems = (int64_t)pb.N * pl.P[0] * pl.P[1] * pl.P[2];
+    pl.epi = EPI_POOL_LSE;
+  } else {
+    for (int a = 0; a < 3; ++a) {
+      pl.P[a] = pl.O[a] / 2 / 2;
+      if (pl.P[a] <= 0) return fail(TC3D_ERR_SHAPE);
+    }
+    pl.y_elems = (int64_t)pb.N * pb.Cout * pl.P[0] * pl.P[1] * pl.P[2];
+    pl.epi = EPI_STORE;  // decided below, once the parity classes are known
+  }
+  if (pl.y_elems <= 0) return fail(TC3D_ERR_SHAPE);
+  for (int a = 0; a < 3; ++a)
+    if (pb.k[a] > kMaxAxisTaps) return fail(TC3D_ERR_UNSUPPORTED);
+  if ((int64_t)pb.N * pb.Cin * pb.S[0] * pb.S[1] * pb.S[2] >= ((int64_t)1 << 40) ||
+      (int64_t)pb.N * pb.Cout * ovol >= ((int64_t)1 << 40))
+    return fail(TC3D_ERR_UNSUPPORTED);
+
+  // ---- rows, offsets, classes
+  for (int a = 0; a < 3; ++a) {
+    const int s = pb.stride[a], p = pb.pad[a], d = pb.dil[a], K = pb.k[a];
+    if (!transposed) {
+      pl.s_in[a] = s;
+      pl.s_out[a] = 1;
+      pl.M[a] = (int)pl.O[a];
+      pl.nU[a] = K;
+      pl.u_min[a] = -p;
+      pl.u_max[a] = d * (K - 1) - p;
+      for (int t = 0; t < K; ++t) pl.u_rel[a][t] = d * t;
+      pl.nRaxis[a] = 1;
+      pl.r_axis[a][0] = 0;
+      for (int t = 0; t < kMaxAxisTaps; ++t) pl.kidx[a][0][t] = t < K ? t : -1;
+    } else {
+      if (s > kMaxClassesAxis) return fail(TC3D_ERR_UNSUPPORTED);
+      pl.s_in[a] = 1;
+      pl.s_out[a] = s;
+      // union of offsets u = (r + p - d k)/s over all classes and taps
+      int uvals[kMaxClassesAxis * kMaxAxisTaps];
+      int nu = 0;
+      for (int r = 0; r < s; ++r)
+        for (int k = 0; k < K; ++k) {
+          int64_t t = (int64_t)r + p - (int64_t)d * k;
+          if (((t % s) + s) % s != 0) continue;
+          int u = (int)(t / s);
+          bool seen = false;
+          for (int i = 0; i < nu; ++i) seen |= uvals[i] == u;
+          if (!seen) uvals[nu++] = u;
+        }
+      std::sort(uvals, uvals + nu);
+      if (nu > kMaxAxisTaps) return fail(TC3D_ERR_UNSUPPORTED);
+      pl.nU[a] = nu;
+      pl.u_min[a] = uvals[0];
+      pl.u_max[a] = uvals[nu - 1];
+      for (int t = 0; t < nu; ++t) pl.u_rel[a][t] = uvals[t] - uvals[0];
+      int nr = 0;
+      for (int r = 0; r < s; ++r) {
+        int row[kMaxAxisTaps];
+        bool any = false;
+        for (int t = 0; t < kMaxAxisTaps; ++t) row[t] = -1;
+        for (int t = 0; t < nu; ++t) {
+          int64_t num = (int64_t)r + p - (int64_t)s * uvals[t];
+          if (num % d != 0) continue;
+          int64_t k = num / d;
+          if (k < 0 || k >= K) continue;
+          row[t] = (int)k;
+          any = true;
+        }
+        if (!any) continue;
+        pl.r_axis[a][nr] = r;
+        for (int t = 0; t < kMaxAxisTaps; ++t) pl.kidx[a][nr][t] = row[t];
+        ++nr;
+      }
+      pl.nRaxis[a] = nr;  // >= 1: class (d*k - p) mod s always has tap k
+      // rows m whose outputs s*m + r (r a class with taps) lie inside the output
+      int64_t mrows = 0;
+      for (int i = 0; i < nr; ++i)
+        mrows = std::max<int64_t>(mrows, ceil_div(pl.O[a] - pl.r_axis[a][i], s));
+      pl.M[a] = (int)mrows;
+      if (mrows * s < pl.O[a]) pl.fill_slab = 1;
+    }
+  }
+  pl.nR = pl.nRaxis[0] * pl.nRaxis[1] * pl.nRaxis[2];
+  if (pb.op == OP_CONVT_BN_POOL) {
+    // fused BatchNorm + 4x4x4 pooling: a row is a 2x2x2 output block with all
+    // 8 parity classes carrying taps, so a 4^3 window is 2x2x2 rows
+    pl.fused = pb.stride[0] == 2 && pb.stride[1] == 2 && pb.stride[2] == 2 && pl.nR == 8;
+    pl.epi = pl.fused ? EPI_BN_POOL : EPI_STORE;
+  }
+  pl.nEmpty = pl.s_out[0] * pl.s_out[1] * pl.s_out[2] - pl.nR;
+  if (pl.nR > 128) return fail(TC3D_ERR_UNSUPPORTED);
+  const int nUtot = pl.nU[0] * pl.nU[1] * pl.nU[2];
+
+  // ---- GEMM N (column blocks)
+  {
+    int cap = pl.epi == EPI_POOL_LSE ? 256 : 128;
+    pl.ocb = std::max(1, std::min(pl.cout_g, cap / pl.nR));
+    pl.n_tile = (int)round_up((int64_t)pl.ocb * pl.nR, 16);
+    if (pl.n_tile > 256) return fail(TC3D_ERR_UNSUPPORTED);
+    pl.nb_per_group = (int)ceil_div(pl.cout_g, pl.ocb);
+    pl.n_colblocks = pb.groups * pl.nb_per_group;
+  }
+
+  // ---- accumulators per tile, TMEM budget
+  if (pl.epi == EPI_POOL_LSE) {
+    pl.dbuf = 1;
+    pl.n_acc = std::max(1, std::min(4, 256 / pl.n_tile));
+  } else {
+    pl.dbuf = pl.n_tile <= 128 ? 2 : 1;
+    pl.n_acc = std::max(1, std::min(4, 256 / (pl.dbuf * pl.n_tile)));
+  }
+  {
+    int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
+    pl.a_stages = std::min(16, (kTmemCols - dcols) / 16);
+    if (pl.a_stages < 4) return fail(TC3D_ERR_UNSUPPORTED);
+  }
+
+  // ---- quarter box Q and quarter arrangement P (search)
+  {
+    const int nq = 4 * pl.n_acc;
+    const int lq = ilog2(nq);
+    double best = 1e300;
+    int bestQ[3] = {0, 0, 0}, bestP[3] = {0, 0, 0};
+    for (int q2 = 0; q2 <= 5; ++q2)
+      for (int q1 = 0; q1 + q2 <= 5; ++q1) {
+        int q0 = 5 - q1 - q2;
+        int Q[3] = {1 << q0, 1 << q1, 1 << q2};
+        if (pl.epi != EPI_STORE && !(Q[0] == 2 && Q[1] == 2 && Q[2] == 8)) continue;
+        for (int p2 = 0; p2 <= lq; ++p2)
+          for (int p1 = 0; p1 + p2 <= lq; ++p1) {
+            int p0 = lq - p1 - p2;
+            int P[3] = {1 << p0, 1 << p1, 1 << p2};
+            int T[3];
+            bool ok = true;
+            double rows = 1;
+            for (int a = 0; a < 3; ++a) {
+              T[a] = P[a] * Q[a];
+              rows *= (double)round_up(pl.M[a], T[a]);
+              int be = box_extent(pl, a, T[a]);
+              if (be > 256) ok = false;
+            }
+            if (!ok) continue;
+            double raw = (double)box_extent(pl, 0, T[0]) * box_extent(pl, 1, T[1]) *
+                         box_extent(pl, 2, T[2]);
+            double per_row = raw / (128.0 * pl.n_acc);
+            double cost = rows * (1.0 + 0.04 * per_row);
+            if (pl.epi == EPI_STORE) {
+              // bytes a warp stores contiguously per (channel, class row)
+              int64_t seg = (int64_t)Q[2] * pl.s_out[2];
+              if (Q[2] == pl.M[2] && pl.s_out[2] == 1 && pl.M[2] == pl.O[2]) {
+                seg *= Q[1];
+                if (Q[1] == pl.M[1] && pl.s_out[1] == 1 && pl.M[1] == pl.O[1]) seg *= Q[0];
+              }
+              const double segb = (double)std::min<int64_t>(seg * 4, 128);
+              cost *= 1.0 + 0.25 * (128.0 / segb - 1.0);
+            }
+            if (cost < best) {
+              best = cost;
+              for (int a = 0; a < 3; ++a) {
+                bestQ[a] = Q[a];
+                bestP[a] = P[a];
+              }
+            }
+          }
+      }
+    if (best >= 1e300) return fail(TC3D_ERR_UNSUPPORTED);
+    for (int a = 0; a < 3; ++a) {
+      pl.Q[a] = bestQ[a];
+      pl.Pq[a] = bestP[a];
+      pl.T[a] = bestQ[a] * bestP[a];
+      pl.ntile[a] = (int)ceil_div(pl.M[a], pl.T[a]);
+      pl.box[a] = box_extent(pl, a, pl.T[a]);
+    }
+    pl.xslack = x_slack(pl, pl.T[2]);
+    pl.tiles = (int64_t)pb.N * pl.ntile[0] * pl.ntile[1] * pl.ntile[2];
+    if (pl.tiles >= ((int64_t)1 << 31)) return fail(TC3D_ERR_UNSUPPORTED);
+  }
+
+  // ---- channel chunk, smem budget
+  {
+    const int64_t bvol = (int64_t)pl.box[0] * pl.box[1] * pl.box[2];
+    const int64_t raw_ch = bvol * 4;
+    const int64_t bstage = 64LL * pl.n_tile;  // w + w_lo, n_tile x 8 tf32 each
+    const int64_t fixed = 4096 + 1024 + 1024; // epilogue scratch, barriers, alignment
+    int best_cc = 0;
+    int64_t best_steps = INT64_MAX;
+    int max_cc = std::min(pl.cin_g, kMaxKChunk / nUtot);
+    if (max_cc < 1) return fail(TC3D_ERR_UNSUPPORTED);
+    for (int cc = 1; cc <= max_cc; ++cc) {
+      int64_t need = 2 * round_up(cc * raw_ch, 1024) + 4 * bstage + fixed +
+                     round_up(ceil_div((int64_t)cc * nUtot, 8) * 32, 1024);
+      if (need > kMaxSmem) break;
+      if (cc * raw_ch > 64 * 1024 && cc > 1) break;  // keep one stage modest
+      int64_t steps = ceil_div(pl.cin_g, cc) * ceil_div((int64_t)cc * nUtot, 8);
+      if (steps <= best_steps) {
+        best_steps = steps;
+        best_cc = cc;
+      }
+    }
+    if (best_cc == 0) return fail(TC3D_ERR_UNSUPPORTED);
+    pl.cin_chunk = best_cc;
+    pl.n_chunks = (int)ceil_div(pl.cin_g, best_cc);
+    pl.k_chunk = best_cc * nUtot;
+    pl.ksteps_chunk = (int)ceil_div(pl.k_chunk, 8);
+    pl.raw_stage_bytes = round_up(best_cc * raw_ch, 1024);
+    const int64_t ktab = round_up((int64_t)pl.ksteps_chunk * 32, 1024);
+    const int64_t total_ksteps = (int64_t)pl.n_chunks * pl.ksteps_chunk;
+    pl.b_stage_bytes = bstage;
+    const int64_t rem = kMaxSmem - fixed - ktab - 2 * pl.raw_stage_bytes;
+    if (pl.n_colblocks == 1 && total_ksteps * bstage <= std::min<int64_t>(rem, 112 * 1024)) {
+      pl.b_resident = 1;
+      pl.b_stages = (int)total_ksteps;
+    } else {
+      pl.b_resident = 0;
+      pl.b_stages = (int)std::min<int64_t>(kMaxBStagesPlan, rem / bstage);
+      if (pl.b_stages < 2) return fail(TC3D_ERR_UNSUPPORTED);
+    }
+    const int64_t used = (int64_t)pl.b_stages * bstage + ktab + fixed;
+    pl.raw_stages = (used + 3 * pl.raw_stage_bytes <= kMaxSmem) ? 3 : 2;
+    pl.smem_bytes = smem_layout(pl).total;
+    if (pl.smem_bytes > kMaxSmem) return fail(TC3D_ERR_UNSUPPORTED);
+  }
+
+  // ---- workspace
+  {
+    int64_t off = 0;
+    pl.ws_wpack_off = off;
+    pl.ws_wpack_bytes =
+        (int64_t)pl.n_colblocks * pl.n_chunks * pl.ksteps_chunk * pl.b_stage_bytes;
+    off = round_up(off + pl.ws_wpack_bytes, 256);
+    if (pb.op == OP_CONVT_BN_POOL) {
+      pl.ws_part_off = off;
+      pl.ws_part_bytes = pl.fused ? pl.tiles * pb.Cout * 8 : (int64_t)pb.N * pb.Cout * 16;
+      off = round_up(off + pl.ws_part_bytes, 256);
+      pl.ws_stat_off = off;
+      pl.ws_stat_bytes = (int64_t)pb.Cout * 8;
+      off = round_up(off + pl.ws_stat_bytes, 256);
+      if (!pl.fused) {
+        pl.ws_full_off = off;
+        pl.ws_full_bytes = (int64_t)pb.N * pb.Cout * ovol * 4;
+        off = round_up(off + pl.ws_full_bytes, 256);
+      }
+    }
+    pl.ws_total = std::max<int64_t>(off, 256);
+  }
+  *out = pl;
+  return TC3D_OK;
+}
+
+}  // namespace tc3d

@@ -1,0 +1,110 @@
+// plan.h -- host-side planning for the implicit-GEMM engine (pure integer
+// code, no CUDA): output sizes, argument validation, the transposed
+// convolution's output-parity classes and tap tables, tile shapes and the
+// shared/tensor-memory budget of one launch.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace tc3d {
+
+enum OpKind : int {
+  OP_CONV = 0,             // conv3d_fwd
+  OP_CONVT = 1,            // conv_transpose3d_fwd
+  OP_CONV_POOL_LSE = 2,    // conv_maxpool_lse_relu
+  OP_CONVT_BN_POOL = 3,    // convT_bn_avgpool
+};
+
+enum EpiKind : int {
+  EPI_STORE = 0,     // bias add + store every output (all parity classes)
+  EPI_POOL_LSE = 1,  // MaxPool3d(2) + channel logsumexp + ReLU
+  EPI_BN_POOL = 2,   // 4x4x4 pooled sums + per-tile BatchNorm partial sums
+};
+
+constexpr int kMaxAxisTaps = 16;    // per-axis kernel extent limit
+constexpr int kMaxClassesAxis = 8;  // per-axis stride limit of a transposed conv
+constexpr int kMaxKChunk = 1024;    // GEMM-K values staged per channel chunk
+constexpr int kMaxBStagesPlan = 16; // streamed weight stages (mbarrier pairs in the kernel)
+constexpr int kTmemCols = 512;
+constexpr int kMaxSmem = 227 * 1024;
+
+struct Problem {
+  int op;
+  int N, Cin, S[3], Cout, k[3], stride[3], pad[3], dil[3], out_pad[3], groups;
+};
+
+// Everything a launch needs, derived from a Problem.  Row space: for every
+// batch n a grid M0 x M1 x M2 of "rows"; row m reads input positions
+// s_in*m + u (u in the per-axis offset lists) and produces outputs
+// s_out*m + r for every parity class r (s_out = 1, one class, for a conv).
+struct Plan {
+  int status;  // 0 or a negative TC3D_ERR_* code
+  Problem pb;
+  int transposed;
+  int64_t O[3];   // conv / transposed-conv output extents
+  int64_t P[3];   // pooled extents (pool-LSE: O/2, BN-pool: O/2/2)
+  int64_t y_elems;
+  int cin_g, cout_g;
+  int epi;        // EpiKind of the main launch
+  int fused;      // 0: convT_bn_avgpool runs through the unfused fallback
+
+  // rows and taps
+  int M[3], s_in[3], s_out[3];
+  int nU[3];                  // union of input offsets per axis
+  int u_rel[3][kMaxAxisTaps]; // offset - u_min
+  int u_min[3], u_max[3];
+  // parity classes (transposed conv): per axis the classes with >= 1 tap
+  int nRaxis[3];
+  int r_axis[3][kMaxClassesAxis];                    // class value r of index ri
+  int kidx[3][kMaxClassesAxis][kMaxAxisTaps];        // kernel tap of (ri, offset t), or -1
+  int nR;                                            // non-empty classes (product set)
+  int nEmpty;                                        // classes with no tap (bias only)
+  // outputs at z_a >= s_out*M (all of them in tap-less classes) are written
+  // by a separate bias fill; fill_slab says whether any exist
+  int fill_slab;
+
+  // GEMM N: per column block ocb output channels x nR classes, oc-major
+  int ocb, n_tile, nb_per_group, n_colblocks;
+
+  // tiles: a tile is n_acc accumulators of 128 rows; each 32-row quarter is a
+  // box Q0 x Q1 x Q2, quarters are arranged P0 x P1 x P2 -> tile T = P*Q
+  int n_acc, dbuf, a_stages;
+  int Q[3], Pq[3], T[3];
+  int ntile[3];
+  int xslack;       // max misalignment (elements) of a raw box's x start
+  int64_t tiles;
+
+  // channel chunks and raw input box
+  int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
+  int box[3];        // B0, B1, B2 (B2 multiple of 4)
+  int raw_stages;
+  int64_t raw_stage_bytes;
+  int b_resident;    // 1: whole packed weight block stays in smem
+  int b_stages;
+  int64_t b_stage_bytes;
+  int64_t smem_bytes;
+
+  // workspace (bytes, each region 256-aligned)
+  int64_t ws_wpack_off, ws_wpack_bytes;
+  int64_t ws_part_off, ws_part_bytes;   // BN partials: fused [Cout][tiles] float2, else [N][Cout] double2
+  int64_t ws_stat_off, ws_stat_bytes;   // BN scale/shift [Cout] float2
+  int64_t ws_full_off, ws_full_bytes;   // unfused fallback: full convT output
+  int64_t ws_total;
+};
+
+// Shared-memory layout of the main kernel (byte offsets from a 1024-aligned
+// base): raw input stages, weight stages, GEMM-K offset table, epilogue
+// scratch (4 KB), mbarriers (1 KB).  Returns the dynamic smem request.
+struct SmemLayout {
+  int64_t raw, b, ktab, misc, bar, total;
+};
+SmemLayout smem_layout(const Plan& pl);
+
+// Fill *plan for problem pb.  Returns plan->status.
+int make_plan(const Problem& pb, Plan* plan);
+
+// Integer output length of one axis.
+int64_t conv_len(int64_t L, int k, int s, int p, int d);
+int64_t convT_len(int64_t L, int k, int s, int p, int d, int op);
+
+}  // namespace tc3d

@@ -94,3 +94,70 @@ WORKLOADS = [
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _axis_pairs(L, K, s, p, d, O, transposed):
+    """Number of (output position, tap) pairs of one axis whose input index is
+    in range (and, for a transposed conv, exactly divisible)."""
+    n = 0
+    for o in range(O):
+        for k in range(K):
+            if transposed:
+                t = o + p - d * k
+                if t % s == 0 and 0 <= t // s < L:
+                    n += 1
+            else:
+                if 0 <= o * s - p + d * k < L:
+                    n += 1
+    return n
+
+
+def out_spatial(wl: Workload):
+    """Output extents of the convolution / transposed convolution (before pooling)."""
+    dims = []
+    for a in range(3):
+        L, K = wl.x_shape[2 + a], wl.w_shape[2 + a]
+        s, p, d = wl.stride[a], wl.padding[a], wl.dilation[a]
+        if wl.transposed:
+            dims.append((L - 1) * s - 2 * p + d * (K - 1) + wl.output_padding[a] + 1)
+        else:
+            dims.append((L + 2 * p - d * (K - 1) - 1) // s + 1)
+    return tuple(dims)
+
+
+def valid_macs(wl: Workload) -> int:
+    """Multiply-adds of the definition's sum, counting only taps whose input
+    index is in range (zero taps ignored): the algorithmic work."""
+    O = out_spatial(wl)
+    prod = 1
+    for a in range(3):
+        prod *= _axis_pairs(wl.x_shape[2 + a], wl.w_shape[2 + a], wl.stride[a], wl.padding[a],
+                            wl.dilation[a], O[a], wl.transposed)
+    cin_g = wl.x_shape[1] // wl.groups
+    return wl.x_shape[0] * wl.cout * cin_g * prod
+
+
+def dense_macs(wl: Workload) -> int:
+    """Multiply-adds of the dense definition (every tap of every output)."""
+    O = out_spatial(wl)
+    cin_g = wl.x_shape[1] // wl.groups
+    return wl.x_shape[0] * wl.cout * cin_g * int(np.prod(O)) * int(np.prod(wl.w_shape[2:]))
+
+
+def y_shape(wl: Workload):
+    O = out_spatial(wl)
+    N = wl.x_shape[0]
+    if wl.op == "conv_maxpool_lse_relu":
+        return (N, 1) + tuple(o // 2 for o in O)
+    if wl.op == "convT_bn_avgpool":
+        return (N, wl.cout) + tuple(o // 4 for o in O)
+    return (N, wl.cout) + O
+
+
+def algorithmic_bytes(wl: Workload) -> int:
+    """Read x and the weights (and bias) once, write y once; fused
+    intermediates count zero."""
+    n = int(np.prod(wl.x_shape)) + int(np.prod(wl.w_shape)) + int(np.prod(y_shape(wl)))
+    if wl.bias:
+        n += wl.cout
+    return 4 * n
