@@ -71,7 +71,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                 "-lms", "100", "-i", self.gpu_id], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -130,8 +130,8 @@ def recorded_traffic(kernel_workload):
 # ---------------------------------------------------------------------------
 # CPU oracle on bounded samples (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
-ORACLE_SAMPLES = {"conv331": 200000, "convT_s2p1d2": 60000, "convT_bn_avgpool": 200000,
-                  "conv_maxpool_lse_relu": 20000}
+ORACLE_SAMPLES = {"conv331": 20000000, "convT_s2p1d2": 6000000, "convT_bn_avgpool": 20000000,
+                  "conv_maxpool_lse_relu": 2000000}
 
 
 def oracle_sample_run(names, scale=1.0, inputs_cache=None):
@@ -380,7 +380,7 @@ def run_reference(args):
         return
     names = args.workloads.split(",")
     cache = {}
-    scale = 0.25
+    scale = 0.005
     for _ in range(args.warmup):
         oracle_sample_run(names, scale=scale, inputs_cache=cache)
     tot_fl = tot_s = 0.0
@@ -410,8 +410,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default=",".join(BENCH_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")

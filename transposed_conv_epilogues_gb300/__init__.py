@@ -206,9 +206,7 @@ def _stream(stream, device):
 def _workspace(nbytes, device, workspace):
     torch = _torch()
     if workspace is not None:
-        if workspace.numel() * workspace.element_size() < nbytes:
-            raise ValueError("workspace too small")
-        return workspace
+        return workspace  # its size is checked by the library (TC3D_ERR_WORKSPACE)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
