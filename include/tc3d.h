@@ -115,6 +115,34 @@ int tc3d_convT_bn_avgpool(const float* x, const float* w, const float* bias, con
                           const int output_padding[3], int groups, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
+/* Scratch size of tc3d_conv_maxpool_lse_relu_noalloc (1 MiB). */
+#define TC3D_NOALLOC_SCRATCH_BYTES (1 << 20)
+
+/* tc3d_conv_maxpool_lse_relu without a workspace argument, for callers that
+ * cannot allocate device memory (code inside an allocator or pool callback,
+ * hosts that own every device allocation, paths where an allocation and its
+ * implicit synchronisation are not allowed).  The paper has no counterpart:
+ * this is an addition for such callers.  Same arguments and result as
+ * tc3d_conv_maxpool_lse_relu minus workspace/workspace_bytes.
+ *  - The scratch is a TC3D_NOALLOC_SCRATCH_BYTES array compiled into the
+ *    library; every GPU that loads the library holds it until process exit.
+ *    The call never allocates or frees memory.
+ *  - Problems whose workspace (tc3d_workspace_bytes) exceeds that size are
+ *    rejected with TC3D_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race and give wrong results; serialise
+ *    them.  Each call rewrites every scratch byte it reads, so nothing needs
+ *    clearing between calls. */
+int tc3d_conv_maxpool_lse_relu_noalloc(const float* x, const float* w, const float* bias,
+                                       float* y, int N, int Cin, int S0, int S1, int S2,
+                                       int Cout, int k0, int k1, int k2, const int stride[3],
+                                       const int pad[3], const int dilation[3],
+                                       const int output_padding[3], int groups,
+                                       cudaStream_t stream);
+
 /* Host-only queries (no device work).  op is a TC3D_OP_* selector; the
  * remaining arguments are those of the matching entry point.  Both validate
  * the arguments exactly as the entry point does. */

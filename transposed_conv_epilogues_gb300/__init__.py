@@ -47,7 +47,7 @@ EXPORTED = [
     "tc3d_conv3d_fwd", "tc3d_conv_transpose3d_fwd", "tc3d_conv_maxpool_lse_relu",
     "tc3d_convT_bn_avgpool", "tc3d_workspace_bytes", "tc3d_out_shape", "tc3d_plan_describe",
     "tc3d_last_device_error", "tc3d_set_wait_timeout_ns", "tc3d_selftest_wait_timeout",
-    "tc3d_status_string",
+    "tc3d_status_string", "tc3d_conv_maxpool_lse_relu_noalloc",
 ]
 
 _lib = None
@@ -79,6 +79,8 @@ def load(path: str | Path | None = None):
         f = getattr(lib, name)
         f.argtypes = [_P, _P, _P, _P] + geom + tail
         f.restype = _I
+    lib.tc3d_conv_maxpool_lse_relu_noalloc.argtypes = [_P, _P, _P, _P] + geom + [_P]
+    lib.tc3d_conv_maxpool_lse_relu_noalloc.restype = _I
     lib.tc3d_convT_bn_avgpool.argtypes = [_P, _P, _P, _P, _P, ctypes.c_float, _P] + geom + tail
     lib.tc3d_convT_bn_avgpool.restype = _I
     lib.tc3d_workspace_bytes.argtypes = [_I] + geom + [ctypes.POINTER(ctypes.c_size_t)]
