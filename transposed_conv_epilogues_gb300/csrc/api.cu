@@ -24,6 +24,10 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 
+// The kernels bound their waits in SM clock cycles; 2.1 cycles per ns is the
+// top clock, so at lower clocks a wait may last somewhat longer in time.
+unsigned long long timeout_cycles(unsigned long long ns) { return ns * 21ull / 10ull; }
+
 struct DeviceState {
   bool init = false;
   int status = TC3D_OK;
@@ -112,7 +116,7 @@ int set_smem(DeviceState* d, int epi) {
 void fill_params(const Plan& pl, EngineParams* ep) {
   std::memset(ep, 0, sizeof(*ep));
   const Problem& pb = pl.pb;
-  ep->timeout_ns = g_timeout_ns.load();
+  ep->timeout_cycles = timeout_cycles(g_timeout_ns.load());
   ep->N = pb.N;
   ep->C = pb.Cin;
   ep->Cout = pb.Cout;
@@ -513,7 +517,8 @@ int tc3d_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
   DeviceState* d = nullptr;
   int rc = device_state(&d);
   if (rc) return rc;
-  if (wait_timeout_launch(d->err, timeout_ns, stream) != cudaSuccess) return TC3D_ERR_CUDA;
+  if (wait_timeout_launch(d->err, timeout_cycles(timeout_ns), stream) != cudaSuccess)
+    return TC3D_ERR_CUDA;
   return tc3d_last_device_error(stream);
 }
 

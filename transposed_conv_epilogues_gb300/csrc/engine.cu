@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   volatile int* abortf = reinterpret_cast<volatile int*>(gbase + p.sm_bar + kBarAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + p.sm_bar + kBarTmemSlot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t tmo = p.timeout_ns;
+  const unsigned long long tmo = p.timeout_cycles;
 
   // ---------------- set-up ----------------
   if (threadIdx.x == 0) {
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       mbar_init(bars.b_full(i), 1);
       mbar_init(bars.b_empty(i), 1);
     }
-    for (int i = 0; i < kMaxAStages; ++i) {
+    for (int i = 0; i < kAStages; ++i) {
       mbar_init(bars.a_full(i), 4);
       mbar_init(bars.a_empty(i), 1);
     }
@@ -301,78 +301,99 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
   }
   // ================= MMA issuer =================
+  // The whole warp runs this loop (warp-uniform control flow); one elected
+  // lane issues each tcgen05 instruction.  Ring positions advance
+  // incrementally and descriptors are formed by adds, so the loop costs far
+  // less than the 3 x 32 tensor cycles of a stage at N = 64.
   else if (warp == kWarpMMA) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_tf32(128, (uint32_t)p.n_tile);
-      const uint32_t lo_off = (uint32_t)p.n_tile * 32u;  // Blo follows Bw in a stage
-      bool ok = true;
-      if (p.b_resident) {
-        ok = mbar_wait(bars.b_full(0), 0, tmo, abortf);
-        if (!ok) raise_abort(p, abortf);
-      }
-      int it_k = 0, it_a = 0, it_d = 0;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-        for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
-          const int dslot = it_d % p.dbuf;
-          if (!mbar_wait(bars.d_empty(dslot), ((it_d / p.dbuf) & 1) ^ 1, tmo, abortf)) {
-            raise_abort(p, abortf);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_base = tmem_base + (uint32_t)(dslot * dcols);
-          bool first = true;
-          for (int c = 0; c < p.n_chunks && ok; ++c) {
-            for (int j = 0; j < p.ksteps_chunk; ++j, ++it_k) {
-              uint32_t b_addr;
-              int bstage = 0;
-              if (p.b_resident) {
-                b_addr = sbase + p.sm_b + (uint32_t)(c * p.ksteps_chunk + j) * p.b_stage_bytes;
-              } else {
-                bstage = it_k % p.b_stages;
-                if (!mbar_wait(bars.b_full(bstage), (it_k / p.b_stages) & 1, tmo, abortf)) {
-                  raise_abort(p, abortf);
-                  ok = false;
-                  break;
-                }
-                b_addr = sbase + p.sm_b + (uint32_t)bstage * p.b_stage_bytes;
+    const uint32_t idesc = idesc_tf32(128, (uint32_t)p.n_tile);
+    const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
+    const uint64_t lo_step = (uint64_t)(p.n_tile * 32) >> 4;  // w_lo follows w in a stage
+    const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;
+    bool ok = true;
+    if (p.b_resident) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
+      if (!ok && lane == 0) raise_abort(p, abortf);
+    }
+    int bstage = 0, as = 0, dslot = 0;
+    uint32_t bphase = 0, aphase = 0, dphase = 0;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.d_empty(dslot), dphase ^ 1, tmo, abortf));
+        if (!ok) {
+          if (lane == 0) raise_abort(p, abortf);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_base = tmem_base + (uint32_t)(dslot * dcols);
+        uint32_t accumulate = 0;
+        int kres = 0;  // K-step index within the resident weight block
+        for (int c = 0; c < p.n_chunks && ok; ++c) {
+          for (int j = 0; j < p.ksteps_chunk; ++j, ++kres) {
+            uint64_t bw;
+            if (p.b_resident) {
+              bw = bdesc0 + (uint64_t)kres * stage_step;
+            } else {
+              ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(bstage), bphase, tmo, abortf));
+              if (!ok) {
+                if (lane == 0) raise_abort(p, abortf);
+                break;
               }
-              const uint64_t bw = smem_desc_noswz(b_addr, 128, 256);
-              const uint64_t blo = smem_desc_noswz(b_addr + lo_off, 128, 256);
-              for (int a = 0; a < p.n_acc; ++a, ++it_a) {
-                const int as = it_a % p.a_stages;
-                if (!mbar_wait(bars.a_full(as), (it_a / p.a_stages) & 1, tmo, abortf)) {
-                  raise_abort(p, abortf);
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                const uint32_t a_tm = tmem_base + a_col0 + (uint32_t)as * 16u;
-                const uint32_t d_tm = d_base + (uint32_t)(a * p.n_tile);
-                mma_tf32_ts(d_tm, a_tm, bw, idesc, first ? 0u : 1u);  // x . w
-                mma_tf32_ts(d_tm, a_tm, blo, idesc, 1u);              // x . w_lo
-                mma_tf32_ts(d_tm, a_tm + 8, bw, idesc, 1u);           // x_lo . w
-                mma_commit(bars.a_empty(as));
-              }
-              if (!ok) break;
-              if (!p.b_resident) mma_commit(bars.b_empty(bstage));
-              first = false;
+              bw = bdesc0 + (uint64_t)bstage * stage_step;
             }
+            const uint64_t blo = bw + lo_step;
+            uint32_t d_tm = d_base;
+            for (int a = 0; a < p.n_acc; ++a) {
+              ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(as), aphase, tmo, abortf));
+              if (!ok) {
+                if (lane == 0) raise_abort(p, abortf);
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_tm = tmem_base + a_col0 + (uint32_t)as * 16u;
+              mma_tf32_ts_elect(d_tm, a_tm, bw, idesc, accumulate);  // x . w
+              mma_tf32_ts_elect(d_tm, a_tm, blo, idesc, 1u);         // x . w_lo
+              mma_tf32_ts_elect(d_tm, a_tm + 8, bw, idesc, 1u);      // x_lo . w
+              mma_commit_elect(bars.a_empty(as));
+              d_tm += (uint32_t)p.n_tile;
+              if (++as == kAStages) {
+                as = 0;
+                aphase ^= 1;
+              }
+            }
+            if (!ok) break;
+            if (!p.b_resident) {
+              mma_commit_elect(bars.b_empty(bstage));
+              if (++bstage == p.b_stages) {
+                bstage = 0;
+                bphase ^= 1;
+              }
+            }
+            accumulate = 1;
           }
-          if (!ok) break;
-          mma_commit(bars.d_full(dslot));
+        }
+        if (!ok) break;
+        mma_commit_elect(bars.d_full(dslot));
+        if (++dslot == p.dbuf) {
+          dslot = 0;
+          dphase ^= 1;
         }
       }
     }
   }
   // ================= conversion warps =================
+  // Warps 7..10 and 11..14 are two groups; each covers all four TMEM lane
+  // quarters.  A-stage s (= K-step * n_acc + accumulator) is filled by group
+  // s & 1.  Per K-step a group gathers all its stages, stores them to TMEM,
+  // waits for the stores once and signals them.
   else if (warp >= kWarpConv0) {
     const int cw = warp - kWarpConv0;
     const int half = cw >> 2;
     const int q = warp & 3;
     const int* ktab = reinterpret_cast<const int*>(gbase + p.sm_ktab);
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    int it_raw = 0, it_a = 0;
+    int rstage = 0, it_a = 0;
+    uint32_t rphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
@@ -387,11 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                      p.s_in[2] * t[2] + xshift;
       }
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
-        for (int c = 0; c < p.n_chunks && ok; ++c, ++it_raw) {
-          const int rstage = it_raw % p.raw_stages;
-          ok = mbar_wait(bars.raw_full(rstage), (it_raw / p.raw_stages) & 1, tmo, abortf);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
+        for (int c = 0; c < p.n_chunks && ok; ++c) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.raw_full(rstage), rphase, tmo, abortf));
+          if (!ok) {
             if (lane == 0) raise_abort(p, abortf);
             break;
           }
@@ -404,36 +423,51 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
             const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
             const int kbase = j * 8;
+            bool vk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vk[e] = kbase + e < valid_k;
+            int np = 0;
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
               if (a >= p.n_acc) break;
-              const int s = it_a++;
+              const int s = it_a + a;
               if ((s & 1) != half) continue;
-              const int as = s % p.a_stages;
-              ok = mbar_wait(bars.a_empty(as), ((s / p.a_stages) & 1) ^ 1, tmo, abortf);
-              if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                if (lane == 0) raise_abort(p, abortf);
-                break;
-              }
+              const int as = s & (kAStages - 1);
+              const uint32_t aph = ((uint32_t)(s / kAStages) & 1u) ^ 1u;
+              ok = __all_sync(0xffffffffu, mbar_wait(bars.a_empty(as), aph, tmo, abortf));
+              if (!ok) break;
               tc_fence_after();
               const float* rp = raw + row_off[a];
               uint32_t v[16];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float xv = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
+                const float xv = vk[e] ? rp[kofs[e]] : 0.f;
                 v[e] = __float_as_uint(xv);
                 v[8 + e] = __float_as_uint(xv - tf32_trunc(xv));
               }
               tmem_st16(tmem_base + lane_addr + a_col0 + (uint32_t)as * 16u, v);
+              ++np;
+            }
+            if (!ok) {
+              if (lane == 0) raise_abort(p, abortf);
+              break;
+            }
+            if (np) {
               tmem_wait_st();
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(bars.a_full(as));
+              if (lane == 0)
+                for (int a = 0; a < p.n_acc; ++a)
+                  if (((it_a + a) & 1) == half) mbar_arrive(bars.a_full((it_a + a) & (kAStages - 1)));
             }
+            it_a += p.n_acc;
           }
           __syncwarp();
           if (ok && lane == 0) mbar_arrive(bars.raw_empty(rstage));
+          if (++rstage == p.raw_stages) {
+            rstage = 0;
+            rphase ^= 1;
+          }
         }
       }
     }
@@ -929,14 +963,14 @@ __global__ void fill_slab_kernel(float* y, const float* bias, int N, int Cout, i
   }
 }
 
-__global__ void wait_timeout_kernel(int* err, unsigned long long timeout_ns) {
+__global__ void wait_timeout_kernel(int* err, unsigned long long timeout_cycles) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);
     fence_barrier_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, timeout_ns, nullptr)) atomicExch(err, 1);
+  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, timeout_cycles, nullptr)) atomicExch(err, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -1011,8 +1045,8 @@ cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const
   return cudaGetLastError();
 }
 
-cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_ns, cudaStream_t st) {
-  wait_timeout_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_cycles, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(err, timeout_cycles);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ constexpr int kThreads = kNumWarps * 32;
 
 constexpr int kMaxRawStages = 3;
 constexpr int kMaxBStages = 16;
-constexpr int kMaxAStages = 16;
+constexpr int kAStages = 16;  // TMEM A-stage ring (16 columns each)
 
 struct EngineParams {
   CUtensorMap xmap;  // 5-D map over x (dims S2, S1, S0, C, N), used when use_tma
@@ -32,7 +32,7 @@ struct EngineParams {
   float* y;
   float2* partials;  // BN-pool: [Cout][tiles] (sum, sum of squares) of bias-free values
   int* err;
-  unsigned long long timeout_ns;
+  unsigned long long timeout_cycles;  // bound of every mbarrier wait (SM clock cycles)
   int use_tma;
 
   int N, C, Cout, G, cin_g, cout_g;
@@ -95,7 +95,7 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
 // rows past the GEMM row grid; all of them in classes without taps)
 cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
                              const int zlo[3], unsigned blocks, cudaStream_t st);
-cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_ns, cudaStream_t st);
+cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_cycles, cudaStream_t st);
 
 // device address of the library's error word on the current device
 cudaError_t error_flag_address(int** addr);

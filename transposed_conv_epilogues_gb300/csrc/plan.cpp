@@ -248,8 +248,9 @@ int make_plan(const Problem& pb_in, Plan* out) {
   }
   {
     int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
-    pl.a_stages = std::min(16, (kTmemCols - dcols) / 16);
-    if (pl.a_stages < 4) return fail(TC3D_ERR_UNSUPPORTED);
+    // the kernel's A-stage ring is 16 stages of 16 TMEM columns
+    pl.a_stages = 16;
+    if (dcols + 16 * pl.a_stages > kTmemCols) return fail(TC3D_ERR_UNSUPPORTED);
   }
 
   // ---- quarter box Q and quarter arrangement P (search)
