@@ -156,6 +156,7 @@ void fill_params(const Plan& pl, EngineParams* ep) {
   ep->n_acc = pl.n_acc;
   ep->dbuf = pl.dbuf;
   ep->a_stages = pl.a_stages;
+  ep->ks_stage = pl.ks_stage;
   ep->tiles = (int)pl.tiles;
   ep->cin_chunk = pl.cin_chunk;
   ep->n_chunks = pl.n_chunks;
@@ -390,6 +391,7 @@ std::string describe(const Plan& pl) {
     append(s, ", \"n_acc\": %lld", pl.n_acc);
     append(s, ", \"dbuf\": %lld", pl.dbuf);
     append(s, ", \"a_stages\": %lld", pl.a_stages);
+    append(s, ", \"ks_stage\": %lld", pl.ks_stage);
     append(s, ", \"tiles\": %lld", pl.tiles);
     append(s, ", \"cin_chunk\": %lld", pl.cin_chunk);
     append(s, ", \"n_chunks\": %lld", pl.n_chunks);

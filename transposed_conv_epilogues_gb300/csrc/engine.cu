@@ -175,14 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       mbar_init(bars.b_full(i), 1);
       mbar_init(bars.b_empty(i), 1);
     }
-    for (int i = 0; i < kAStages; ++i) {
-      mbar_init(bars.a_full(i), 4);
+    // with one accumulator the two conversion groups take alternate K-steps
+    // (4 warps fill a stage); otherwise both groups fill every stage
+    const uint32_t a_full_count = p.n_acc >= 2 ? kNumConvWarps : kNumConvWarps / 2;
+    for (int i = 0; i < kMaxAStages; ++i) {
+      mbar_init(bars.a_full(i), a_full_count);
       mbar_init(bars.a_empty(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.d_full(i), 1);
-      mbar_init(bars.d_empty(i), kNumEpiWarps);
-      mbar_init(bars.epi(i), kNumEpiWarps);
+      mbar_init(bars.d_empty(i), kEpiGroup);
+      mbar_init(bars.epi(i), kEpiGroup);
     }
     *abortf = 0;
     fence_barrier_init();
@@ -283,17 +286,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
           for (int cb = 0; cb < p.n_colblocks && ok; ++cb)
             for (int c = 0; c < p.n_chunks && ok; ++c)
-              for (int j = 0; j < p.ksteps_chunk; ++j, ++it) {
+              for (int j = 0; j < p.ksteps_chunk; j += p.ks_stage, ++it) {
                 const int stage = it % p.b_stages;
+                const uint32_t bytes =
+                    (uint32_t)(min(p.ks_stage, p.ksteps_chunk - j) * 64 * p.n_tile);
                 if (!mbar_wait(bars.b_empty(stage), ((it / p.b_stages) & 1) ^ 1, tmo, abortf)) {
                   raise_abort(p, abortf);
                   ok = false;
                   break;
                 }
-                mbar_arrive_expect_tx(bars.b_full(stage), p.b_stage_bytes);
+                mbar_arrive_expect_tx(bars.b_full(stage), bytes);
                 const size_t src =
-                    (((size_t)cb * p.n_chunks + c) * p.ksteps_chunk + j) * (p.b_stage_bytes / 4);
-                bulk_g2s(sbase + p.sm_b + stage * p.b_stage_bytes, p.wpack + src, p.b_stage_bytes,
+                    (((size_t)cb * p.n_chunks + c) * p.ksteps_chunk + j) * (16 * (size_t)p.n_tile);
+                bulk_g2s(sbase + p.sm_b + stage * p.b_stage_bytes, p.wpack + src, bytes,
                          bars.b_full(stage));
               }
         }
@@ -309,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     const uint32_t idesc = idesc_tf32(128, (uint32_t)p.n_tile);
     const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
     const uint64_t lo_step = (uint64_t)(p.n_tile * 32) >> 4;  // w_lo follows w in a stage
-    const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;
+    const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;   // one streamed stage
+    const uint64_t kstep_step = (uint64_t)(64 * p.n_tile) >> 4;    // one K-step of weights
     bool ok = true;
     if (p.b_resident) {
       ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
@@ -329,39 +335,42 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         uint32_t accumulate = 0;
         int kres = 0;  // K-step index within the resident weight block
         for (int c = 0; c < p.n_chunks && ok; ++c) {
-          for (int j = 0; j < p.ksteps_chunk; ++j, ++kres) {
-            uint64_t bw;
+          for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(as), aphase, tmo, abortf));
+            if (!ok) {
+              if (lane == 0) raise_abort(p, abortf);
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_stage =
+                tmem_base + a_col0 + (uint32_t)(as * 16 * p.n_acc * p.ks_stage);
+            uint64_t bstage_desc;
             if (p.b_resident) {
-              bw = bdesc0 + (uint64_t)kres * stage_step;
+              bstage_desc = bdesc0 + (uint64_t)kres * kstep_step;
             } else {
               ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(bstage), bphase, tmo, abortf));
               if (!ok) {
                 if (lane == 0) raise_abort(p, abortf);
                 break;
               }
-              bw = bdesc0 + (uint64_t)bstage * stage_step;
+              bstage_desc = bdesc0 + (uint64_t)bstage * stage_step;
             }
-            const uint64_t blo = bw + lo_step;
-            uint32_t d_tm = d_base;
-            for (int a = 0; a < p.n_acc; ++a) {
-              ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(as), aphase, tmo, abortf));
-              if (!ok) {
-                if (lane == 0) raise_abort(p, abortf);
-                break;
+            const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
+            for (int kk = 0; kk < kcount; ++kk) {
+              const uint64_t bw = bstage_desc + (uint64_t)kk * kstep_step;
+              const uint64_t blo = bw + lo_step;
+              const uint32_t a_tm = a_stage + (uint32_t)(kk * 16 * p.n_acc);
+#pragma unroll
+              for (int a = 0; a < 4; ++a) {
+                if (a >= p.n_acc) break;
+                const uint32_t d_tm = d_base + (uint32_t)(a * p.n_tile);
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc, accumulate);  // x . w
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, blo, idesc, 1u);         // x . w_lo
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc, 1u);      // x_lo . w
               }
-              tc_fence_after();
-              const uint32_t a_tm = tmem_base + a_col0 + (uint32_t)as * 16u;
-              mma_tf32_ts_elect(d_tm, a_tm, bw, idesc, accumulate);  // x . w
-              mma_tf32_ts_elect(d_tm, a_tm, blo, idesc, 1u);         // x . w_lo
-              mma_tf32_ts_elect(d_tm, a_tm + 8, bw, idesc, 1u);      // x_lo . w
-              mma_commit_elect(bars.a_empty(as));
-              d_tm += (uint32_t)p.n_tile;
-              if (++as == kAStages) {
-                as = 0;
-                aphase ^= 1;
-              }
+              accumulate = 1;
             }
-            if (!ok) break;
+            kres += kcount;
             if (!p.b_resident) {
               mma_commit_elect(bars.b_empty(bstage));
               if (++bstage == p.b_stages) {
@@ -369,7 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                 bphase ^= 1;
               }
             }
-            accumulate = 1;
+            if (!ok) break;
+            mma_commit_elect(bars.a_empty(as));
+            if (++as == p.a_stages) {
+              as = 0;
+              aphase ^= 1;
+            }
           }
         }
         if (!ok) break;
@@ -383,17 +397,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   }
   // ================= conversion warps =================
   // Warps 7..10 and 11..14 are two groups; each covers all four TMEM lane
-  // quarters.  A-stage s (= K-step * n_acc + accumulator) is filled by group
-  // s & 1.  Per K-step a group gathers all its stages, stores them to TMEM,
-  // waits for the stores once and signals them.
+  // quarters.  An A-stage holds one K-step for all accumulators (16 columns
+  // each: x then x_lo).  With two or more accumulators, group g fills the
+  // accumulators a with a % 2 == g of every stage; with one accumulator the
+  // groups take alternate K-steps.
   else if (warp >= kWarpConv0) {
     const int cw = warp - kWarpConv0;
     const int half = cw >> 2;
     const int q = warp & 3;
     const int* ktab = reinterpret_cast<const int*>(gbase + p.sm_ktab);
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    int rstage = 0, it_a = 0;
-    uint32_t rphase = 0;
+    const bool split_acc = p.n_acc >= 2;
+    int rstage = 0, as = 0, kglob = 0;
+    uint32_t rphase = 0, aphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
@@ -418,49 +434,49 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
               reinterpret_cast<const float*>(gbase + p.sm_raw + rstage * p.raw_stage_bytes);
           const int cin_valid = min(p.cin_chunk, p.cin_g - c * p.cin_chunk);
           const int valid_k = cin_valid * p.nUtot;
-          for (int j = 0; j < p.ksteps_chunk && ok; ++j) {
-            const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
-            const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
-            const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            const int kbase = j * 8;
-            bool vk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) vk[e] = kbase + e < valid_k;
-            int np = 0;
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-              if (a >= p.n_acc) break;
-              const int s = it_a + a;
-              if ((s & 1) != half) continue;
-              const int as = s & (kAStages - 1);
-              const uint32_t aph = ((uint32_t)(s / kAStages) & 1u) ^ 1u;
-              ok = __all_sync(0xffffffffu, mbar_wait(bars.a_empty(as), aph, tmo, abortf));
-              if (!ok) break;
-              tc_fence_after();
-              const float* rp = raw + row_off[a];
-              uint32_t v[16];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float xv = vk[e] ? rp[kofs[e]] : 0.f;
-                v[e] = __float_as_uint(xv);
-                v[8 + e] = __float_as_uint(xv - tf32_trunc(xv));
+          for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage, ++kglob) {
+            const bool mine = split_acc || ((kglob & 1) == half);
+            if (mine) {
+              ok = __all_sync(0xffffffffu, mbar_wait(bars.a_empty(as), aphase ^ 1, tmo, abortf));
+              if (!ok) {
+                if (lane == 0) raise_abort(p, abortf);
+                break;
               }
-              tmem_st16(tmem_base + lane_addr + a_col0 + (uint32_t)as * 16u, v);
-              ++np;
-            }
-            if (!ok) {
-              if (lane == 0) raise_abort(p, abortf);
-              break;
-            }
-            if (np) {
+              tc_fence_after();
+              const uint32_t stage_col =
+                  tmem_base + lane_addr + a_col0 + (uint32_t)(as * 16 * p.n_acc * p.ks_stage);
+              const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
+              for (int kk = 0; kk < kcount; ++kk) {
+                const int j = j0 + kk;
+                const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
+                const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
+                const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                const int kbase = j * 8;
+                const uint32_t kcol = stage_col + (uint32_t)(kk * 16 * p.n_acc);
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                  if (a >= p.n_acc) break;
+                  if (split_acc && (a & 1) != half) continue;
+                  const float* rp = raw + row_off[a];
+                  uint32_t v[16];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    const float xv = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
+                    v[e] = __float_as_uint(xv);
+                    v[8 + e] = __float_as_uint(xv - tf32_trunc(xv));
+                  }
+                  tmem_st16(kcol + (uint32_t)(a * 16), v);
+                }
+              }
               tmem_wait_st();
               tc_fence_before();
               __syncwarp();
-              if (lane == 0)
-                for (int a = 0; a < p.n_acc; ++a)
-                  if (((it_a + a) & 1) == half) mbar_arrive(bars.a_full((it_a + a) & (kAStages - 1)));
+              if (lane == 0) mbar_arrive(bars.a_full(as));
             }
-            it_a += p.n_acc;
+            if (++as == p.a_stages) {
+              as = 0;
+              aphase ^= 1;
+            }
           }
           __syncwarp();
           if (ok && lane == 0) mbar_arrive(bars.raw_empty(rstage));
@@ -475,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   // ================= epilogue warps =================
   else {
     const int q = warp & 3;
-    const int ew = warp - kWarpEpi0;  // 0..3
+    const int egroup = (warp - kWarpEpi0) / kEpiGroup;  // 0 or 1
+    const int ew = (warp - kWarpEpi0) % kEpiGroup;       // 0..3 within the group
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const long long ovol = (long long)p.O[0] * p.O[1] * p.O[2];
     const long long o12 = (long long)p.O[1] * p.O[2];
@@ -505,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         lse_s[a] = 0.f;
       }
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
+        // with two accumulator buffers group g takes buffer g; with one,
+        // group 0 takes every tile
+        if (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0)) continue;
         const int g = cb / p.nb_per_group, nb = cb % p.nb_per_group;
         const int oc0 = g * p.cout_g + nb * p.ocb;
         const int ocb_valid = min(p.ocb, p.cout_g - nb * p.ocb);
@@ -519,39 +539,100 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         const uint32_t dbase = tmem_base + lane_addr + (uint32_t)(dslot * dcols);
 
         if constexpr (EPI == EPI_STORE) {
+          const int F = p.s_out[0] * p.s_out[1] * p.s_out[2];
+          if (p.nR == 1 && F <= 8) {
+            // fast path: one class with taps (fstar), the others hold the bias.
+            // Class f = (r0, r1, r2) of the full s_out grid sits at offset
+            // off[f] from the row's first output.
+            int off[8], rr[8][3];
+            int fstar = 0;
+#pragma unroll
+            for (int f = 0; f < 8; ++f) {
+              const int r2 = f % p.s_out[2], r1 = (f / p.s_out[2]) % p.s_out[1],
+                        r0 = f / (p.s_out[2] * p.s_out[1]);
+              rr[f][0] = r0;
+              rr[f][1] = r1;
+              rr[f][2] = r2;
+              off[f] = (int)(r0 * o12 + (long long)r1 * p.O[2] + r2);
+              if (f < F && r0 == p.r_axis[0][0] && r1 == p.r_axis[1][0] && r2 == p.r_axis[2][0])
+                fstar = f;
+            }
 #pragma unroll 1
-          for (int a = 0; a < p.n_acc; ++a) {
-            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
-            int mm[3];
-            bool rv = false;
+            for (int a = 0; a < p.n_acc; ++a) {
+              const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+              int mm[3] = {0, 0, 0};
+              bool rv = false;
 #pragma unroll
-            for (int aa = 0; aa < 4; ++aa)
-              if (aa == a) {
-                mm[0] = m[aa][0];
-                mm[1] = m[aa][1];
-                mm[2] = m[aa][2];
-                rv = rvalid[aa];
-              }
-            const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1], zb2 = p.s_out[2] * mm[2];
-            const long long ybase = (long long)tc.n * p.Cout * ovol + (long long)zb0 * o12 +
-                                    (long long)zb1 * p.O[2] + zb2;
-            const bool plain = p.nR == 1 && p.nEmpty == 0;
-            for (int cc = 0; cc < p.n_tile; cc += 16) {
-              uint32_t v[16];
-              tmem_ld16(taddr + (uint32_t)cc, v);
-              tmem_wait_ld();
-              if (!rv) continue;
-              if (plain) {
+              for (int aa = 0; aa < 4; ++aa)
+                if (aa == a) {
+                  mm[0] = m[aa][0];
+                  mm[1] = m[aa][1];
+                  mm[2] = m[aa][2];
+                  rv = rvalid[aa];
+                }
+              const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1],
+                        zb2 = p.s_out[2] * mm[2];
+              uint32_t mask = 0;
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                  const int oc_l = cc + jj;
-                  if (oc_l < ocb_valid) {
-                    const int oc = oc0 + oc_l;
-                    const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
-                    p.y[ybase + (long long)oc * ovol] = __uint_as_float(v[jj]) + b;
+              for (int f = 0; f < 8; ++f)
+                if (rv && f < F && zb0 + rr[f][0] < p.O[0] && zb1 + rr[f][1] < p.O[1] &&
+                    zb2 + rr[f][2] < p.O[2])
+                  mask |= 1u << f;
+              float* yrow = p.y + ((long long)tc.n * p.Cout + oc0) * ovol + (long long)zb0 * o12 +
+                            (long long)zb1 * p.O[2] + zb2;
+              for (int cc = 0; cc < p.n_tile; cc += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + (uint32_t)cc, v);
+                tmem_wait_ld();
+                const int oc_lane = cc + lane;
+                const float bl = (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
+                float* yo = yrow + (long long)cc * ovol;
+                if (F == 1) {  // a convolution: one output per row and channel
+#pragma unroll
+                  for (int jj = 0; jj < 32; ++jj) {
+                    if (cc + jj >= ocb_valid) break;
+                    const float b = __shfl_sync(0xffffffffu, bl, jj);
+                    if (mask & 1u) *yo = __uint_as_float(v[jj]) + b;
+                    yo += ovol;
+                  }
+                } else {
+#pragma unroll
+                  for (int jj = 0; jj < 32; ++jj) {
+                    if (cc + jj >= ocb_valid) break;
+                    const float b = __shfl_sync(0xffffffffu, bl, jj);
+                    const float val = __uint_as_float(v[jj]) + b;
+#pragma unroll
+                    for (int f = 0; f < 8; ++f)
+                      if ((mask >> f) & 1u) yo[off[f]] = (f == fstar) ? val : b;
+                    yo += ovol;
                   }
                 }
-              } else {
+              }
+            }
+          } else {
+            // general path: several classes with taps (oc-major columns)
+#pragma unroll 1
+            for (int a = 0; a < p.n_acc; ++a) {
+              const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+              int mm[3] = {0, 0, 0};
+              bool rv = false;
+#pragma unroll
+              for (int aa = 0; aa < 4; ++aa)
+                if (aa == a) {
+                  mm[0] = m[aa][0];
+                  mm[1] = m[aa][1];
+                  mm[2] = m[aa][2];
+                  rv = rvalid[aa];
+                }
+              const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1],
+                        zb2 = p.s_out[2] * mm[2];
+              const long long ybase = (long long)tc.n * p.Cout * ovol + (long long)zb0 * o12 +
+                                      (long long)zb1 * p.O[2] + zb2;
+              for (int cc = 0; cc < p.n_tile; cc += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + (uint32_t)cc, v);
+                tmem_wait_ld();
+                if (!rv) continue;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                   const int col = cc + jj;
@@ -593,29 +674,34 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             }
           }
         } else if constexpr (EPI == EPI_POOL_LSE) {
-          // rows of a quarter are a 2x2x2 block of 2x2x8 positions: lanes
-          // {l, l^1, l^8, l^16} .. form one MaxPool3d(2) window
+          // rows of a quarter are a 2x2x8 block of positions: lanes
+          // {l, l^1, l^8, l^16} form one MaxPool3d(2) window
+          const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
             if (a >= p.n_acc) break;
             const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
-            const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
-            for (int cc = 0; cc < p.n_tile; cc += 16) {
-              uint32_t u[16];
-              tmem_ld16(taddr + (uint32_t)cc, u);
+            for (int cc = 0; cc < p.n_tile; cc += 32) {
+              uint32_t u[32];
+              tmem_ld32(taddr + (uint32_t)cc, u);
               tmem_wait_ld();
-              float v[16], mx[2];
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(u[jj]);
-              reduce_scatter16_window<true>(v, lane, mx);
+              for (int hh = 0; hh < 2; ++hh) {
+                const int c16 = cc + 16 * hh;
+                if (c16 >= p.n_tile) break;
+                float v[16], mx[2];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int oc_l = cc + bsel + h;
-                if (oc_l < ocb_valid) {
-                  const float val = mx[h] + (p.bias ? __ldg(p.bias + oc0 + oc_l) : 0.f);
-                  const float nm = fmaxf(lse_m[a], val);
-                  lse_s[a] = lse_s[a] * expf(lse_m[a] - nm) + expf(val - nm);
-                  lse_m[a] = nm;
+                for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(u[16 * hh + jj]);
+                reduce_scatter16_window<true>(v, lane, mx);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int oc_l = c16 + bsel + h;
+                  if (oc_l < ocb_valid) {
+                    const float val = mx[h] + (p.bias ? __ldg(p.bias + oc0 + oc_l) : 0.f);
+                    const float nm = fmaxf(lse_m[a], val);
+                    lse_s[a] = lse_s[a] * expf(lse_m[a] - nm) + expf(val - nm);
+                    lse_m[a] = nm;
+                  }
                 }
               }
             }
@@ -652,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
 #pragma unroll 1
           for (int a = 0; a < p.n_acc; ++a) {
             const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
-            int mm[3];
+            int mm[3] = {0, 0, 0};
             bool rv = false;
 #pragma unroll
             for (int aa = 0; aa < 4; ++aa)
@@ -674,13 +760,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 16; ++i) ps[i] = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {  // 16 columns = 2 channels x 8 classes
-              if (cc * 16 >= p.n_tile) break;
-              uint32_t u[16];
-              tmem_ld16(taddr + (uint32_t)(cc * 16), u);
+            for (int cc = 0; cc < 4; ++cc) {  // 32 columns = 4 channels x 8 classes
+              if (cc * 32 >= p.n_tile) break;
+              uint32_t u[32];
+              tmem_ld32(taddr + (uint32_t)(cc * 32), u);
               tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+              for (int h = 0; h < 4; ++h) {
                 float sum = 0.f, a1 = 0.f, a2 = 0.f;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -690,9 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                   a1 += vm;
                   a2 = fmaf(vm, vm, a2);
                 }
-                ps[2 * cc + h] = sum;
-                s1[2 * cc + h] += a1;
-                s2[2 * cc + h] += a2;
+                ps[4 * cc + h] = sum;
+                s1[4 * cc + h] += a1;
+                s2[4 * cc + h] += a2;
               }
             }
             // pooled sums over the 8 rows of each 4x4x4 window
@@ -733,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             if (lane < ocb_valid) {
               float2 acc = red[lane];
 #pragma unroll
-              for (int w = 1; w < kNumEpiWarps; ++w) {
+              for (int w = 1; w < kEpiGroup; ++w) {
                 acc.x += red[w * 16 + lane].x;
                 acc.y += red[w * 16 + lane].y;
               }

@@ -13,16 +13,17 @@ namespace tc3d {
 constexpr int kWarpRaw = 0;     // TMA (or plain-load) producer of raw input boxes
 constexpr int kWarpB = 1;       // bulk-copy producer of packed weight K-steps
 constexpr int kWarpMMA = 2;     // TMEM allocator + single-thread tcgen05.mma issuer
-constexpr int kWarpEpi0 = 3;    // 4 epilogue warps (TMEM lane quarter = warp % 4)
-constexpr int kNumEpiWarps = 4;
-constexpr int kWarpConv0 = 7;   // 8 conversion warps: raw fp32 -> (x, x - trunc(x)) in TMEM
+constexpr int kWarpEpi0 = 3;    // 8 epilogue warps in two groups of 4 (TMEM lane quarter =
+constexpr int kNumEpiWarps = 8; // warp % 4); with two accumulator buffers the groups alternate
+constexpr int kEpiGroup = 4;    // warps per epilogue group
+constexpr int kWarpConv0 = 11;  // 8 conversion warps: raw fp32 -> (x, x - trunc(x)) in TMEM
 constexpr int kNumConvWarps = 8;
-constexpr int kNumWarps = 15;
+constexpr int kNumWarps = 19;
 constexpr int kThreads = kNumWarps * 32;
 
 constexpr int kMaxRawStages = 3;
 constexpr int kMaxBStages = 16;
-constexpr int kAStages = 16;  // TMEM A-stage ring (16 columns each)
+constexpr int kMaxAStages = 16;  // TMEM A-stage ring: one K-step of all accumulators per stage
 
 struct EngineParams {
   CUtensorMap xmap;  // 5-D map over x (dims S2, S1, S0, C, N), used when use_tma
@@ -47,7 +48,8 @@ struct EngineParams {
   int cls_mask[3];  // per axis: bit r set iff class r has a tap
 
   int ocb, n_tile, nb_per_group, n_colblocks;
-  int n_acc, dbuf, a_stages;
+  int n_acc, dbuf, a_stages;  // a_stages: ring depth, 16*n_acc*ks_stage TMEM columns each
+  int ks_stage;              // K-steps per A-stage
   int Q[3], Pq[3], T[3], ntile[3];
   int tiles;
 

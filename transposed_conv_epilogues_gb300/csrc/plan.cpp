@@ -248,9 +248,8 @@ int make_plan(const Problem& pb_in, Plan* out) {
   }
   {
     int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
-    // the kernel's A-stage ring is 16 stages of 16 TMEM columns
-    pl.a_stages = 16;
-    if (dcols + 16 * pl.a_stages > kTmemCols) return fail(TC3D_ERR_UNSUPPORTED);
+    // A-stage ring sized below, once the K-steps per channel chunk are known
+    pl.a_stages = 0;
   }
 
   // ---- quarter box Q and quarter arrangement P (search)
@@ -341,6 +340,24 @@ int make_plan(const Problem& pb_in, Plan* out) {
     pl.k_chunk = best_cc * nUtot;
     pl.ksteps_chunk = (int)ceil_div(pl.k_chunk, 8);
     pl.raw_stage_bytes = round_up(best_cc * raw_ch, 1024);
+    // An A-stage carries up to ks_stage K-steps of all accumulators (up to 24
+    // MMAs) so that each stage's barrier wait / commit is amortised; a stage
+    // never straddles two channel chunks.  Streamed weight stages match
+    // A-stages.
+    {
+      const int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
+      pl.ks_stage = 1;
+      // the last stage of a chunk may hold fewer K-steps; a weight stage
+      // stays within 32 KB
+      for (int ks = std::min(std::max(1, 8 / pl.n_acc), pl.ksteps_chunk); ks > 1; --ks)
+        if (64LL * pl.n_tile * ks <= 32 * 1024 &&
+            (kTmemCols - dcols) / (16 * pl.n_acc * ks) >= 2) {
+          pl.ks_stage = ks;
+          break;
+        }
+      pl.a_stages = std::min(16, (kTmemCols - dcols) / (16 * pl.n_acc * pl.ks_stage));
+      if (pl.a_stages < 2) return fail(TC3D_ERR_UNSUPPORTED);
+    }
     const int64_t ktab = round_up((int64_t)pl.ksteps_chunk * 32, 1024);
     const int64_t total_ksteps = (int64_t)pl.n_chunks * pl.ksteps_chunk;
     pl.b_stage_bytes = bstage;
@@ -350,10 +367,11 @@ int make_plan(const Problem& pb_in, Plan* out) {
       pl.b_stages = (int)total_ksteps;
     } else {
       pl.b_resident = 0;
-      pl.b_stages = (int)std::min<int64_t>(kMaxBStagesPlan, rem / bstage);
+      pl.b_stage_bytes = bstage * pl.ks_stage;
+      pl.b_stages = (int)std::min<int64_t>(kMaxBStagesPlan, rem / pl.b_stage_bytes);
       if (pl.b_stages < 2) return fail(TC3D_ERR_UNSUPPORTED);
     }
-    const int64_t used = (int64_t)pl.b_stages * bstage + ktab + fixed;
+    const int64_t used = (int64_t)pl.b_stages * pl.b_stage_bytes + ktab + fixed;
     pl.raw_stages = (used + 3 * pl.raw_stage_bytes <= kMaxSmem) ? 3 : 2;
     pl.smem_bytes = smem_layout(pl).total;
     if (pl.smem_bytes > kMaxSmem) return fail(TC3D_ERR_UNSUPPORTED);
@@ -363,8 +381,7 @@ int make_plan(const Problem& pb_in, Plan* out) {
   {
     int64_t off = 0;
     pl.ws_wpack_off = off;
-    pl.ws_wpack_bytes =
-        (int64_t)pl.n_colblocks * pl.n_chunks * pl.ksteps_chunk * pl.b_stage_bytes;
+    pl.ws_wpack_bytes = (int64_t)pl.n_colblocks * pl.n_chunks * pl.ksteps_chunk * 64 * pl.n_tile;
     off = round_up(off + pl.ws_wpack_bytes, 256);
     if (pb.op == OP_CONVT_BN_POOL) {
       pl.ws_part_off = off;

@@ -69,6 +69,7 @@ struct Plan {
   // tiles: a tile is n_acc accumulators of 128 rows; each 32-row quarter is a
   // box Q0 x Q1 x Q2, quarters are arranged P0 x P1 x P2 -> tile T = P*Q
   int n_acc, dbuf, a_stages;
+  int ks_stage;     // K-steps per A-stage (a stage = ks_stage x n_acc x 16 TMEM columns)
   int Q[3], Pq[3], T[3];
   int ntile[3];
   int xslack;       // max misalignment (elements) of a raw box's x start

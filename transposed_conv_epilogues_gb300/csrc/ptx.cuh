@@ -41,19 +41,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_try_wait, but a thread whose phase is not complete may be
+// suspended (not polling, not issuing) for up to ~hint_ns before returning
+// false; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false if it did not complete within timeout_cycles SM clock cycles, or if
-// *abort becomes non-zero (another role of the CTA gave up).  The deadline is
-// checked with the SM-local cycle counter every 256 polls, so a wait that
-// succeeds after a few polls costs no timer read.  Never spins forever.
+// *abort becomes non-zero (another role of the CTA gave up).  A waiting
+// thread is suspended inside try_wait (up to 0.1 ms per try) instead of
+// spinning, so waiting warps leave the issue slots to working ones.  The
+// deadline is checked with the SM-local cycle counter every 16 tries.
+// Never waits forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           unsigned long long timeout_cycles,
                                           const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = -1;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+    if ((it & 15u) == 0) {
       if (abort && *abort) return false;
       const long long now = clock64();
       if (t0 < 0)
@@ -152,6 +170,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
         "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns into registers
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr)
       : "memory");
 }
