@@ -157,6 +157,8 @@ void fill_params(const Plan& pl, EngineParams* ep) {
   ep->dbuf = pl.dbuf;
   ep->a_stages = pl.a_stages;
   ep->ks_stage = pl.ks_stage;
+  ep->wide = pl.wide;
+  ep->acc_cols = pl.acc_cols;
   ep->tiles = (int)pl.tiles;
   ep->cin_chunk = pl.cin_chunk;
   ep->n_chunks = pl.n_chunks;
@@ -392,6 +394,8 @@ std::string describe(const Plan& pl) {
     append(s, ", \"dbuf\": %lld", pl.dbuf);
     append(s, ", \"a_stages\": %lld", pl.a_stages);
     append(s, ", \"ks_stage\": %lld", pl.ks_stage);
+    append(s, ", \"wide\": %lld", pl.wide);
+    append(s, ", \"acc_cols\": %lld", pl.acc_cols);
     append(s, ", \"tiles\": %lld", pl.tiles);
     append(s, ", \"cin_chunk\": %lld", pl.cin_chunk);
     append(s, ", \"n_chunks\": %lld", pl.n_chunks);

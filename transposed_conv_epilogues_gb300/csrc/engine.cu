@@ -151,10 +151,146 @@ __device__ __forceinline__ void reduce_scatter16_window(const float (&v)[16], in
   }
 }
 
+
+
+// Read 32 (16) accumulator columns of this thread's row; with the fused
+// [w | w_lo] MMA the accumulator has a second half lo_off columns to the right
+// whose values are added.
+__device__ __forceinline__ void load_acc32(uint32_t taddr, uint32_t lo_off, uint32_t (&v)[32]) {
+  tmem_ld32(taddr, v);
+  if (lo_off) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[16];
+      tmem_ld16(taddr + lo_off + 16 * h, u);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[16 * h + i] = __float_as_uint(__uint_as_float(v[16 * h + i]) + __uint_as_float(u[i]));
+    }
+  } else {
+    tmem_wait_ld();
+  }
+}
+__device__ __forceinline__ void load_acc16(uint32_t taddr, uint32_t lo_off, uint32_t (&v)[16]) {
+  tmem_ld16(taddr, v);
+  if (lo_off) {
+    uint32_t u[16];
+    tmem_ld16(taddr + lo_off, u);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(u[i]));
+  } else {
+    tmem_wait_ld();
+  }
+}
+
+// The MMA issuer.  The whole warp runs this loop (warp-uniform control
+// flow) and one elected lane issues each tcgen05 instruction; the accumulator
+// loop is unrolled at compile time, ring positions advance incrementally and
+// descriptors are formed by adds.  Per (accumulator, K-step):
+//   WIDE:  D[0:2n] (+)= x . [w | w_lo]   (one N = 2n MMA over the adjacent
+//                                          weight halves) and D[0:n] += x_lo . w
+//   else:  D (+)= x . w,  D += x . w_lo,  D += x_lo . w
+template <int NACC, bool WIDE>
+__device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars, uint32_t sbase,
+                                         uint32_t tmem_base, uint32_t a_col0, int dcols,
+                                         volatile int* abortf, unsigned long long tmo, int lane) {
+  const uint32_t idesc_n = idesc_tf32(128, (uint32_t)p.n_tile);
+  const uint32_t idesc_2n = idesc_tf32(128, (uint32_t)(2 * p.n_tile));
+  const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
+  const uint64_t lo_step = (uint64_t)(p.n_tile * 32) >> 4;     // w_lo follows w in a K-step
+  const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;  // one streamed stage
+  const uint64_t kstep_step = (uint64_t)(64 * p.n_tile) >> 4;  // one K-step of weights
+  const uint32_t acc_cols = (uint32_t)p.acc_cols;
+  bool ok = true;
+  if (p.b_resident) {
+    ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
+    if (!ok && lane == 0) raise_abort(p, abortf);
+  }
+  int bstage = 0, as = 0, dslot = 0;
+  uint32_t bphase = 0, aphase = 0, dphase = 0;
+  for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+    for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.d_empty(dslot), dphase ^ 1, tmo, abortf));
+      if (!ok) {
+        if (lane == 0) raise_abort(p, abortf);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_base = tmem_base + (uint32_t)(dslot * dcols);
+      uint32_t accumulate = 0;
+      int kres = 0;  // K-step index within the resident weight block
+      for (int c = 0; c < p.n_chunks && ok; ++c) {
+        for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(as), aphase, tmo, abortf));
+          if (!ok) {
+            if (lane == 0) raise_abort(p, abortf);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_stage = tmem_base + a_col0 + (uint32_t)(as * 16 * NACC * p.ks_stage);
+          uint64_t bstage_desc;
+          if (p.b_resident) {
+            bstage_desc = bdesc0 + (uint64_t)kres * kstep_step;
+          } else {
+            ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(bstage), bphase, tmo, abortf));
+            if (!ok) {
+              if (lane == 0) raise_abort(p, abortf);
+              break;
+            }
+            bstage_desc = bdesc0 + (uint64_t)bstage * stage_step;
+          }
+          const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
+          for (int kk = 0; kk < kcount; ++kk) {
+            const uint64_t bw = bstage_desc + (uint64_t)kk * kstep_step;
+            const uint32_t a_tm = a_stage + (uint32_t)(kk * 16 * NACC);
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) {
+              const uint32_t d_tm = d_base + (uint32_t)a * acc_cols;
+              if (WIDE) {
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc_2n, accumulate);  // x.[w|w_lo]
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc_n, 1u);       // x_lo . w
+              } else {
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc_n, accumulate);   // x . w
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw + lo_step, idesc_n, 1u); // x . w_lo
+                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc_n, 1u);       // x_lo . w
+              }
+            }
+            accumulate = 1;
+          }
+          kres += kcount;
+          if (!p.b_resident) {
+            mma_commit_elect(bars.b_empty(bstage));
+            if (++bstage == p.b_stages) {
+              bstage = 0;
+              bphase ^= 1;
+            }
+          }
+          mma_commit_elect(bars.a_empty(as));
+          if (++as == p.a_stages) {
+            as = 0;
+            aphase ^= 1;
+          }
+        }
+      }
+      if (!ok) break;
+      mma_commit_elect(bars.d_full(dslot));
+      if (++dslot == p.dbuf) {
+        dslot = 0;
+        dphase ^= 1;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngineParams p) {
+__global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
+    engine_kernel(const __grid_constant__ EngineParams p) {
+  constexpr int kWarpConv0 = WarpCfg<EPI>::kConv0;
+  constexpr int kThreads = WarpCfg<EPI>::kThreads;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s_unaligned = smem_u32(smem_dyn);
   const uint32_t sbase = (s_unaligned + 1023u) & ~1023u;
@@ -213,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int dcols = p.n_acc * p.n_tile;  // columns of one D buffer
+  const int dcols = p.n_acc * p.acc_cols;  // columns of one D buffer
   const uint32_t a_col0 = (uint32_t)(p.dbuf * dcols);
 
   // ================= raw-input producer =================
@@ -306,93 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
   }
   // ================= MMA issuer =================
-  // The whole warp runs this loop (warp-uniform control flow); one elected
-  // lane issues each tcgen05 instruction.  Ring positions advance
-  // incrementally and descriptors are formed by adds, so the loop costs far
-  // less than the 3 x 32 tensor cycles of a stage at N = 64.
   else if (warp == kWarpMMA) {
-    const uint32_t idesc = idesc_tf32(128, (uint32_t)p.n_tile);
-    const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
-    const uint64_t lo_step = (uint64_t)(p.n_tile * 32) >> 4;  // w_lo follows w in a stage
-    const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;   // one streamed stage
-    const uint64_t kstep_step = (uint64_t)(64 * p.n_tile) >> 4;    // one K-step of weights
-    bool ok = true;
-    if (p.b_resident) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
-      if (!ok && lane == 0) raise_abort(p, abortf);
-    }
-    int bstage = 0, as = 0, dslot = 0;
-    uint32_t bphase = 0, aphase = 0, dphase = 0;
-    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.d_empty(dslot), dphase ^ 1, tmo, abortf));
-        if (!ok) {
-          if (lane == 0) raise_abort(p, abortf);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_base = tmem_base + (uint32_t)(dslot * dcols);
-        uint32_t accumulate = 0;
-        int kres = 0;  // K-step index within the resident weight block
-        for (int c = 0; c < p.n_chunks && ok; ++c) {
-          for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(as), aphase, tmo, abortf));
-            if (!ok) {
-              if (lane == 0) raise_abort(p, abortf);
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_stage =
-                tmem_base + a_col0 + (uint32_t)(as * 16 * p.n_acc * p.ks_stage);
-            uint64_t bstage_desc;
-            if (p.b_resident) {
-              bstage_desc = bdesc0 + (uint64_t)kres * kstep_step;
-            } else {
-              ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(bstage), bphase, tmo, abortf));
-              if (!ok) {
-                if (lane == 0) raise_abort(p, abortf);
-                break;
-              }
-              bstage_desc = bdesc0 + (uint64_t)bstage * stage_step;
-            }
-            const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
-            for (int kk = 0; kk < kcount; ++kk) {
-              const uint64_t bw = bstage_desc + (uint64_t)kk * kstep_step;
-              const uint64_t blo = bw + lo_step;
-              const uint32_t a_tm = a_stage + (uint32_t)(kk * 16 * p.n_acc);
-#pragma unroll
-              for (int a = 0; a < 4; ++a) {
-                if (a >= p.n_acc) break;
-                const uint32_t d_tm = d_base + (uint32_t)(a * p.n_tile);
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc, accumulate);  // x . w
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, blo, idesc, 1u);         // x . w_lo
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc, 1u);      // x_lo . w
-              }
-              accumulate = 1;
-            }
-            kres += kcount;
-            if (!p.b_resident) {
-              mma_commit_elect(bars.b_empty(bstage));
-              if (++bstage == p.b_stages) {
-                bstage = 0;
-                bphase ^= 1;
-              }
-            }
-            if (!ok) break;
-            mma_commit_elect(bars.a_empty(as));
-            if (++as == p.a_stages) {
-              as = 0;
-              aphase ^= 1;
-            }
-          }
-        }
-        if (!ok) break;
-        mma_commit_elect(bars.d_full(dslot));
-        if (++dslot == p.dbuf) {
-          dslot = 0;
-          dphase ^= 1;
-        }
-      }
+    switch (p.n_acc * 2 + p.wide) {
+      case 2: mma_role<1, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 3: mma_role<1, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 4: mma_role<2, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 5: mma_role<2, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 6: mma_role<3, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 7: mma_role<3, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      case 8: mma_role<4, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+      default: mma_role<4, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
     }
   }
   // ================= conversion warps =================
@@ -492,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   else {
     const int q = warp & 3;
     const int egroup = (warp - kWarpEpi0) / kEpiGroup;  // 0 or 1
+    const uint32_t lo_off = p.wide ? (uint32_t)p.n_tile : 0u;
     const int ew = (warp - kWarpEpi0) % kEpiGroup;       // 0..3 within the group
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const long long ovol = (long long)p.O[0] * p.O[1] * p.O[2];
@@ -559,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             }
 #pragma unroll 1
             for (int a = 0; a < p.n_acc; ++a) {
-              const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+              const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
               int mm[3] = {0, 0, 0};
               bool rv = false;
 #pragma unroll
@@ -582,8 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                             (long long)zb1 * p.O[2] + zb2;
               for (int cc = 0; cc < p.n_tile; cc += 32) {
                 uint32_t v[32];
-                tmem_ld32(taddr + (uint32_t)cc, v);
-                tmem_wait_ld();
+                load_acc32(taddr + (uint32_t)cc, lo_off, v);
                 const int oc_lane = cc + lane;
                 const float bl = (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
                 float* yo = yrow + (long long)cc * ovol;
@@ -613,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             // general path: several classes with taps (oc-major columns)
 #pragma unroll 1
             for (int a = 0; a < p.n_acc; ++a) {
-              const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+              const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
               int mm[3] = {0, 0, 0};
               bool rv = false;
 #pragma unroll
@@ -630,8 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                                       (long long)zb1 * p.O[2] + zb2;
               for (int cc = 0; cc < p.n_tile; cc += 16) {
                 uint32_t v[16];
-                tmem_ld16(taddr + (uint32_t)cc, v);
-                tmem_wait_ld();
+                load_acc16(taddr + (uint32_t)cc, lo_off, v);
                 if (!rv) continue;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
@@ -680,11 +738,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
             if (a >= p.n_acc) break;
-            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+            const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
             for (int cc = 0; cc < p.n_tile; cc += 32) {
               uint32_t u[32];
-              tmem_ld32(taddr + (uint32_t)cc, u);
-              tmem_wait_ld();
+              load_acc32(taddr + (uint32_t)cc, lo_off, u);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const int c16 = cc + 16 * hh;
@@ -737,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
 #pragma unroll 1
           for (int a = 0; a < p.n_acc; ++a) {
-            const uint32_t taddr = dbase + (uint32_t)(a * p.n_tile);
+            const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
             int mm[3] = {0, 0, 0};
             bool rv = false;
 #pragma unroll
@@ -1080,13 +1137,13 @@ cudaError_t engine_launch(int epi, const EngineParams& p, unsigned grid, size_t 
                           cudaStream_t st) {
   switch (epi) {
     case EPI_STORE:
-      engine_kernel<EPI_STORE><<<grid, kThreads, smem, st>>>(p);
+      engine_kernel<EPI_STORE><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
       break;
     case EPI_POOL_LSE:
-      engine_kernel<EPI_POOL_LSE><<<grid, kThreads, smem, st>>>(p);
+      engine_kernel<EPI_POOL_LSE><<<grid, WarpCfg<EPI_POOL_LSE>::kThreads, smem, st>>>(p);
       break;
     default:
-      engine_kernel<EPI_BN_POOL><<<grid, kThreads, smem, st>>>(p);
+      engine_kernel<EPI_BN_POOL><<<grid, WarpCfg<EPI_BN_POOL>::kThreads, smem, st>>>(p);
       break;
   }
   return cudaGetLastError();

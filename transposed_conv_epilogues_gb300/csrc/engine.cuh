@@ -9,17 +9,28 @@
 
 namespace tc3d {
 
-// Warp roles of the implicit-GEMM kernel (one CTA per SM, 15 warps).
-constexpr int kWarpRaw = 0;     // TMA (or plain-load) producer of raw input boxes
-constexpr int kWarpB = 1;       // bulk-copy producer of packed weight K-steps
-constexpr int kWarpMMA = 2;     // TMEM allocator + single-thread tcgen05.mma issuer
-constexpr int kWarpEpi0 = 3;    // 8 epilogue warps in two groups of 4 (TMEM lane quarter =
-constexpr int kNumEpiWarps = 8; // warp % 4); with two accumulator buffers the groups alternate
-constexpr int kEpiGroup = 4;    // warps per epilogue group
-constexpr int kWarpConv0 = 11;  // 8 conversion warps: raw fp32 -> (x, x - trunc(x)) in TMEM
+// Warp roles of the implicit-GEMM kernel (one CTA per SM):
+//   warp 0        TMA (or plain-load) producer of raw input boxes
+//   warp 1        bulk-copy producer of packed weight K-steps
+//   warp 2        TMEM allocator + MMA issuer
+//   warps 3..     epilogue: one group of 4 warps (TMEM lane quarter = warp % 4),
+//                 or two groups that alternate accumulator buffers when the
+//                 epilogue uses two buffers (stores, BatchNorm pooling)
+//   last 8 warps  conversion: raw fp32 -> (x, x - trunc(x)) in TMEM
+constexpr int kWarpRaw = 0;
+constexpr int kWarpB = 1;
+constexpr int kWarpMMA = 2;
+constexpr int kWarpEpi0 = 3;
+constexpr int kEpiGroup = 4;  // warps per epilogue group
 constexpr int kNumConvWarps = 8;
-constexpr int kNumWarps = 19;
-constexpr int kThreads = kNumWarps * 32;
+
+template <int EPI>
+struct WarpCfg {
+  static constexpr int kEpiWarps = EPI == EPI_POOL_LSE ? 4 : 8;
+  static constexpr int kConv0 = kWarpEpi0 + kEpiWarps;
+  static constexpr int kWarps = kConv0 + kNumConvWarps;
+  static constexpr int kThreads = kWarps * 32;
+};
 
 constexpr int kMaxRawStages = 3;
 constexpr int kMaxBStages = 16;
@@ -50,6 +61,7 @@ struct EngineParams {
   int ocb, n_tile, nb_per_group, n_colblocks;
   int n_acc, dbuf, a_stages;  // a_stages: ring depth, 16*n_acc*ks_stage TMEM columns each
   int ks_stage;              // K-steps per A-stage
+  int wide, acc_cols;        // fused [w | w_lo] MMA; TMEM columns of one accumulator
   int Q[3], Pq[3], T[3], ntile[3];
   int tiles;
 

@@ -239,15 +239,19 @@ int make_plan(const Problem& pb_in, Plan* out) {
   }
 
   // ---- accumulators per tile, TMEM budget
-  if (pl.epi == EPI_POOL_LSE) {
-    pl.dbuf = 1;
-    pl.n_acc = std::max(1, std::min(4, 256 / pl.n_tile));
-  } else {
-    pl.dbuf = pl.n_tile <= 128 ? 2 : 1;
-    pl.n_acc = std::max(1, std::min(4, 256 / (pl.dbuf * pl.n_tile)));
-  }
+  // Short MMAs (N <= 64) issue about as fast as the tensor core executes them,
+  // so when TMEM allows two accumulators the x.w and x.w_lo products are
+  // fused into one MMA over the adjacent [w | w_lo] weight block (N = 2
+  // n_tile), its two halves summed in the epilogue.
+  pl.dbuf = (pl.epi == EPI_POOL_LSE || pl.n_tile > 128) ? 1 : 2;
+  pl.wide = (pl.epi != EPI_BN_POOL && 2 * pl.n_tile <= 128 &&
+             256 / (pl.dbuf * 2 * pl.n_tile) >= 2)
+                ? 1
+                : 0;
+  pl.acc_cols = pl.wide ? 2 * pl.n_tile : pl.n_tile;
+  pl.n_acc = std::max(1, std::min(4, 256 / (pl.dbuf * pl.acc_cols)));
   {
-    int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
+    int dcols = pl.n_acc * pl.acc_cols * pl.dbuf;
     // A-stage ring sized below, once the K-steps per channel chunk are known
     pl.a_stages = 0;
   }
@@ -345,11 +349,13 @@ int make_plan(const Problem& pb_in, Plan* out) {
     // never straddles two channel chunks.  Streamed weight stages match
     // A-stages.
     {
-      const int dcols = pl.n_acc * pl.n_tile * pl.dbuf;
+      const int dcols = pl.n_acc * pl.acc_cols * pl.dbuf;
       pl.ks_stage = 1;
       // the last stage of a chunk may hold fewer K-steps; a weight stage
       // stays within 32 KB
-      for (int ks = std::min(std::max(1, 8 / pl.n_acc), pl.ksteps_chunk); ks > 1; --ks)
+      // about 24 MMAs per stage (2 per accumulator and K-step when wide, else 3)
+      const int per_ks = pl.n_acc * (pl.wide ? 2 : 3);
+      for (int ks = std::min(std::max(1, 24 / per_ks), pl.ksteps_chunk); ks > 1; --ks)
         if (64LL * pl.n_tile * ks <= 32 * 1024 &&
             (kTmemCols - dcols) / (16 * pl.n_acc * ks) >= 2) {
           pl.ks_stage = ks;

@@ -69,6 +69,8 @@ struct Plan {
   // tiles: a tile is n_acc accumulators of 128 rows; each 32-row quarter is a
   // box Q0 x Q1 x Q2, quarters are arranged P0 x P1 x P2 -> tile T = P*Q
   int n_acc, dbuf, a_stages;
+  int wide;         // 1: x.[w|w_lo] as one N = 2 n_tile MMA + x_lo.w (accumulator 2 n_tile wide)
+  int acc_cols;     // TMEM columns of one accumulator (n_tile, or 2 n_tile when wide)
   int ks_stage;     // K-steps per A-stage (a stage = ks_stage x n_acc x 16 TMEM columns)
   int Q[3], Pq[3], T[3];
   int ntile[3];
