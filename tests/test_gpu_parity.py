@@ -124,6 +124,8 @@ BN_CASES = [
     ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # fused
     ((2, 7, 9, 8, 10), (7, 5, 3, 3, 3), 2, 1, 1, (0, 1, 1), 1, True),  # fused, ragged
     ((2, 4, 6, 7, 8), (4, 3, 3, 3, 3), 2, 1, 1, 0, 2, True),          # fused, groups
+    ((1, 5, 10, 12, 9), (5, 40, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # fused, 3 column blocks
+    ((4, 3, 24, 24, 24), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),     # fused, more tiles than CTAs
     ((2, 3, 9, 5, 6), (3, 4, 3, 3, 3), (1, 2, 2), 1, 1, 0, 1, True),  # unfused: stride 1 axis
     ((2, 3, 6, 6, 6), (3, 4, 3, 3, 3), 2, 1, 2, 0, 1, True),          # unfused: dilation 2
 ]

@@ -144,6 +144,12 @@ void fill_params(const Plan& pl, EngineParams* ep) {
     ep->Pq[a] = pl.Pq[a];
     ep->T[a] = pl.T[a];
     ep->ntile[a] = pl.ntile[a];
+    ep->ntile_div[a] = make_fastdiv(pl.ntile[a]);
+    // the planner builds Q and Pq as powers of two
+    ep->lQ[a] = 0;
+    while ((1 << ep->lQ[a]) < pl.Q[a]) ++ep->lQ[a];
+    ep->lPq[a] = 0;
+    while ((1 << ep->lPq[a]) < pl.Pq[a]) ++ep->lPq[a];
     ep->box[a] = pl.box[a];
   }
   ep->nUtot = pl.nU[0] * pl.nU[1] * pl.nU[2];
@@ -258,7 +264,8 @@ int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, c
   ep.partials = partials;
   ep.err = d->err;
   encode_xmap(pl, x, &ep);
-  const unsigned grid = (unsigned)std::min<int64_t>(pl.tiles, d->sm_count);
+  const unsigned grid = (unsigned)engine_grid(pl, d->sm_count);
+  ep.part_slots = (int)bn_part_slots(pl, grid);
   int rc = set_smem(d, epi);
   if (rc) return rc;
   return engine_launch(epi, ep, grid, (size_t)pl.smem_bytes, st) == cudaSuccess ? TC3D_OK
@@ -309,7 +316,8 @@ int run(int op, const float* x, const float* w, const float* bias, const float* 
     rc = launch_engine(pl, EPI_BN_POOL, x, wpack, bias, y, part, d, st);
     if (rc) return rc;
     const double count = (double)N * (double)pl.O[0] * (double)pl.O[1] * (double)pl.O[2];
-    if (bn_stats_f2_launch(part, (int)pl.tiles, bias, gamma, beta, count, eps, Cout, stat, st) !=
+    const int slots = (int)bn_part_slots(pl, engine_grid(pl, d->sm_count));
+    if (bn_stats_f2_launch(part, slots, bias, gamma, beta, count, eps, Cout, stat, st) !=
             cudaSuccess ||
         bn_apply_launch(y, pl.y_elems, pvol, Cout, stat, blocks, st) != cudaSuccess)
       return TC3D_ERR_CUDA;

@@ -9,15 +9,18 @@
 //                            the tile's rows read (zero fill = padding)
 //   warp 1  (B producer)     bulk copies of pre-packed weight K-steps
 //                            (resident in shared memory when they fit)
-//   warps 7..14 (conversion) gather, for each K-step of 8 (channel, tap)
+//   last 8 warps (conversion) gather, for each K-step of 8 (channel, tap)
 //                            pairs and each row, x and x - trunc_tf32(x) from
 //                            the raw box and store them to TMEM (A operand)
-//   warp 2  (MMA)            tcgen05.mma kind::tf32, A from TMEM, B from
+//   warps 2, 3 (MMA)         tcgen05.mma kind::tf32, A from TMEM, B from
 //                            shared memory: D += A.Bw + A.Blo + Alo.Bw
 //                            (3xTF32: the tensor core reads the top 19 bits
 //                            of each fp32 operand, so x itself is the "hi"
-//                            part and only the low parts are formed)
-//   warps 3..6 (epilogue)    tcgen05.ld of D and the fused epilogue
+//                            part and only the low parts are formed).  Warp
+//                            2 issues for the even accumulators, warp 3 for
+//                            the odd ones, so that one issuer's barrier wait
+//                            and commit overlap the other's queued MMAs.
+//   warps 4.. (epilogue)     tcgen05.ld of D and the fused epilogue
 //
 // Every mbarrier wait is bounded; on time-out the CTA sets an error word and
 // all roles return, TMEM is freed, the kernel exits.
@@ -57,30 +60,31 @@ struct TileCoord {
 
 __device__ __forceinline__ TileCoord decode_tile(const EngineParams& p, int t) {
   TileCoord c;
-  const int b2 = t % p.ntile[2];
-  t /= p.ntile[2];
-  const int b1 = t % p.ntile[1];
-  t /= p.ntile[1];
-  const int b0 = t % p.ntile[0];
-  c.n = t / p.ntile[0];
+  const int t1 = fast_div(p.ntile_div[2], t);
+  const int b2 = t - t1 * p.ntile[2];
+  const int t2 = fast_div(p.ntile_div[1], t1);
+  const int b1 = t1 - t2 * p.ntile[1];
+  c.n = fast_div(p.ntile_div[0], t2);
+  const int b0 = t2 - c.n * p.ntile[0];
   c.o[0] = b0 * p.T[0];
   c.o[1] = b1 * p.T[1];
   c.o[2] = b2 * p.T[2];
   return c;
 }
 
-// local row coordinates of (accumulator a, lane quarter q, lane l)
+// local row coordinates of (accumulator a, lane quarter q, lane l); the
+// quarter box Q and the quarter arrangement Pq are powers of two
 __device__ __forceinline__ void row_local(const EngineParams& p, int a, int q, int l, int (&t)[3]) {
   const int j = a * 4 + q;
-  const int p0 = j / (p.Pq[1] * p.Pq[2]);
-  const int p1 = (j / p.Pq[2]) % p.Pq[1];
-  const int p2 = j % p.Pq[2];
-  const int l0 = l / (p.Q[1] * p.Q[2]);
-  const int l1 = (l / p.Q[2]) % p.Q[1];
-  const int l2 = l % p.Q[2];
-  t[0] = p0 * p.Q[0] + l0;
-  t[1] = p1 * p.Q[1] + l1;
-  t[2] = p2 * p.Q[2] + l2;
+  const int p0 = j >> (p.lPq[1] + p.lPq[2]);
+  const int p1 = (j >> p.lPq[2]) & (p.Pq[1] - 1);
+  const int p2 = j & (p.Pq[2] - 1);
+  const int l0 = l >> (p.lQ[1] + p.lQ[2]);
+  const int l1 = (l >> p.lQ[2]) & (p.Q[1] - 1);
+  const int l2 = l & (p.Q[2] - 1);
+  t[0] = (p0 << p.lQ[0]) + l0;
+  t[1] = (p1 << p.lQ[1]) + l1;
+  t[2] = (p2 << p.lQ[2]) + l2;
 }
 
 __device__ __forceinline__ void raise_abort(const EngineParams& p, volatile int* abortf) {
@@ -90,6 +94,11 @@ __device__ __forceinline__ void raise_abort(const EngineParams& p, volatile int*
 
 __device__ __forceinline__ float tf32_trunc(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// Value index whose total reduce_scatter16_sum leaves in a lane.
+__device__ __forceinline__ int scatter16_index(int lane) {
+  return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
 }
 
 // Sum 16 values over all 32 lanes; lane ends with the total of value index
@@ -185,17 +194,20 @@ __device__ __forceinline__ void load_acc16(uint32_t taddr, uint32_t lo_off, uint
   }
 }
 
-// The MMA issuer.  The whole warp runs this loop (warp-uniform control
-// flow) and one elected lane issues each tcgen05 instruction; the accumulator
-// loop is unrolled at compile time, ring positions advance incrementally and
-// descriptors are formed by adds.  Per (accumulator, K-step):
+// An MMA issuer.  The whole warp runs this loop (warp-uniform control flow)
+// and one elected lane issues each tcgen05 instruction; the loop over this
+// warp's NACC accumulators (a = a_first, a_first + a_stride, ...) is unrolled
+// at compile time, ring positions advance incrementally and descriptors are
+// formed by adds.  Every barrier this warp commits to counts one arrival per
+// issuer.  Per (accumulator, K-step):
 //   WIDE:  D[0:2n] (+)= x . [w | w_lo]   (one N = 2n MMA over the adjacent
 //                                          weight halves) and D[0:n] += x_lo . w
 //   else:  D (+)= x . w,  D += x . w_lo,  D += x_lo . w
 template <int NACC, bool WIDE>
 __device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars, uint32_t sbase,
                                          uint32_t tmem_base, uint32_t a_col0, int dcols,
-                                         volatile int* abortf, unsigned long long tmo, int lane) {
+                                         int a_first, int a_stride, volatile int* abortf,
+                                         unsigned long long tmo, int lane) {
   const uint32_t idesc_n = idesc_tf32(128, (uint32_t)p.n_tile);
   const uint32_t idesc_2n = idesc_tf32(128, (uint32_t)(2 * p.n_tile));
   const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
@@ -203,6 +215,7 @@ __device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars
   const uint64_t stage_step = (uint64_t)p.b_stage_bytes >> 4;  // one streamed stage
   const uint64_t kstep_step = (uint64_t)(64 * p.n_tile) >> 4;  // one K-step of weights
   const uint32_t acc_cols = (uint32_t)p.acc_cols;
+  const uint32_t kstep_cols = 16u * (uint32_t)p.n_acc;  // A columns of one K-step
   bool ok = true;
   if (p.b_resident) {
     ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
@@ -229,7 +242,7 @@ __device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars
             break;
           }
           tc_fence_after();
-          const uint32_t a_stage = tmem_base + a_col0 + (uint32_t)(as * 16 * NACC * p.ks_stage);
+          const uint32_t a_stage = tmem_base + a_col0 + (uint32_t)as * kstep_cols * p.ks_stage;
           uint64_t bstage_desc;
           if (p.b_resident) {
             bstage_desc = bdesc0 + (uint64_t)kres * kstep_step;
@@ -244,17 +257,19 @@ __device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars
           const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
           for (int kk = 0; kk < kcount; ++kk) {
             const uint64_t bw = bstage_desc + (uint64_t)kk * kstep_step;
-            const uint32_t a_tm = a_stage + (uint32_t)(kk * 16 * NACC);
+            const uint32_t a_tm = a_stage + (uint32_t)kk * kstep_cols;
 #pragma unroll
-            for (int a = 0; a < NACC; ++a) {
+            for (int i = 0; i < NACC; ++i) {
+              const int a = a_first + i * a_stride;
               const uint32_t d_tm = d_base + (uint32_t)a * acc_cols;
+              const uint32_t x_tm = a_tm + 16u * (uint32_t)a;
               if (WIDE) {
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc_2n, accumulate);  // x.[w|w_lo]
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc_n, 1u);       // x_lo . w
+                mma_tf32_ts_elect(d_tm, x_tm, bw, idesc_2n, accumulate);          // x.[w|w_lo]
+                mma_tf32_ts_elect(d_tm, x_tm + 8, bw, idesc_n, 1u);               // x_lo . w
               } else {
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw, idesc_n, accumulate);   // x . w
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a, bw + lo_step, idesc_n, 1u); // x . w_lo
-                mma_tf32_ts_elect(d_tm, a_tm + 16 * a + 8, bw, idesc_n, 1u);       // x_lo . w
+                mma_tf32_ts_elect(d_tm, x_tm, bw, idesc_n, accumulate);           // x . w
+                mma_tf32_ts_elect(d_tm, x_tm, bw + lo_step, idesc_n, 1u);         // x . w_lo
+                mma_tf32_ts_elect(d_tm, x_tm + 8, bw, idesc_n, 1u);               // x_lo . w
               }
             }
             accumulate = 1;
@@ -307,19 +322,21 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       mbar_init(bars.raw_full(i), 1);
       mbar_init(bars.raw_empty(i), kNumConvWarps);
     }
+    // stages and accumulator buffers are released by a commit of every issuer
+    const uint32_t issuers = p.n_acc >= 2 ? 2u : 1u;
     for (int i = 0; i < kMaxBStages; ++i) {
       mbar_init(bars.b_full(i), 1);
-      mbar_init(bars.b_empty(i), 1);
+      mbar_init(bars.b_empty(i), issuers);
     }
     // with one accumulator the two conversion groups take alternate K-steps
     // (4 warps fill a stage); otherwise both groups fill every stage
     const uint32_t a_full_count = p.n_acc >= 2 ? kNumConvWarps : kNumConvWarps / 2;
     for (int i = 0; i < kMaxAStages; ++i) {
       mbar_init(bars.a_full(i), a_full_count);
-      mbar_init(bars.a_empty(i), 1);
+      mbar_init(bars.a_empty(i), issuers);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.d_full(i), 1);
+      mbar_init(bars.d_full(i), issuers);
       mbar_init(bars.d_empty(i), kEpiGroup);
       mbar_init(bars.epi(i), kEpiGroup);
     }
@@ -442,22 +459,27 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     }
   }
   // ================= MMA issuer =================
-  else if (warp == kWarpMMA) {
-    switch (p.n_acc * 2 + p.wide) {
-      case 2: mma_role<1, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 3: mma_role<1, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 4: mma_role<2, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 5: mma_role<2, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 6: mma_role<3, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 7: mma_role<3, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      case 8: mma_role<4, false>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
-      default: mma_role<4, true>(p, bars, sbase, tmem_base, a_col0, dcols, abortf, tmo, lane); break;
+  else if (warp == kWarpMMA || warp == kWarpMMA1) {
+    // with two or more accumulators warp 2 takes the even ones, warp 3 the
+    // odd ones; with one, warp 2 takes it and warp 3 has nothing to do
+    const int par = warp - kWarpMMA;
+    const int stride = p.n_acc >= 2 ? 2 : 1;
+    const int mine = (p.n_acc - par + stride - 1) / stride;
+    switch (mine * 2 + p.wide) {
+      case 0: case 1: break;
+#define TC3D_MMA_ROLE(n, w) \
+  mma_role<n, w>(p, bars, sbase, tmem_base, a_col0, dcols, par, stride, abortf, tmo, lane)
+      case 2: TC3D_MMA_ROLE(1, false); break;
+      case 3: TC3D_MMA_ROLE(1, true); break;
+      case 4: TC3D_MMA_ROLE(2, false); break;
+      default: TC3D_MMA_ROLE(2, true); break;
+#undef TC3D_MMA_ROLE
     }
   }
   // ================= conversion warps =================
-  // Warps 7..10 and 11..14 are two groups; each covers all four TMEM lane
-  // quarters.  An A-stage holds one K-step for all accumulators (16 columns
-  // each: x then x_lo).  With two or more accumulators, group g fills the
+  // The first and last four conversion warps are two groups; each covers
+  // all four TMEM lane quarters.  An A-stage holds ks_stage K-steps of all
+  // accumulators (16 columns each: x then x_lo).  With two or more accumulators, group g fills the
   // accumulators a with a % 2 == g of every stage; with one accumulator the
   // groups take alternate K-steps.
   else if (warp >= kWarpConv0) {
@@ -470,18 +492,20 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     int rstage = 0, as = 0, kglob = 0;
     uint32_t rphase = 0, aphase = 0;
     bool ok = true;
+    // raw-box offset of this lane's row of each accumulator, before the
+    // tile's x alignment shift
+    int row_base[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      int t[3];
+      row_local(p, a < p.n_acc ? a : 0, q, lane, t);
+      row_base[a] = ((p.s_in[0] * t[0]) * p.box[1] + p.s_in[1] * t[1]) * p.box[2] +
+                    p.s_in[2] * t[2];
+    }
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
       const int xs = p.s_in[2] * tc.o[2] + p.u_min[2];
       const int xshift = xs - (xs & ~3);
-      int row_off[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        int t[3];
-        row_local(p, a < p.n_acc ? a : 0, q, lane, t);
-        row_off[a] = ((p.s_in[0] * t[0]) * p.box[1] + p.s_in[1] * t[1]) * p.box[2] +
-                     p.s_in[2] * t[2] + xshift;
-      }
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
         for (int c = 0; c < p.n_chunks && ok; ++c) {
           ok = __all_sync(0xffffffffu, mbar_wait(bars.raw_full(rstage), rphase, tmo, abortf));
@@ -489,8 +513,10 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             if (lane == 0) raise_abort(p, abortf);
             break;
           }
+          // raw box of this chunk, moved by the tile's x alignment shift
           const float* raw =
-              reinterpret_cast<const float*>(gbase + p.sm_raw + rstage * p.raw_stage_bytes);
+              reinterpret_cast<const float*>(gbase + p.sm_raw + rstage * p.raw_stage_bytes) +
+              xshift;
           const int cin_valid = min(p.cin_chunk, p.cin_g - c * p.cin_chunk);
           const int valid_k = cin_valid * p.nUtot;
           for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage, ++kglob) {
@@ -516,7 +542,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 for (int a = 0; a < 4; ++a) {
                   if (a >= p.n_acc) break;
                   if (split_acc && (a & 1) != half) continue;
-                  const float* rp = raw + row_off[a];
+                  const float* rp = raw + row_base[a];
                   uint32_t v[16];
 #pragma unroll
                   for (int e = 0; e < 8; ++e) {
@@ -558,6 +584,16 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     const long long o12 = (long long)p.O[1] * p.O[2];
     int it_d = 0;
     bool ok = true;
+    // BatchNorm partial sums (bias-free values) of the 16 channels this lane
+    // sees.  With one column block they run over every tile this warp takes
+    // and are written once at the end, to this warp's own slot; with several
+    // they are reduced and written per tile.
+    float s1[16], s2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      s1[i] = 0.f;
+      s2[i] = 0.f;
+    }
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
       // per accumulator: row coordinates of this lane
@@ -785,12 +821,6 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             }
           }
         } else {  // EPI_BN_POOL: stride-2 transposed conv, 8 classes per row (oc-major columns)
-          float s1[16], s2[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            s1[i] = 0.f;
-            s2[i] = 0.f;
-          }
           const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
 #pragma unroll 1
           for (int a = 0; a < p.n_acc; ++a) {
@@ -824,18 +854,30 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               tmem_wait_ld();
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
-                float sum = 0.f, a1 = 0.f, a2 = 0.f;
+                float sum = 0.f, sq = 0.f;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                   const float v = __uint_as_float(u[h * 8 + r]);
                   sum += v;
-                  const float vm = ((vmask >> r) & 1) ? v : 0.f;
-                  a1 += vm;
-                  a2 = fmaf(vm, vm, a2);
+                  sq = fmaf(v, v, sq);
+                }
+                if (vmask != 0xffu) {
+                  // a row on the output's far faces (or past M): only the
+                  // classes inside the output count.  Its 4^3 window index is
+                  // at least P on that axis, so its pooled sum is never
+                  // stored and the masked sum can serve for it too.
+                  sum = 0.f;
+                  sq = 0.f;
+#pragma unroll
+                  for (int r = 0; r < 8; ++r) {
+                    const float v = ((vmask >> r) & 1) ? __uint_as_float(u[h * 8 + r]) : 0.f;
+                    sum += v;
+                    sq = fmaf(v, v, sq);
+                  }
                 }
                 ps[4 * cc + h] = sum;
-                s1[4 * cc + h] += a1;
-                s2[4 * cc + h] += a2;
+                s1[4 * cc + h] += sum;
+                s2[4 * cc + h] += sq;
               }
             }
             // pooled sums over the 8 rows of each 4x4x4 window
@@ -856,37 +898,53 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               }
             }
           }
-          // BatchNorm partial sums of this tile: all lanes, then all 4 warps
-          const float t1 = reduce_scatter16_sum(s1, lane);
-          const float t2 = reduce_scatter16_sum(s2, lane);
-          float2* red = reinterpret_cast<float2*>(gbase + p.sm_misc) + (it_d & 1) * 64;
-          const int idx = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
-                          ((lane >> 1) & 1);
-          if ((lane & 1) == 0) red[ew * 16 + idx] = make_float2(t1, t2);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.epi(it_d & 1));
-          if (ew == 0) {
-            ok = mbar_wait(bars.epi(it_d & 1), (it_d >> 1) & 1, tmo, abortf);
-            if (!__all_sync(0xffffffffu, ok)) {
-              ok = false;
-              if (lane == 0) raise_abort(p, abortf);
-              break;
-            }
-            if (lane < ocb_valid) {
-              float2 acc = red[lane];
+          if (p.n_colblocks > 1) {
+            // BatchNorm partial sums of this tile: all lanes, then all 4 warps
+            const float t1 = reduce_scatter16_sum(s1, lane);
+            const float t2 = reduce_scatter16_sum(s2, lane);
 #pragma unroll
-              for (int w = 1; w < kEpiGroup; ++w) {
-                acc.x += red[w * 16 + lane].x;
-                acc.y += red[w * 16 + lane].y;
+            for (int i = 0; i < 16; ++i) {
+              s1[i] = 0.f;
+              s2[i] = 0.f;
+            }
+            float2* red = reinterpret_cast<float2*>(gbase + p.sm_misc) + (it_d & 1) * 64;
+            if ((lane & 1) == 0) red[ew * 16 + scatter16_index(lane)] = make_float2(t1, t2);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.epi(it_d & 1));
+            if (ew == 0) {
+              ok = mbar_wait(bars.epi(it_d & 1), (it_d >> 1) & 1, tmo, abortf);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                if (lane == 0) raise_abort(p, abortf);
+                break;
               }
-              p.partials[(size_t)(oc0 + lane) * p.tiles + tile] = acc;
+              if (lane < ocb_valid) {
+                float2 acc = red[lane];
+#pragma unroll
+                for (int w = 1; w < kEpiGroup; ++w) {
+                  acc.x += red[w * 16 + lane].x;
+                  acc.y += red[w * 16 + lane].y;
+                }
+                p.partials[(size_t)(oc0 + lane) * p.part_slots + tile] = acc;
+              }
             }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.d_empty(dslot));
+      }
+    }
+    if constexpr (EPI == EPI_BN_POOL) {
+      if (ok && p.n_colblocks == 1) {
+        // slot of this warp: CTA-major, then epilogue warp
+        const float t1 = reduce_scatter16_sum(s1, lane);
+        const float t2 = reduce_scatter16_sum(s2, lane);
+        const int oc = scatter16_index(lane);
+        const int slot = blockIdx.x * WarpCfg<EPI>::kEpiWarps + (warp - kWarpEpi0);
+        if ((lane & 1) == 0 && oc < p.cout_g)
+          p.partials[(size_t)oc * p.part_slots + slot] = make_float2(t1, t2);
       }
     }
   }
@@ -897,6 +955,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   tc_fence_after();
   if (warp == kWarpMMA) tmem_dealloc(tmem_base, kTmemCols);
 }
+
+static_assert(WarpCfg<EPI_BN_POOL>::kEpiWarps == kBnEpiWarps,
+              "BatchNorm partial slots are counted per epilogue warp");
 
 template __global__ void engine_kernel<EPI_STORE>(const __grid_constant__ EngineParams p);
 template __global__ void engine_kernel<EPI_POOL_LSE>(const __grid_constant__ EngineParams p);

@@ -12,15 +12,17 @@ namespace tc3d {
 // Warp roles of the implicit-GEMM kernel (one CTA per SM):
 //   warp 0        TMA (or plain-load) producer of raw input boxes
 //   warp 1        bulk-copy producer of packed weight K-steps
-//   warp 2        TMEM allocator + MMA issuer
-//   warps 3..     epilogue: one group of 4 warps (TMEM lane quarter = warp % 4),
+//   warp 2        TMEM allocator + MMA issuer of the even accumulators
+//   warp 3        MMA issuer of the odd accumulators (idle with one)
+//   warps 4..     epilogue: one group of 4 warps (TMEM lane quarter = warp % 4),
 //                 or two groups that alternate accumulator buffers when the
 //                 epilogue uses two buffers (stores, BatchNorm pooling)
 //   last 8 warps  conversion: raw fp32 -> (x, x - trunc(x)) in TMEM
 constexpr int kWarpRaw = 0;
 constexpr int kWarpB = 1;
 constexpr int kWarpMMA = 2;
-constexpr int kWarpEpi0 = 3;
+constexpr int kWarpMMA1 = 3;
+constexpr int kWarpEpi0 = 4;
 constexpr int kEpiGroup = 4;  // warps per epilogue group
 constexpr int kNumConvWarps = 8;
 
@@ -32,6 +34,33 @@ struct WarpCfg {
   static constexpr int kThreads = kWarps * 32;
 };
 
+// Division of an int in [0, 2^31) by a fixed divisor d >= 1 as one 64-bit
+// multiply and a shift (division by invariant integers, Granlund and
+// Montgomery, PLDI 1994): with l = ceil(log2 d), shift = 32 + l and
+// mul = ceil(2^shift / d), (n * mul) >> shift = floor(n / d), because
+// mul * d - 2^shift < d and n < 2^31 keep the error term below 1 / (2d).
+// mul < 2^33, so the product stays below 2^64.
+struct FastDiv {
+  unsigned long long mul;
+  int shift;
+  int d;
+};
+
+inline FastDiv make_fastdiv(int d) {
+  int l = 0;
+  while ((1LL << l) < (long long)d) ++l;
+  FastDiv f;
+  f.shift = 32 + l;
+  f.d = d;
+  const unsigned long long num = 1ULL << f.shift;  // shift <= 63 for d < 2^31
+  f.mul = num / (unsigned long long)d + (num % (unsigned long long)d ? 1 : 0);
+  return f;
+}
+
+__host__ __device__ __forceinline__ int fast_div(const FastDiv& f, int n) {
+  return (int)(((unsigned long long)(unsigned)n * f.mul) >> f.shift);
+}
+
 constexpr int kMaxRawStages = 3;
 constexpr int kMaxBStages = 16;
 constexpr int kMaxAStages = 16;  // TMEM A-stage ring: one K-step of all accumulators per stage
@@ -42,7 +71,8 @@ struct EngineParams {
   const float* wpack;
   const float* bias;
   float* y;
-  float2* partials;  // BN-pool: [Cout][tiles] (sum, sum of squares) of bias-free values
+  float2* partials;  // BN-pool: [Cout][part_slots] (sum, sum of squares) of bias-free values
+  int part_slots;    // one per epilogue warp of the grid (one column block), else one per tile
   int* err;
   unsigned long long timeout_cycles;  // bound of every mbarrier wait (SM clock cycles)
   int use_tma;
@@ -63,6 +93,8 @@ struct EngineParams {
   int ks_stage;              // K-steps per A-stage
   int wide, acc_cols;        // fused [w | w_lo] MMA; TMEM columns of one accumulator
   int Q[3], Pq[3], T[3], ntile[3];
+  int lQ[3], lPq[3];     // log2 of Q and Pq (powers of two)
+  FastDiv ntile_div[3];  // tile index -> tile coordinates
   int tiles;
 
   int cin_chunk, n_chunks, k_chunk, ksteps_chunk;

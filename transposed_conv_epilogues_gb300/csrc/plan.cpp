@@ -391,7 +391,9 @@ int make_plan(const Problem& pb_in, Plan* out) {
     off = round_up(off + pl.ws_wpack_bytes, 256);
     if (pb.op == OP_CONVT_BN_POOL) {
       pl.ws_part_off = off;
-      pl.ws_part_bytes = pl.fused ? pl.tiles * pb.Cout * 8 : (int64_t)pb.N * pb.Cout * 16;
+      // fused: enough slots for any grid; unfused: per (n, c) double sums
+      const int64_t slots = bn_part_slots(pl, std::min<int64_t>(pl.tiles, kMaxGrid));
+      pl.ws_part_bytes = pl.fused ? slots * pb.Cout * 8 : (int64_t)pb.N * pb.Cout * 16;
       off = round_up(off + pl.ws_part_bytes, 256);
       pl.ws_stat_off = off;
       pl.ws_stat_bytes = (int64_t)pb.Cout * 8;

@@ -3,6 +3,7 @@
 // convolution's output-parity classes and tap tables, tile shapes and the
 // shared/tensor-memory budget of one launch.
 #pragma once
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 
@@ -27,6 +28,8 @@ constexpr int kMaxKChunk = 1024;    // GEMM-K values staged per channel chunk
 constexpr int kMaxBStagesPlan = 16; // streamed weight stages (mbarrier pairs in the kernel)
 constexpr int kTmemCols = 512;
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxGrid = 1024;      // CTAs of a persistent engine launch, at most
+constexpr int kBnEpiWarps = 8;      // epilogue warps of the BatchNorm-pool engine
 
 struct Problem {
   int op;
@@ -89,7 +92,7 @@ struct Plan {
 
   // workspace (bytes, each region 256-aligned)
   int64_t ws_wpack_off, ws_wpack_bytes;
-  int64_t ws_part_off, ws_part_bytes;   // BN partials: fused [Cout][tiles] float2, else [N][Cout] double2
+  int64_t ws_part_off, ws_part_bytes;   // BN partials: fused [Cout][slots] float2, else [N][Cout] double2
   int64_t ws_stat_off, ws_stat_bytes;   // BN scale/shift [Cout] float2
   int64_t ws_full_off, ws_full_bytes;   // unfused fallback: full convT output
   int64_t ws_total;
@@ -104,6 +107,18 @@ struct SmemLayout {
 SmemLayout smem_layout(const Plan& pl);
 
 // Fill *plan for problem pb.  Returns plan->status.
+// Engine grid: one persistent CTA per SM, never more CTAs than tiles.
+inline int64_t engine_grid(const Plan& pl, int sm_count) {
+  return std::min<int64_t>(std::min<int64_t>(pl.tiles, sm_count), kMaxGrid);
+}
+
+// Slots of the fused BatchNorm partial sums per channel: with one column
+// block every epilogue warp of the grid keeps its own running sums (one slot
+// each), otherwise every tile writes one slot.
+inline int64_t bn_part_slots(const Plan& pl, int64_t grid) {
+  return pl.n_colblocks == 1 ? grid * kBnEpiWarps : pl.tiles;
+}
+
 int make_plan(const Problem& pb, Plan* plan);
 
 // Integer output length of one axis.
