@@ -87,6 +87,21 @@ __device__ __forceinline__ void row_local(const EngineParams& p, int a, int q, i
   t[2] = (p2 << p.lQ[2]) + l2;
 }
 
+// global row coordinates of (accumulator a, lane quarter q, lane l) in the
+// tile at origin o, and whether the row lies inside M
+__device__ __forceinline__ bool row_global(const EngineParams& p, const int (&o)[3], int a, int q,
+                                           int l, int (&m)[3]) {
+  int t[3];
+  row_local(p, a, q, l, t);
+  bool rv = true;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    m[i] = o[i] + t[i];
+    rv = rv && m[i] < p.M[i];
+  }
+  return rv;
+}
+
 __device__ __forceinline__ void raise_abort(const EngineParams& p, volatile int* abortf) {
   *abortf = 1;
   atomicExch(p.err, 1);
@@ -96,38 +111,56 @@ __device__ __forceinline__ float tf32_trunc(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// Value index whose total reduce_scatter16_sum leaves in a lane.
-__device__ __forceinline__ int scatter16_index(int lane) {
-  return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
-}
-
-// Sum 16 values over all 32 lanes; lane ends with the total of value index
-// 8*b4 + 4*b3 + 2*b2 + b1 (b = lane bits).
-__device__ __forceinline__ float reduce_scatter16_sum(const float (&v)[16], int lane) {
-  float w8[8], w4[4], w2[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float send = b4 ? v[i] : v[i + 8];
-    const float keep = b4 ? v[i + 8] : v[i];
-    w8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
+// Sum 8 values over all 32 lanes; lane ends with the total of value index
+// 4*b4 + 2*b3 + b2 (b = lane bits).
+__device__ __forceinline__ float reduce_scatter8_sum(const float (&v)[8], int lane) {
+  float w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float send = b3 ? w8[i] : w8[i + 4];
-    const float keep = b3 ? w8[i + 4] : w8[i];
-    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    const float send = b4 ? v[i] : v[i + 4];
+    const float keep = b4 ? v[i + 4] : v[i];
+    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const float send = b2 ? w4[i] : w4[i + 2];
-    const float keep = b2 ? w4[i + 2] : w4[i];
-    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    const float send = b3 ? w4[i] : w4[i + 2];
+    const float keep = b3 ? w4[i + 2] : w4[i];
+    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
   }
-  const float send = b1 ? w2[0] : w2[1];
-  const float keep = b1 ? w2[1] : w2[0];
-  const float w1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  const float send = b2 ? w2[0] : w2[1];
+  const float keep = b2 ? w2[1] : w2[0];
+  float w1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
   return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
+}
+__device__ __forceinline__ int scatter8_index(int lane) {
+  return 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+}
+
+// Sum 8 values over the 8 lanes of a 2x2x2 pool window (lane bits 0, 3, 4);
+// lane ends with the total of value index 4*b0 + 2*b3 + b4.
+__device__ __forceinline__ float reduce_scatter8_window_sum(const float (&v)[8], int lane) {
+  float w4[4], w2[2];
+  const bool b0 = lane & 1, b3 = lane & 8, b4 = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b0 ? v[i] : v[i + 4];
+    const float keep = b0 ? v[i + 4] : v[i];
+    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? w4[i] : w4[i + 2];
+    const float keep = b3 ? w4[i + 2] : w4[i];
+    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float send = b4 ? w2[0] : w2[1];
+  const float keep = b4 ? w2[1] : w2[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 16);
+}
+__device__ __forceinline__ int window8_index(int lane) {
+  return 4 * (lane & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 4) & 1);
 }
 
 // Reduce 16 values over the 8 lanes of a 2x2x2 pool window (lane bits 0, 3,
@@ -335,10 +368,12 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       mbar_init(bars.a_full(i), a_full_count);
       mbar_init(bars.a_empty(i), issuers);
     }
+    // BatchNorm pooling: both epilogue groups work on every tile
+    const uint32_t epi_arrivals = EPI == EPI_BN_POOL ? 2 * kEpiGroup : kEpiGroup;
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.d_full(i), issuers);
-      mbar_init(bars.d_empty(i), kEpiGroup);
-      mbar_init(bars.epi(i), kEpiGroup);
+      mbar_init(bars.d_empty(i), epi_arrivals);
+      mbar_init(bars.epi(i), epi_arrivals);
     }
     *abortf = 0;
     fence_barrier_init();
@@ -584,32 +619,18 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     const long long o12 = (long long)p.O[1] * p.O[2];
     int it_d = 0;
     bool ok = true;
-    // BatchNorm partial sums (bias-free values) of the 16 channels this lane
-    // sees.  With one column block they run over every tile this warp takes
-    // and are written once at the end, to this warp's own slot; with several
-    // they are reduced and written per tile.
-    float s1[16], s2[16];
+    // BatchNorm partial sums (bias-free values) of the 8 channels this
+    // lane's group takes.  With one column block they run over every tile
+    // and are written once at the end, to the slot of this CTA and lane
+    // quarter; with several they are reduced and written per tile.
+    float s1[8], s2[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       s1[i] = 0.f;
       s2[i] = 0.f;
     }
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
-      // per accumulator: row coordinates of this lane
-      int m[4][3];
-      bool rvalid[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        int t[3];
-        row_local(p, a < p.n_acc ? a : 0, q, lane, t);
-        rvalid[a] = true;
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          m[a][i] = tc.o[i] + t[i];
-          rvalid[a] = rvalid[a] && m[a][i] < p.M[i];
-        }
-      }
       // pool-LSE running state per accumulator (channels this lane holds)
       float lse_m[4], lse_s[4];
 #pragma unroll
@@ -618,9 +639,10 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
         lse_s[a] = 0.f;
       }
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
-        // with two accumulator buffers group g takes buffer g; with one,
-        // group 0 takes every tile
-        if (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0)) continue;
+        // BatchNorm pooling: both groups take every tile (group g the
+        // channels 8g..8g+7).  Otherwise, with two accumulator buffers group
+        // g takes buffer g; with one, group 0 takes every tile.
+        if (EPI != EPI_BN_POOL && (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0))) continue;
         const int g = cb / p.nb_per_group, nb = cb % p.nb_per_group;
         const int oc0 = g * p.cout_g + nb * p.ocb;
         const int ocb_valid = min(p.ocb, p.cout_g - nb * p.ocb);
@@ -656,16 +678,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 #pragma unroll 1
             for (int a = 0; a < p.n_acc; ++a) {
               const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
-              int mm[3] = {0, 0, 0};
-              bool rv = false;
-#pragma unroll
-              for (int aa = 0; aa < 4; ++aa)
-                if (aa == a) {
-                  mm[0] = m[aa][0];
-                  mm[1] = m[aa][1];
-                  mm[2] = m[aa][2];
-                  rv = rvalid[aa];
-                }
+              int mm[3];
+              const bool rv = row_global(p, tc.o, a, q, lane, mm);
               const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1],
                         zb2 = p.s_out[2] * mm[2];
               uint32_t mask = 0;
@@ -709,16 +723,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 #pragma unroll 1
             for (int a = 0; a < p.n_acc; ++a) {
               const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
-              int mm[3] = {0, 0, 0};
-              bool rv = false;
-#pragma unroll
-              for (int aa = 0; aa < 4; ++aa)
-                if (aa == a) {
-                  mm[0] = m[aa][0];
-                  mm[1] = m[aa][1];
-                  mm[2] = m[aa][2];
-                  rv = rvalid[aa];
-                }
+              int mm[3];
+              const bool rv = row_global(p, tc.o, a, q, lane, mm);
               const int zb0 = p.s_out[0] * mm[0], zb1 = p.s_out[1] * mm[1],
                         zb2 = p.s_out[2] * mm[2];
               const long long ybase = (long long)tc.n * p.Cout * ovol + (long long)zb0 * o12 +
@@ -813,7 +819,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 ss = (ss > 0.f ? ss * expf(mm - nm) : 0.f) + (os > 0.f ? os * expf(om - nm) : 0.f);
                 mm = nm;
               }
-              const int w0 = m[a][0] >> 1, w1 = m[a][1] >> 1, w2 = m[a][2] >> 1;
+              int mm3[3];
+              row_global(p, tc.o, a, q, lane, mm3);
+              const int w0 = mm3[0] >> 1, w1 = mm3[1] >> 1, w2 = mm3[2] >> 1;
               if ((lane & 0x19) == 0 && w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2]) {
                 const float l = mm + logf(ss);
                 p.y[(((long long)tc.n * p.P[0] + w0) * p.P[1] + w1) * p.P[2] + w2] = fmaxf(l, 0.f);
@@ -821,39 +829,32 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             }
           }
         } else {  // EPI_BN_POOL: stride-2 transposed conv, 8 classes per row (oc-major columns)
-          const int bsel = 8 * (lane & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
+          // group g takes the channels 8g .. 8g+7 of the column block: 64
+          // columns, two TMEM loads in flight together
+          const int ch0 = 8 * egroup;
+          const int nch = min(8, ocb_valid - ch0);
 #pragma unroll 1
-          for (int a = 0; a < p.n_acc; ++a) {
-            const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
-            int mm[3] = {0, 0, 0};
-            bool rv = false;
-#pragma unroll
-            for (int aa = 0; aa < 4; ++aa)
-              if (aa == a) {
-                mm[0] = m[aa][0];
-                mm[1] = m[aa][1];
-                mm[2] = m[aa][2];
-                rv = rvalid[aa];
-              }
+          for (int a = 0; a < p.n_acc && nch > 0; ++a) {
+            const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols + 8 * ch0);
+            int mm[3];
+            const bool rv = row_global(p, tc.o, a, q, lane, mm);
             // class r = 4 r0 + 2 r1 + r2 lies inside the output iff 2m + r < O
-            uint32_t vmask = 0;
+            // on every axis: bit r of the product of per-axis class masks
+            const uint32_t m0 = (2 * mm[0] < p.O[0] ? 0x0fu : 0u) | (2 * mm[0] + 1 < p.O[0] ? 0xf0u : 0u);
+            const uint32_t m1 = (2 * mm[1] < p.O[1] ? 0x33u : 0u) | (2 * mm[1] + 1 < p.O[1] ? 0xccu : 0u);
+            const uint32_t m2 = (2 * mm[2] < p.O[2] ? 0x55u : 0u) | (2 * mm[2] + 1 < p.O[2] ? 0xaau : 0u);
+            const uint32_t vmask = rv ? (m0 & m1 & m2) : 0u;
+            uint32_t u[64];
+            tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+            if (nch > 4) tmem_ld32(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+            tmem_wait_ld();
+            float ps[8];
+            if (__all_sync(0xffffffffu, vmask == 0xffu)) {
+              // every row of the warp has all 8 classes inside the output
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const bool in = rv && 2 * mm[0] + (r >> 2) < p.O[0] &&
-                              2 * mm[1] + ((r >> 1) & 1) < p.O[1] && 2 * mm[2] + (r & 1) < p.O[2];
-              vmask |= (in ? 1u : 0u) << r;
-            }
-            float ps[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ps[i] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {  // 32 columns = 4 channels x 8 classes
-              if (cc * 32 >= p.n_tile) break;
-              uint32_t u[32];
-              tmem_ld32(taddr + (uint32_t)(cc * 32), u);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
+              for (int h = 0; h < 8; ++h) {
+                ps[h] = 0.f;
+                if (h >= 4 && nch <= 4) continue;
                 float sum = 0.f, sq = 0.f;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -861,58 +862,58 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                   sum += v;
                   sq = fmaf(v, v, sq);
                 }
-                if (vmask != 0xffu) {
-                  // a row on the output's far faces (or past M): only the
-                  // classes inside the output count.  Its 4^3 window index is
-                  // at least P on that axis, so its pooled sum is never
-                  // stored and the masked sum can serve for it too.
-                  sum = 0.f;
-                  sq = 0.f;
+                ps[h] = sum;
+                s1[h] += sum;
+                s2[h] += sq;
+              }
+            } else {
+              // rows on the output's far faces (or past M): only the classes
+              // inside the output count.  Such a row's 4^3 window index is at
+              // least P on that axis, so its pooled sum is never stored and
+              // the masked sum can serve for it too.
 #pragma unroll
-                  for (int r = 0; r < 8; ++r) {
-                    const float v = ((vmask >> r) & 1) ? __uint_as_float(u[h * 8 + r]) : 0.f;
-                    sum += v;
-                    sq = fmaf(v, v, sq);
-                  }
+              for (int h = 0; h < 8; ++h) {
+                ps[h] = 0.f;
+                if (h >= 4 && nch <= 4) continue;
+                float sum = 0.f, sq = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const float v = ((vmask >> r) & 1) ? __uint_as_float(u[h * 8 + r]) : 0.f;
+                  sum += v;
+                  sq = fmaf(v, v, sq);
                 }
-                ps[4 * cc + h] = sum;
-                s1[4 * cc + h] += sum;
-                s2[4 * cc + h] += sq;
+                ps[h] = sum;
+                s1[h] += sum;
+                s2[h] += sq;
               }
             }
             // pooled sums over the 8 rows of each 4x4x4 window
-            float pw[2];
-            reduce_scatter16_window<false>(ps, lane, pw);
+            const float pw = reduce_scatter8_window_sum(ps, lane);
             const int w0 = mm[0] >> 1, w1 = mm[1] >> 1, w2 = mm[2] >> 1;
-            if (w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2]) {
-              // lanes of a window group hold different channel pairs
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int oc_l = bsel + h;
-                if (oc_l < ocb_valid) {
-                  const int oc = oc0 + oc_l;
-                  const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
-                  p.y[(((long long)tc.n * p.Cout + oc) * p.P[0] + w0) * p.P[1] * p.P[2] +
-                      (long long)w1 * p.P[2] + w2] = pw[h] * (1.0f / 64.0f) + b;
-                }
-              }
+            const int oc_l = ch0 + window8_index(lane);
+            if (w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2] && oc_l < ocb_valid) {
+              const int oc = oc0 + oc_l;
+              const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+              p.y[(((long long)tc.n * p.Cout + oc) * p.P[0] + w0) * p.P[1] * p.P[2] +
+                  (long long)w1 * p.P[2] + w2] = pw * (1.0f / 64.0f) + b;
             }
           }
           if (p.n_colblocks > 1) {
-            // BatchNorm partial sums of this tile: all lanes, then all 4 warps
-            const float t1 = reduce_scatter16_sum(s1, lane);
-            const float t2 = reduce_scatter16_sum(s2, lane);
+            // BatchNorm partial sums of this tile: all lanes, then the 4
+            // quarters of both groups
+            const float t1 = reduce_scatter8_sum(s1, lane);
+            const float t2 = reduce_scatter8_sum(s2, lane);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
               s1[i] = 0.f;
               s2[i] = 0.f;
             }
             float2* red = reinterpret_cast<float2*>(gbase + p.sm_misc) + (it_d & 1) * 64;
-            if ((lane & 1) == 0) red[ew * 16 + scatter16_index(lane)] = make_float2(t1, t2);
+            if ((lane & 3) == 0) red[ew * 16 + ch0 + scatter8_index(lane)] = make_float2(t1, t2);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.epi(it_d & 1));
-            if (ew == 0) {
+            if (warp == kWarpEpi0) {
               ok = mbar_wait(bars.epi(it_d & 1), (it_d >> 1) & 1, tmo, abortf);
               if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
@@ -938,12 +939,13 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     }
     if constexpr (EPI == EPI_BN_POOL) {
       if (ok && p.n_colblocks == 1) {
-        // slot of this warp: CTA-major, then epilogue warp
-        const float t1 = reduce_scatter16_sum(s1, lane);
-        const float t2 = reduce_scatter16_sum(s2, lane);
-        const int oc = scatter16_index(lane);
-        const int slot = blockIdx.x * WarpCfg<EPI>::kEpiWarps + (warp - kWarpEpi0);
-        if ((lane & 1) == 0 && oc < p.cout_g)
+        // slot: CTA-major, then lane quarter; each channel's slots are all
+        // written by the 4 warps of the group that takes it
+        const float t1 = reduce_scatter8_sum(s1, lane);
+        const float t2 = reduce_scatter8_sum(s2, lane);
+        const int oc = 8 * egroup + scatter8_index(lane);
+        const int slot = blockIdx.x * kBnSlotsPerCta + ew;
+        if ((lane & 3) == 0 && oc < p.cout_g)
           p.partials[(size_t)oc * p.part_slots + slot] = make_float2(t1, t2);
       }
     }
@@ -956,8 +958,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   if (warp == kWarpMMA) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-static_assert(WarpCfg<EPI_BN_POOL>::kEpiWarps == kBnEpiWarps,
-              "BatchNorm partial slots are counted per epilogue warp");
+static_assert(WarpCfg<EPI_BN_POOL>::kEpiWarps == 2 * kEpiGroup && kBnSlotsPerCta == kEpiGroup,
+              "BatchNorm pooling: two groups of 8 channels, one partial slot per lane quarter");
 
 template __global__ void engine_kernel<EPI_STORE>(const __grid_constant__ EngineParams p);
 template __global__ void engine_kernel<EPI_POOL_LSE>(const __grid_constant__ EngineParams p);

@@ -29,7 +29,7 @@ constexpr int kMaxBStagesPlan = 16; // streamed weight stages (mbarrier pairs in
 constexpr int kTmemCols = 512;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxGrid = 1024;      // CTAs of a persistent engine launch, at most
-constexpr int kBnEpiWarps = 8;      // epilogue warps of the BatchNorm-pool engine
+constexpr int kBnSlotsPerCta = 4;   // BatchNorm partial slots per CTA (one per lane quarter)
 
 struct Problem {
   int op;
@@ -113,10 +113,10 @@ inline int64_t engine_grid(const Plan& pl, int sm_count) {
 }
 
 // Slots of the fused BatchNorm partial sums per channel: with one column
-// block every epilogue warp of the grid keeps its own running sums (one slot
-// each), otherwise every tile writes one slot.
+// block every CTA keeps running sums per TMEM lane quarter (one slot each),
+// otherwise every tile writes one slot.
 inline int64_t bn_part_slots(const Plan& pl, int64_t grid) {
-  return pl.n_colblocks == 1 ? grid * kBnEpiWarps : pl.tiles;
+  return pl.n_colblocks == 1 ? grid * kBnSlotsPerCta : pl.tiles;
 }
 
 int make_plan(const Problem& pb, Plan* plan);
