@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   // ================= raw-input producer =================
   if (warp == kWarpRaw) {
     const int bvol = p.box[0] * p.box[1] * p.box[2];
-    int it = 0;
+    int rs = 0;        // raw ring stage
+    uint32_t rph = 0;  // and its phase
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
       if (*abortf) break;
       const TileCoord tc = decode_tile(p, tile);
@@ -415,11 +416,17 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       const int yc = p.s_in[1] * tc.o[1] + p.u_min[1];
       const int xc = (p.s_in[2] * tc.o[2] + p.u_min[2]) & ~3;
       bool ok = true;
-      for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
-        const int g = cb / p.nb_per_group;
-        for (int c = 0; c < p.n_chunks; ++c, ++it) {
-          const int stage = it % p.raw_stages;
-          ok = mbar_wait(bars.raw_empty(stage), ((it / p.raw_stages) & 1) ^ 1, tmo, abortf);
+      // column block cb belongs to group g (nb_per_group blocks per group)
+      for (int cb = 0, g = 0, nb = 0; cb < p.n_colblocks && ok;
+           ++cb, nb = (nb + 1 == p.nb_per_group) ? 0 : nb + 1, g += (nb == 0)) {
+        for (int c = 0; c < p.n_chunks; ++c) {
+          const int stage = rs;
+          const uint32_t par = rph ^ 1;
+          if (++rs == p.raw_stages) {
+            rs = 0;
+            rph ^= 1;
+          }
+          ok = mbar_wait(bars.raw_empty(stage), par, tmo, abortf);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             if (lane == 0) raise_abort(p, abortf);
@@ -469,16 +476,18 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
           bulk_g2s(sbase + p.sm_b + s * p.b_stage_bytes,
                    p.wpack + (size_t)s * (p.b_stage_bytes / 4), p.b_stage_bytes, bars.b_full(0));
       } else {
-        int it = 0;
+        int stage = 0;       // weight ring stage
+        uint32_t bph = 0;    // and its phase
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
           for (int cb = 0; cb < p.n_colblocks && ok; ++cb)
             for (int c = 0; c < p.n_chunks && ok; ++c)
-              for (int j = 0; j < p.ksteps_chunk; j += p.ks_stage, ++it) {
-                const int stage = it % p.b_stages;
+              for (int j = 0; j < p.ksteps_chunk;
+                   j += p.ks_stage, stage = (stage + 1 == p.b_stages) ? 0 : stage + 1,
+                       bph ^= (stage == 0)) {
                 const uint32_t bytes =
                     (uint32_t)(min(p.ks_stage, p.ksteps_chunk - j) * 64 * p.n_tile);
-                if (!mbar_wait(bars.b_empty(stage), ((it / p.b_stages) & 1) ^ 1, tmo, abortf)) {
+                if (!mbar_wait(bars.b_empty(stage), bph ^ 1, tmo, abortf)) {
                   raise_abort(p, abortf);
                   ok = false;
                   break;
@@ -538,8 +547,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                     p.s_in[2] * t[2];
     }
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(p, tile);
-      const int xs = p.s_in[2] * tc.o[2] + p.u_min[2];
+      // only the x origin of the tile matters here (its alignment shift)
+      const int b2 = tile - fast_div(p.ntile_div[2], tile) * p.ntile[2];
+      const int xs = p.s_in[2] * (b2 * p.T[2]) + p.u_min[2];
       const int xshift = xs - (xs & ~3);
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
         for (int c = 0; c < p.n_chunks && ok; ++c) {
@@ -638,16 +648,18 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
         lse_m[a] = -INFINITY;
         lse_s[a] = 0.f;
       }
-      for (int cb = 0; cb < p.n_colblocks && ok; ++cb, ++it_d) {
+      // column block cb is block nb of group g
+      for (int cb = 0, g = 0, nb = 0; cb < p.n_colblocks && ok;
+           ++cb, ++it_d, nb = (nb + 1 == p.nb_per_group) ? 0 : nb + 1, g += (nb == 0)) {
         // BatchNorm pooling: both groups take every tile (group g the
         // channels 8g..8g+7).  Otherwise, with two accumulator buffers group
         // g takes buffer g; with one, group 0 takes every tile.
         if (EPI != EPI_BN_POOL && (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0))) continue;
-        const int g = cb / p.nb_per_group, nb = cb % p.nb_per_group;
         const int oc0 = g * p.cout_g + nb * p.ocb;
         const int ocb_valid = min(p.ocb, p.cout_g - nb * p.ocb);
-        const int dslot = it_d % p.dbuf;
-        ok = mbar_wait(bars.d_full(dslot), (it_d / p.dbuf) & 1, tmo, abortf);
+        const int dslot = p.dbuf == 2 ? (it_d & 1) : 0;
+        const uint32_t dpar = (uint32_t)(p.dbuf == 2 ? (it_d >> 1) : it_d) & 1u;
+        ok = mbar_wait(bars.d_full(dslot), dpar, tmo, abortf);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           if (lane == 0) raise_abort(p, abortf);
@@ -838,54 +850,42 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols + 8 * ch0);
             int mm[3];
             const bool rv = row_global(p, tc.o, a, q, lane, mm);
-            // class r = 4 r0 + 2 r1 + r2 lies inside the output iff 2m + r < O
-            // on every axis: bit r of the product of per-axis class masks
-            const uint32_t m0 = (2 * mm[0] < p.O[0] ? 0x0fu : 0u) | (2 * mm[0] + 1 < p.O[0] ? 0xf0u : 0u);
-            const uint32_t m1 = (2 * mm[1] < p.O[1] ? 0x33u : 0u) | (2 * mm[1] + 1 < p.O[1] ? 0xccu : 0u);
-            const uint32_t m2 = (2 * mm[2] < p.O[2] ? 0x55u : 0u) | (2 * mm[2] + 1 < p.O[2] ? 0xaau : 0u);
-            const uint32_t vmask = rv ? (m0 & m1 & m2) : 0u;
+            // Class r = 4 r0 + 2 r1 + r2 lies inside the output iff 2m + r < O
+            // on every axis.  A row inside M always has 2m < O, so class r is
+            // in iff f_i = [2 m_i + 1 < O_i] holds on every axis with r_i = 1:
+            // its weight is f0^r0 f1^r1 f2^r2, and the class sums below nest
+            // as a tree of FMAs over those 0/1 weights.  Rows past M drop out
+            // through the weight fr of their running sums.
+            const float f0 = 2 * mm[0] + 1 < p.O[0] ? 1.f : 0.f;
+            const float f1 = 2 * mm[1] + 1 < p.O[1] ? 1.f : 0.f;
+            const float f2 = 2 * mm[2] + 1 < p.O[2] ? 1.f : 0.f;
+            const float fr = rv ? 1.f : 0.f;
             uint32_t u[64];
             tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
             if (nch > 4) tmem_ld32(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
             tmem_wait_ld();
             float ps[8];
-            if (__all_sync(0xffffffffu, vmask == 0xffu)) {
-              // every row of the warp has all 8 classes inside the output
 #pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                ps[h] = 0.f;
-                if (h >= 4 && nch <= 4) continue;
-                float sum = 0.f, sq = 0.f;
+            for (int h = 0; h < 8; ++h) {
+              ps[h] = 0.f;
+              if (h >= 4 && nch <= 4) continue;
+              float a[4], c[4];  // per (r0, r1): classes r2 = 0, 1 combined
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                  const float v = __uint_as_float(u[h * 8 + r]);
-                  sum += v;
-                  sq = fmaf(v, v, sq);
-                }
-                ps[h] = sum;
-                s1[h] += sum;
-                s2[h] += sq;
+              for (int k = 0; k < 4; ++k) {
+                const float ve = __uint_as_float(u[h * 8 + 2 * k]);
+                const float vo = __uint_as_float(u[h * 8 + 2 * k + 1]);
+                const float w = f2 * vo;
+                a[k] = ve + w;
+                c[k] = fmaf(w, vo, ve * ve);
               }
-            } else {
-              // rows on the output's far faces (or past M): only the classes
-              // inside the output count.  Such a row's 4^3 window index is at
-              // least P on that axis, so its pooled sum is never stored and
-              // the masked sum can serve for it too.
-#pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                ps[h] = 0.f;
-                if (h >= 4 && nch <= 4) continue;
-                float sum = 0.f, sq = 0.f;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                  const float v = ((vmask >> r) & 1) ? __uint_as_float(u[h * 8 + r]) : 0.f;
-                  sum += v;
-                  sq = fmaf(v, v, sq);
-                }
-                ps[h] = sum;
-                s1[h] += sum;
-                s2[h] += sq;
-              }
+              const float sum = fmaf(f0, fmaf(f1, a[3], a[2]), fmaf(f1, a[1], a[0]));
+              const float sq = fmaf(f0, fmaf(f1, c[3], c[2]), fmaf(f1, c[1], c[0]));
+              // a row whose window is stored has every class inside the
+              // output (its window index is below P on every axis), so this
+              // is then the plain sum over the 8 classes
+              ps[h] = sum;
+              s1[h] = fmaf(fr, sum, s1[h]);
+              s2[h] = fmaf(fr, sq, s2[h]);
             }
             // pooled sums over the 8 rows of each 4x4x4 window
             const float pw = reduce_scatter8_window_sum(ps, lane);
