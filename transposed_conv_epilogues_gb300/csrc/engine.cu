@@ -361,11 +361,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       mbar_init(bars.b_full(i), 1);
       mbar_init(bars.b_empty(i), issuers);
     }
-    // with one accumulator the two conversion groups take alternate K-steps
-    // (4 warps fill a stage); otherwise both groups fill every stage
-    const uint32_t a_full_count = p.n_acc >= 2 ? kNumConvWarps : kNumConvWarps / 2;
+    // both conversion groups fill every A-stage (alternate K-steps of it)
     for (int i = 0; i < kMaxAStages; ++i) {
-      mbar_init(bars.a_full(i), a_full_count);
+      mbar_init(bars.a_full(i), kNumConvWarps);
       mbar_init(bars.a_empty(i), issuers);
     }
     // BatchNorm pooling: both epilogue groups work on every tile
@@ -523,17 +521,16 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   // ================= conversion warps =================
   // The first and last four conversion warps are two groups; each covers
   // all four TMEM lane quarters.  An A-stage holds ks_stage K-steps of all
-  // accumulators (16 columns each: x then x_lo).  With two or more accumulators, group g fills the
-  // accumulators a with a % 2 == g of every stage; with one accumulator the
-  // groups take alternate K-steps.
+  // accumulators (16 columns each: x then x_lo).  Group g fills the K-steps
+  // kk with kk % 2 == g of every stage, for all accumulators, so that a warp
+  // has the gathers of n_acc rows in flight at once.
   else if (warp >= kWarpConv0) {
     const int cw = warp - kWarpConv0;
     const int half = cw >> 2;
     const int q = warp & 3;
     const int* ktab = reinterpret_cast<const int*>(gbase + p.sm_ktab);
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    const bool split_acc = p.n_acc >= 2;
-    int rstage = 0, as = 0, kglob = 0;
+    int rstage = 0, as = 0;
     uint32_t rphase = 0, aphase = 0;
     bool ok = true;
     // raw-box offset of this lane's row of each accumulator, before the
@@ -564,9 +561,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               xshift;
           const int cin_valid = min(p.cin_chunk, p.cin_g - c * p.cin_chunk);
           const int valid_k = cin_valid * p.nUtot;
-          for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage, ++kglob) {
-            const bool mine = split_acc || ((kglob & 1) == half);
-            if (mine) {
+          for (int j0 = 0; j0 < p.ksteps_chunk; j0 += p.ks_stage) {
+            {  // fill this group's K-steps of A-stage as
               ok = __all_sync(0xffffffffu, mbar_wait(bars.a_empty(as), aphase ^ 1, tmo, abortf));
               if (!ok) {
                 if (lane == 0) raise_abort(p, abortf);
@@ -576,24 +572,31 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               const uint32_t stage_col =
                   tmem_base + lane_addr + a_col0 + (uint32_t)(as * 16 * p.n_acc * p.ks_stage);
               const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
-              for (int kk = 0; kk < kcount; ++kk) {
+              for (int kk = half; kk < kcount; kk += 2) {
                 const int j = j0 + kk;
                 const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
                 const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
                 const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
                 const int kbase = j * 8;
                 const uint32_t kcol = stage_col + (uint32_t)(kk * 16 * p.n_acc);
+                // the gathers of all accumulators first (independent loads in
+                // flight together), then the splits and TMEM stores
+                float xg[4][8];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
                   if (a >= p.n_acc) break;
-                  if (split_acc && (a & 1) != half) continue;
                   const float* rp = raw + row_base[a];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) xg[a][e] = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                  if (a >= p.n_acc) break;
                   uint32_t v[16];
 #pragma unroll
                   for (int e = 0; e < 8; ++e) {
-                    const float xv = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
-                    v[e] = __float_as_uint(xv);
-                    v[8 + e] = __float_as_uint(xv - tf32_trunc(xv));
+                    v[e] = __float_as_uint(xg[a][e]);
+                    v[8 + e] = __float_as_uint(xg[a][e] - tf32_trunc(xg[a][e]));
                   }
                   tmem_st16(kcol + (uint32_t)(a * 16), v);
                 }
