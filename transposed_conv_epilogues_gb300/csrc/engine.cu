@@ -655,9 +655,12 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       for (int cb = 0, g = 0, nb = 0; cb < p.n_colblocks && ok;
            ++cb, ++it_d, nb = (nb + 1 == p.nb_per_group) ? 0 : nb + 1, g += (nb == 0)) {
         // BatchNorm pooling: both groups take every tile (group g the
-        // channels 8g..8g+7).  Otherwise, with two accumulator buffers group
-        // g takes buffer g; with one, group 0 takes every tile.
-        if (EPI != EPI_BN_POOL && (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0))) continue;
+        // channels 8g..8g+7).  A single group (pool + logsumexp) takes every
+        // tile too.  Otherwise, with two accumulator buffers group g takes
+        // buffer g; with one, group 0 takes every tile.
+        constexpr bool kAllTiles =
+            EPI == EPI_BN_POOL || WarpCfg<EPI>::kEpiWarps == kEpiGroup;
+        if (!kAllTiles && (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0))) continue;
         const int oc0 = g * p.cout_g + nb * p.ocb;
         const int ocb_valid = min(p.ocb, p.cout_g - nb * p.ocb);
         const int dslot = p.dbuf == 2 ? (it_d & 1) : 0;

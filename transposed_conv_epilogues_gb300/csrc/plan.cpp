@@ -239,11 +239,14 @@ int make_plan(const Problem& pb_in, Plan* out) {
   }
 
   // ---- accumulators per tile, TMEM budget
-  // Short MMAs (N <= 64) issue about as fast as the tensor core executes them,
-  // so when TMEM allows two accumulators the x.w and x.w_lo products are
-  // fused into one MMA over the adjacent [w | w_lo] weight block (N = 2
-  // n_tile), its two halves summed in the epilogue.
-  pl.dbuf = (pl.epi == EPI_POOL_LSE || pl.n_tile > 128) ? 1 : 2;
+  // Accumulators are double-buffered (the epilogue drains one buffer while
+  // the MMAs fill the other) whenever two buffers of at least one 128-row
+  // accumulator fit in half of TMEM.  Short MMAs (N <= 64) issue about as
+  // fast as the tensor core executes them, so when TMEM still allows two
+  // accumulators per buffer the x.w and x.w_lo products are fused into one
+  // MMA over the adjacent [w | w_lo] weight block (N = 2 n_tile), its two
+  // halves summed in the epilogue.
+  pl.dbuf = pl.n_tile > 128 ? 1 : 2;
   pl.wide = (pl.epi != EPI_BN_POOL && 2 * pl.n_tile <= 128 &&
              256 / (pl.dbuf * 2 * pl.n_tile) >= 2)
                 ? 1
