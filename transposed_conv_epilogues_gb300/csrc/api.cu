@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -151,6 +152,23 @@ void fill_params(const Plan& pl, EngineParams* ep) {
     ep->lPq[a] = 0;
     while ((1 << ep->lPq[a]) < pl.Pq[a]) ++ep->lPq[a];
     ep->box[a] = pl.box[a];
+  }
+  {
+    // class tables of the one-class store path: at most 8 classes, whose
+    // offsets from a row's first output fit in an int
+    const int F = pl.s_out[0] * pl.s_out[1] * pl.s_out[2];
+    const long long o12 = (long long)pl.O[1] * pl.O[2];
+    ep->cls_fast = pl.nR == 1 && F <= 8;
+    for (int f = 0; f < 8 && f < F; ++f) {
+      const int r2 = f % pl.s_out[2], r1 = (f / pl.s_out[2]) % pl.s_out[1],
+                r0 = f / (pl.s_out[2] * pl.s_out[1]);
+      const long long off = r0 * o12 + (long long)r1 * pl.O[2] + r2;
+      if (off > INT32_MAX) ep->cls_fast = 0;
+      ep->cls_off[f] = (int)std::min<long long>(off, INT32_MAX);
+      ep->cls_r[f] = r0 | (r1 << 8) | (r2 << 16);
+      if (pl.nR == 1 && r0 == pl.r_axis[0][0] && r1 == pl.r_axis[1][0] && r2 == pl.r_axis[2][0])
+        ep->cls_star = f;
+    }
   }
   ep->nUtot = pl.nU[0] * pl.nU[1] * pl.nU[2];
   ep->nR = pl.nR;

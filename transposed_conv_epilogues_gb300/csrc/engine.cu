@@ -676,23 +676,46 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 
         if constexpr (EPI == EPI_STORE) {
           const int F = p.s_out[0] * p.s_out[1] * p.s_out[2];
-          if (p.nR == 1 && F <= 8) {
-            // fast path: one class with taps (fstar), the others hold the bias.
-            // Class f = (r0, r1, r2) of the full s_out grid sits at offset
-            // off[f] from the row's first output.
-            int off[8], rr[8][3];
-            int fstar = 0;
+          if (F == 1) {
+            // a convolution (or a stride-1 transposed one): one output per
+            // row and channel.  Column chunks outer, so that each chunk's
+            // bias is loaded once for all accumulators; a full chunk stores
+            // its 32 channels without bound checks.
+            for (int cc = 0; cc < p.n_tile; cc += 32) {
+              const int oc_lane = cc + lane;
+              const float bl =
+                  (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
+              const bool full = cc + 32 <= ocb_valid;
+#pragma unroll 1
+              for (int a = 0; a < p.n_acc; ++a) {
+                uint32_t v[32];
+                load_acc32(dbase + (uint32_t)(a * p.acc_cols + cc), lo_off, v);
+                int mm[3];
+                const bool rv = row_global(p, tc.o, a, q, lane, mm);
+                float* yo = p.y + ((long long)tc.n * p.Cout + oc0 + cc) * ovol +
+                            (long long)mm[0] * o12 + (long long)mm[1] * p.O[2] + mm[2];
+                if (full) {
 #pragma unroll
-            for (int f = 0; f < 8; ++f) {
-              const int r2 = f % p.s_out[2], r1 = (f / p.s_out[2]) % p.s_out[1],
-                        r0 = f / (p.s_out[2] * p.s_out[1]);
-              rr[f][0] = r0;
-              rr[f][1] = r1;
-              rr[f][2] = r2;
-              off[f] = (int)(r0 * o12 + (long long)r1 * p.O[2] + r2);
-              if (f < F && r0 == p.r_axis[0][0] && r1 == p.r_axis[1][0] && r2 == p.r_axis[2][0])
-                fstar = f;
+                  for (int jj = 0; jj < 32; ++jj) {
+                    const float b = __shfl_sync(0xffffffffu, bl, jj);
+                    if (rv) *yo = __uint_as_float(v[jj]) + b;
+                    yo += ovol;
+                  }
+                } else {
+#pragma unroll
+                  for (int jj = 0; jj < 32; ++jj) {
+                    if (cc + jj >= ocb_valid) break;
+                    const float b = __shfl_sync(0xffffffffu, bl, jj);
+                    if (rv) *yo = __uint_as_float(v[jj]) + b;
+                    yo += ovol;
+                  }
+                }
+              }
             }
+          } else if (p.cls_fast) {
+            // one class with taps (cls_star), the others hold the bias.
+            // Class f = (r0, r1, r2) of the s_out grid sits at offset
+            // cls_off[f] from the row's first output (tables from the host).
 #pragma unroll 1
             for (int a = 0; a < p.n_acc; ++a) {
               const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
@@ -702,37 +725,30 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                         zb2 = p.s_out[2] * mm[2];
               uint32_t mask = 0;
 #pragma unroll
-              for (int f = 0; f < 8; ++f)
-                if (rv && f < F && zb0 + rr[f][0] < p.O[0] && zb1 + rr[f][1] < p.O[1] &&
-                    zb2 + rr[f][2] < p.O[2])
+              for (int f = 0; f < 8; ++f) {
+                const int r = p.cls_r[f];
+                if (rv && f < F && zb0 + (r & 255) < p.O[0] && zb1 + ((r >> 8) & 255) < p.O[1] &&
+                    zb2 + (r >> 16) < p.O[2])
                   mask |= 1u << f;
+              }
               float* yrow = p.y + ((long long)tc.n * p.Cout + oc0) * ovol + (long long)zb0 * o12 +
                             (long long)zb1 * p.O[2] + zb2;
               for (int cc = 0; cc < p.n_tile; cc += 32) {
                 uint32_t v[32];
                 load_acc32(taddr + (uint32_t)cc, lo_off, v);
                 const int oc_lane = cc + lane;
-                const float bl = (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
+                const float bl =
+                    (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
                 float* yo = yrow + (long long)cc * ovol;
-                if (F == 1) {  // a convolution: one output per row and channel
 #pragma unroll
-                  for (int jj = 0; jj < 32; ++jj) {
-                    if (cc + jj >= ocb_valid) break;
-                    const float b = __shfl_sync(0xffffffffu, bl, jj);
-                    if (mask & 1u) *yo = __uint_as_float(v[jj]) + b;
-                    yo += ovol;
-                  }
-                } else {
+                for (int jj = 0; jj < 32; ++jj) {
+                  if (cc + jj >= ocb_valid) break;
+                  const float b = __shfl_sync(0xffffffffu, bl, jj);
+                  const float val = __uint_as_float(v[jj]) + b;
 #pragma unroll
-                  for (int jj = 0; jj < 32; ++jj) {
-                    if (cc + jj >= ocb_valid) break;
-                    const float b = __shfl_sync(0xffffffffu, bl, jj);
-                    const float val = __uint_as_float(v[jj]) + b;
-#pragma unroll
-                    for (int f = 0; f < 8; ++f)
-                      if ((mask >> f) & 1u) yo[off[f]] = (f == fstar) ? val : b;
-                    yo += ovol;
-                  }
+                  for (int f = 0; f < 8; ++f)
+                    if ((mask >> f) & 1u) yo[p.cls_off[f]] = (f == p.cls_star) ? val : b;
+                  yo += ovol;
                 }
               }
             }

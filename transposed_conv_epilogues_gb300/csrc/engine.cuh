@@ -87,6 +87,10 @@ struct EngineParams {
   int nR, nRaxis[3], nEmpty;
   int r_axis[3][kMaxClassesAxis];
   int cls_mask[3];  // per axis: bit r set iff class r has a tap
+  // one class with taps and at most 8 classes: output offset of class f =
+  // (r0, r1, r2) from its row's first output, the class packed as
+  // r0 | r1 << 8 | r2 << 16, and the index of the class with taps
+  int cls_fast, cls_off[8], cls_r[8], cls_star;
 
   int ocb, n_tile, nb_per_group, n_colblocks;
   int n_acc, dbuf, a_stages;  // a_stages: ring depth, 16*n_acc*ks_stage TMEM columns each
