@@ -90,6 +90,13 @@ CONVT_CASES = [
     ((1, 5, 6, 7, 8), (5, 6, 3, 3, 3), 1, 1, 1, 0, 1, True),
     ((2, 3, 3, 4, 4), (3, 5, 2, 2, 2), 4, 0, 1, (3, 0, 2), 1, True),  # many empty classes
     ((1, 2, 4, 5, 6), (2, 3, 1, 3, 2), (2, 3, 2), (0, 1, 1), (1, 1, 2), (1, 2, 0), 1, True),
+    # one parity class with taps, stride 2 along x: the dense pair-store path
+    ((1, 4, 3, 5, 20), (4, 6, 3, 3, 3), 2, 1, 2, (1, 0, 1), 1, True),
+    ((2, 3, 4, 6, 9), (3, 5, 3, 3, 3), (1, 2, 2), 1, (1, 2, 2), 0, 1, True),
+    ((1, 4, 5, 4, 11), (4, 3, 3, 3, 3), (2, 1, 2), 1, (2, 1, 2), 0, 2, True),
+    ((1, 3, 2, 3, 40), (3, 40, 3, 3, 3), 2, 1, 2, 0, 1, True),
+    # one parity class with taps, stride 1 along x
+    ((1, 3, 4, 5, 6), (3, 4, 3, 3, 3), (2, 2, 1), 1, (2, 2, 1), 0, 1, True),
 ]
 
 

@@ -712,6 +712,76 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 }
               }
             }
+          } else if (p.cls_fast && p.s_out[2] == 2) {
+            // one class with taps, stride 2 along x: dense stores.  The Q2
+            // lanes of a row group hold consecutive m2 with equal (m0, m1),
+            // so for a class pair (r0, r1) the group's outputs at x = 2 m2
+            // + r2 form one run of 2 Q2 floats.  The warp's 64 values of a
+            // pair are written by 2 stores of 32 consecutive floats per
+            // run: writer lane l of store k takes flattened position
+            // i = 32 k + l, i.e. run g = i / (2 Q2) at x offset i % (2 Q2),
+            // whose value sits in source lane g Q2 + (i % (2 Q2)) / 2.
+            const int npair = F >> 1;  // class pairs (r0, r1)
+            const int star01 = p.cls_star >> 1, star2 = p.cls_star & 1;
+            int src[2], xodd[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int i = 32 * k + lane;
+              const int xl = i & (2 * p.Q[2] - 1);
+              src[k] = (i >> (p.lQ[2] + 1)) * p.Q[2] + (xl >> 1);
+              xodd[k] = xl & 1;
+            }
+#pragma unroll 1
+            for (int a = 0; a < p.n_acc; ++a) {
+              const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
+              float* pk[2];
+              uint32_t mk[2];  // bit c: class pair c of this writer is inside
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                int t[3];
+                row_local(p, a, q, src[k], t);
+                const int m0 = tc.o[0] + t[0], m1 = tc.o[1] + t[1], m2 = tc.o[2] + t[2];
+                const bool rv = m0 < p.M[0] && m1 < p.M[1] && m2 < p.M[2];
+                const int zb0 = p.s_out[0] * m0, zb1 = p.s_out[1] * m1, xb = 2 * m2 + xodd[k];
+                pk[k] = p.y + ((long long)tc.n * p.Cout + oc0) * ovol + (long long)zb0 * o12 +
+                        (long long)zb1 * p.O[2] + xb;
+                mk[k] = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const int r = p.cls_r[2 * c];
+                  if (c < npair && rv && xb < p.O[2] && zb0 + (r & 255) < p.O[0] &&
+                      zb1 + ((r >> 8) & 255) < p.O[1])
+                    mk[k] |= 1u << c;
+                }
+              }
+              for (int cc = 0; cc < p.n_tile; cc += 32) {
+                uint32_t v[32];
+                load_acc32(taddr + (uint32_t)cc, lo_off, v);
+                const int oc_lane = cc + lane;
+                const float bl =
+                    (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
+                float* y0 = pk[0] + (long long)cc * ovol;
+                float* y1 = pk[1] + (long long)cc * ovol;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                  if (cc + jj >= ocb_valid) break;
+                  const float b = __shfl_sync(0xffffffffu, bl, jj);
+                  const float val = __uint_as_float(v[jj]) + b;
+                  const float v0 = __shfl_sync(0xffffffffu, val, src[0]);
+                  const float v1 = __shfl_sync(0xffffffffu, val, src[1]);
+                  const float s0 = xodd[0] == star2 ? v0 : b;
+                  const float s1 = xodd[1] == star2 ? v1 : b;
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    const int off = p.cls_off[2 * c];
+                    if ((mk[0] >> c) & 1u) y0[off] = c == star01 ? s0 : b;
+                    if ((mk[1] >> c) & 1u) y1[off] = c == star01 ? s1 : b;
+                  }
+                  y0 += ovol;
+                  y1 += ovol;
+                }
+              }
+            }
           } else if (p.cls_fast) {
             // one class with taps (cls_star), the others hold the bias.
             // Class f = (r0, r1, r2) of the s_out grid sits at offset
