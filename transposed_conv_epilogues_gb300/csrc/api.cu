@@ -264,7 +264,7 @@ int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cud
   const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
   int zlo[3];
   for (int a = 0; a < 3; ++a) zlo[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
-  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count * 4, st) ==
+  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count * 16, st) ==
                  cudaSuccess
              ? TC3D_OK
              : TC3D_ERR_CUDA;

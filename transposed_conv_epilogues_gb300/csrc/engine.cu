@@ -1225,39 +1225,43 @@ __global__ void bn_pool4_kernel(const float* t, float* y, int N, int Cout, int O
 }
 
 // three disjoint boxes: z0 >= zlo0 | z0 < zlo0, z1 >= zlo1 | z0 < zlo0, z1 < zlo1, z2 >= zlo2
-__global__ void fill_slab_kernel(float* y, const float* bias, int N, int Cout, int O0, int O1,
-                                 int O2, int zl0, int zl1, int zl2) {
-  const long long nA = (long long)(O0 - zl0) * O1 * O2;
-  const long long nB = (long long)zl0 * (O1 - zl1) * O2;
-  const long long nC = (long long)zl0 * zl1 * (O2 - zl2);
-  const long long per = nA + nB + nC;
-  const long long total = per * N * Cout;
+// Bias fill of the outputs past the last row with taps on some axis (rows m
+// >= M of the transposed-conv row grid hold only tap-less classes).  Per
+// (n, c) slice, with zl = s_out * M clipped to O:
+//   rows (z, y) with z >= zl0, or y >= zl1: the whole x range;
+//   the other rows: x in [zl2, O2).
+// Block row blockIdx.y takes slices; whole rows go one per warp with the
+// lanes along x, the short x tails one element per thread.
+__global__ void __launch_bounds__(256) fill_slab_kernel(float* y, const float* bias, int NC,
+                                                        int Cout, int O0, int O1, int O2, int zl0,
+                                                        int zl1, int zl2) {
+  const int n_zrows = (O0 - zl0) * O1;           // rows of the z >= zl0 planes
+  const int n_full = n_zrows + zl0 * (O1 - zl1);  // rows filled over the whole x range
+  const int wtail = O2 - zl2;
+  const int n_tail = wtail > 0 ? zl0 * zl1 * wtail : 0;
   const long long ovol = (long long)O0 * O1 * O2;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long nc = i / per;
-    long long r = i % per;
-    int z0, z1, z2;
-    if (r < nA) {
-      z2 = (int)(r % O2);
-      r /= O2;
-      z1 = (int)(r % O1);
-      z0 = zl0 + (int)(r / O1);
-    } else if (r < nA + nB) {
-      r -= nA;
-      z2 = (int)(r % O2);
-      r /= O2;
-      z1 = zl1 + (int)(r % (O1 - zl1));
-      z0 = (int)(r / (O1 - zl1));
-    } else {
-      r -= nA + nB;
-      z2 = zl2 + (int)(r % (O2 - zl2));
-      r /= (O2 - zl2);
-      z1 = (int)(r % zl1);
-      z0 = (int)(r / zl1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int nc = blockIdx.y; nc < NC; nc += gridDim.y) {
+    float* ys = y + (long long)nc * ovol;
+    const float b = bias ? __ldg(bias + nc % Cout) : 0.f;
+    for (int r = blockIdx.x * 8 + warp; r < n_full; r += gridDim.x * 8) {
+      int z, yy;
+      if (r < n_zrows) {
+        z = zl0 + r / O1;
+        yy = r - (z - zl0) * O1;
+      } else {
+        const int r2 = r - n_zrows, w1 = O1 - zl1;
+        z = r2 / w1;
+        yy = zl1 + (r2 - z * w1);
+      }
+      float* row = ys + ((long long)z * O1 + yy) * O2;
+      for (int x = lane; x < O2; x += 32) row[x] = b;
     }
-    const int c = (int)(nc % Cout);
-    y[nc * ovol + ((long long)z0 * O1 + z1) * O2 + z2] = bias ? bias[c] : 0.f;
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < n_tail; i += gridDim.x * 256) {
+      const int r = i / wtail, x = zl2 + (i - r * wtail);
+      const int z = r / zl1, yy = r - z * zl1;
+      ys[((long long)z * O1 + yy) * O2 + x] = b;
+    }
   }
 }
 
@@ -1338,8 +1342,12 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
 
 cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
                              const int zlo[3], unsigned blocks, cudaStream_t st) {
-  fill_slab_kernel<<<blocks, 256, 0, st>>>(y, bias, N, Cout, O[0], O[1], O[2], zlo[0], zlo[1],
-                                           zlo[2]);
+  // blocks: a target count of CTAs; each slice gets up to 8 (64 warps)
+  const int NC = N * Cout;
+  const unsigned per_slice = std::max(1u, std::min(8u, blocks / (unsigned)std::max(1, NC)));
+  const dim3 grid(per_slice, (unsigned)std::min(NC, 65535));
+  fill_slab_kernel<<<grid, 256, 0, st>>>(y, bias, NC, Cout, O[0], O[1], O[2], zlo[0], zlo[1],
+                                         zlo[2]);
   return cudaGetLastError();
 }
 
