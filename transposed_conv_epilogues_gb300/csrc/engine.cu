@@ -576,8 +576,14 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 const int j = j0 + kk;
                 const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
                 const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
-                const int kofs[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                // GEMM-K entries past the chunk's valid ones (ragged last chunk,
+                // K padding) have zero weights; they read the row's own first
+                // raw element, which is already a term of the row's sum
                 const int kbase = j * 8;
+                const int kraw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                int kofs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kofs[e] = kbase + e < valid_k ? kraw[e] : 0;
                 const uint32_t kcol = stage_col + (uint32_t)(kk * 16 * p.n_acc);
                 // the gathers of all accumulators first (independent loads in
                 // flight together), then the splits and TMEM stores
@@ -587,7 +593,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                   if (a >= p.n_acc) break;
                   const float* rp = raw + row_base[a];
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) xg[a][e] = (kbase + e < valid_k) ? rp[kofs[e]] : 0.f;
+                  for (int e = 0; e < 8; ++e) xg[a][e] = rp[kofs[e]];
                 }
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
