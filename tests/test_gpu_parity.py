@@ -71,6 +71,13 @@ CONV_CASES = [
     ((2, 8, 7, 9, 8), (8, 2, 3, 3, 3), 1, 1, 1, 4, True),            # groups 4
     ((1, 3, 13, 12, 16), (5, 3, 5, 3, 5), (1, 2, 1), 2, 2, 1, True),  # k5 dil 2
     ((3, 17, 6, 5, 20), (9, 17, 2, 3, 2), 1, 0, 1, 1, True),         # Cin 17: 2 chunks
+    # view mode: one tap along x, x lines filling 128-row accumulators
+    ((2, 8, 7, 9, 8), (5, 8, 3, 3, 1), 1, (1, 1, 0), 1, 1, True),
+    ((1, 8, 9, 10, 16), (8, 8, 3, 3, 1), 1, (2, 0, 0), (2, 1, 1), 1, True),
+    ((1, 16, 4, 5, 32), (20, 16, 2, 2, 1), 1, 0, 1, 1, False),
+    ((2, 8, 6, 20, 4), (4, 8, 1, 3, 1), 1, (0, 1, 0), 1, 1, True),
+    ((1, 40, 6, 6, 8), (16, 40, 3, 3, 1), 1, (1, 1, 0), 1, 1, True),  # 5 channel chunks
+    ((1, 24, 5, 7, 8), (130, 24, 3, 3, 1), 1, 1, 1, 1, True),         # 2 column blocks: gather path
 ]
 
 

@@ -34,7 +34,7 @@ struct DeviceState {
   int status = TC3D_OK;
   int sm_count = 0;
   int* err = nullptr;  // device address of the error word
-  bool smem_set[3] = {false, false, false};
+  bool smem_set[4] = {false, false, false, false};  // per kernel id
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -105,11 +105,11 @@ int plan_for(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, i
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int set_smem(DeviceState* d, int epi) {
+int set_smem(DeviceState* d, int kid) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!d->smem_set[epi]) {
-    if (engine_set_smem(epi, kMaxSmem) != cudaSuccess) return TC3D_ERR_CUDA;
-    d->smem_set[epi] = true;
+  if (!d->smem_set[kid]) {
+    if (engine_set_smem(kid, kMaxSmem) != cudaSuccess) return TC3D_ERR_CUDA;
+    d->smem_set[kid] = true;
   }
   return TC3D_OK;
 }
@@ -181,6 +181,9 @@ void fill_params(const Plan& pl, EngineParams* ep) {
   ep->dbuf = pl.dbuf;
   ep->a_stages = pl.a_stages;
   ep->ks_stage = pl.ks_stage;
+  ep->view = pl.view;
+  ep->nslots = pl.nslots;
+  ep->slot_bytes = (unsigned)pl.slot_bytes;
   ep->wide = pl.wide;
   ep->acc_cols = pl.acc_cols;
   ep->tiles = (int)pl.tiles;
@@ -196,6 +199,7 @@ void fill_params(const Plan& pl, EngineParams* ep) {
   const SmemLayout L = smem_layout(pl);
   ep->sm_raw = (unsigned)L.raw;
   ep->sm_b = (unsigned)L.b;
+  ep->sm_xs = (unsigned)L.xs;
   ep->sm_ktab = (unsigned)L.ktab;
   ep->sm_misc = (unsigned)L.misc;
   ep->sm_bar = (unsigned)L.bar;
@@ -253,6 +257,7 @@ int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cuda
   pp.n_chunks = pl.n_chunks;
   pp.k_chunk = pl.k_chunk;
   pp.ksteps_chunk = pl.ksteps_chunk;
+  pp.octet_major = pl.view;
   pp.total = pl.ws_wpack_bytes / 4;
   long long blocks = (pp.total + 255) / 256;
   if (blocks > (long long)sm_count * 8) blocks = (long long)sm_count * 8;
@@ -284,9 +289,10 @@ int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, c
   encode_xmap(pl, x, &ep);
   const unsigned grid = (unsigned)engine_grid(pl, d->sm_count);
   ep.part_slots = (int)bn_part_slots(pl, grid);
-  int rc = set_smem(d, epi);
+  const int kid = pl.view ? kEngineView : epi;
+  int rc = set_smem(d, kid);
   if (rc) return rc;
-  return engine_launch(epi, ep, grid, (size_t)pl.smem_bytes, st) == cudaSuccess ? TC3D_OK
+  return engine_launch(kid, ep, grid, (size_t)pl.smem_bytes, st) == cudaSuccess ? TC3D_OK
                                                                                : TC3D_ERR_CUDA;
 }
 
@@ -420,6 +426,9 @@ std::string describe(const Plan& pl) {
     append(s, ", \"dbuf\": %lld", pl.dbuf);
     append(s, ", \"a_stages\": %lld", pl.a_stages);
     append(s, ", \"ks_stage\": %lld", pl.ks_stage);
+    append(s, ", \"view\": %lld", pl.view);
+    append(s, ", \"nslots\": %lld", pl.nslots);
+    append(s, ", \"slot_bytes\": %lld", pl.slot_bytes);
     append(s, ", \"wide\": %lld", pl.wide);
     append(s, ", \"acc_cols\": %lld", pl.acc_cols);
     append(s, ", \"tiles\": %lld", pl.tiles);

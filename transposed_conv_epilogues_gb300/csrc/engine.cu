@@ -332,9 +332,164 @@ __device__ __forceinline__ void mma_role(const EngineParams& p, const Bars& bars
   }
 }
 
+// View mode (plain stride-1 conv, no x halo, x lines filling 128-row
+// accumulators): row r of accumulator a is raw-box position a*B1*B2 + r, so
+// for tap t the A operand of an octet of channels is the 128 x 8 window at
+// position a*B1*B2 + toff[t] of a channels-last copy of the box.  A slot
+// holds one octet: x as [2][box volume][4] floats (4-channel groups, each
+// position 16 bytes), then x_lo in the same layout.  In the no-swizzle
+// K-major layout a core matrix is 8 positions x 4 channels (128 contiguous
+// bytes): SBO = 128 B between 8-position groups, LBO = box volume x 16 B
+// between the two 4-channel groups.
+//
+// The MMA issuer of accumulator a: per octet slot, the taps' MMAs
+// back-to-back (x.[w|w_lo] and x_lo.w when wide, else 3 per tap), one
+// commit per slot.  Weights are resident in K-step order (octet-major,
+// tap-minor).
+template <bool WIDE>
+__device__ __forceinline__ void mma_view_role(const EngineParams& p, const Bars& bars,
+                                              uint32_t sbase, const int* ktab, uint32_t tmem_base,
+                                              int dcols, int a, volatile int* abortf,
+                                              unsigned long long tmo, int lane) {
+  const uint32_t idesc_n = idesc_tf32(128, (uint32_t)p.n_tile);
+  const uint32_t idesc_2n = idesc_tf32(128, (uint32_t)(2 * p.n_tile));
+  const uint64_t bdesc0 = smem_desc_noswz(sbase + p.sm_b, 128, 256);
+  const uint64_t lo_step = (uint64_t)(p.n_tile * 32) >> 4;   // w_lo follows w in a K-step
+  const uint64_t kstep_step = (uint64_t)(64 * p.n_tile) >> 4;  // one K-step of weights
+  const uint32_t bvol = (uint32_t)(p.box[0] * p.box[1] * p.box[2]);
+  const uint32_t gstride = bvol * 16u;                  // bytes between 4-channel groups
+  const uint32_t lo_off = (uint32_t)p.slot_bytes / 2u;  // x_lo follows x in a slot
+  const uint32_t row0 = (uint32_t)(a * p.box[1] * p.box[2]) * 16u;
+  const int noct = p.cin_chunk / 8;
+  bool ok = __all_sync(0xffffffffu, mbar_wait(bars.b_full(0), 0, tmo, abortf));
+  if (!ok && lane == 0) raise_abort(p, abortf);
+  int slot = 0, dslot = 0;
+  uint32_t sphase = 0, dphase = 0;
+  for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+    for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.d_empty(dslot), dphase ^ 1, tmo, abortf));
+      if (!ok) {
+        if (lane == 0) raise_abort(p, abortf);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tm = tmem_base + (uint32_t)(dslot * dcols + a * p.acc_cols);
+      uint32_t accumulate = 0;
+      int kres = 0;  // K-step index within the resident weights
+      for (int c = 0; c < p.n_chunks && ok; ++c) {
+        for (int o = 0; o < noct; ++o) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.a_full(slot), sphase, tmo, abortf));
+          if (!ok) {
+            if (lane == 0) raise_abort(p, abortf);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xaddr = sbase + p.sm_xs + (uint32_t)slot * (uint32_t)p.slot_bytes + row0;
+          for (int t = 0; t < p.nUtot; ++t, ++kres) {
+            const uint32_t aaddr = xaddr + (uint32_t)ktab[t] * 16u;
+            const uint64_t ahi = smem_desc_noswz(aaddr, gstride, 128);
+            const uint64_t alo = smem_desc_noswz(aaddr + lo_off, gstride, 128);
+            const uint64_t bw = bdesc0 + (uint64_t)kres * kstep_step;
+            if (WIDE) {
+              mma_tf32_ss_elect(d_tm, ahi, bw, idesc_2n, accumulate);  // x.[w|w_lo]
+              mma_tf32_ss_elect(d_tm, alo, bw, idesc_n, 1u);           // x_lo . w
+            } else {
+              mma_tf32_ss_elect(d_tm, ahi, bw, idesc_n, accumulate);   // x . w
+              mma_tf32_ss_elect(d_tm, ahi, bw + lo_step, idesc_n, 1u); // x . w_lo
+              mma_tf32_ss_elect(d_tm, alo, bw, idesc_n, 1u);           // x_lo . w
+            }
+            accumulate = 1;
+          }
+          mma_commit_elect(bars.a_empty(slot));
+          if (++slot == p.nslots) {
+            slot = 0;
+            sphase ^= 1;
+          }
+        }
+      }
+      if (!ok) break;
+      mma_commit_elect(bars.d_full(dslot));
+      if (++dslot == p.dbuf) {
+        dslot = 0;
+        dphase ^= 1;
+      }
+    }
+  }
+}
+
+// View-mode conversion: per raw stage (a channel chunk in TMA's [c][position]
+// layout) and per channel octet, write the slot's channels-last x and x_lo.
+// Thread i takes positions i, i + 256, ...; a lane reads 4 channels of its
+// position and stores them as one 16-byte vector, so both sides are
+// conflict-free.  Channels past the chunk's valid ones are written as 0.
+__device__ __forceinline__ void view_conversion_role(const EngineParams& p, const Bars& bars,
+                                                     uint8_t* gbase, int cw, int lane,
+                                                     volatile int* abortf,
+                                                     unsigned long long tmo) {
+  const int bvol = p.box[0] * p.box[1] * p.box[2];
+  const int noct = p.cin_chunk / 8;
+  const int tid = cw * 32 + lane;
+  int rstage = 0, slot = 0;
+  uint32_t rphase = 0, sphase = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+    for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
+      for (int c = 0; c < p.n_chunks && ok; ++c) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.raw_full(rstage), rphase, tmo, abortf));
+        if (!ok) {
+          if (lane == 0) raise_abort(p, abortf);
+          break;
+        }
+        const float* raw =
+            reinterpret_cast<const float*>(gbase + p.sm_raw + rstage * p.raw_stage_bytes);
+        const int cin_valid = min(p.cin_chunk, p.cin_g - c * p.cin_chunk);
+        for (int o = 0; o < noct; ++o) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.a_empty(slot), sphase ^ 1, tmo, abortf));
+          if (!ok) {
+            if (lane == 0) raise_abort(p, abortf);
+            break;
+          }
+          float4* xs = reinterpret_cast<float4*>(gbase + p.sm_xs + slot * p.slot_bytes);
+          float4* xl = xs + 2 * bvol;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int c0 = 8 * o + 4 * g;
+            for (int pos = tid; pos < bvol; pos += 8 * 32) {
+              float v[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                v[i] = c0 + i < cin_valid ? raw[(size_t)(c0 + i) * bvol + pos] : 0.f;
+              float lo[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                lo[i] = v[i] - __uint_as_float(__float_as_uint(v[i]) & 0xFFFFE000u);
+              xs[g * bvol + pos] = make_float4(v[0], v[1], v[2], v[3]);
+              xl[g * bvol + pos] = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
+          // the tensor core reads the slot through the async proxy
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.a_full(slot));
+          if (++slot == p.nslots) {
+            slot = 0;
+            sphase ^= 1;
+          }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(bars.raw_empty(rstage));
+        if (++rstage == p.raw_stages) {
+          rstage = 0;
+          rphase ^= 1;
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 
-template <int EPI>
+template <int EPI, bool VIEW>
 __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     engine_kernel(const __grid_constant__ EngineParams p) {
   constexpr int kWarpConv0 = WarpCfg<EPI>::kConv0;
@@ -381,7 +536,14 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpRaw && lane == 0 && p.use_tma) prefetch_tensormap(&p.xmap);
-  {
+  if constexpr (VIEW) {
+    // per tap: raw-box position offset of the tap's window
+    int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
+    for (int t = threadIdx.x; t < p.nUtot; t += kThreads) {
+      const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
+      ktab[t] = (p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2];
+    }
+  } else {
     // GEMM-K table of one channel chunk: raw-box offset of (channel, tap) pair k
     int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
     const int bvol = p.box[0] * p.box[1] * p.box[2];
@@ -501,7 +663,15 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     }
   }
   // ================= MMA issuer =================
-  else if (warp == kWarpMMA || warp == kWarpMMA1) {
+  else if (VIEW && (warp == kWarpMMA || warp == kWarpMMA1)) {
+    // view mode: two accumulators, warp 2 takes accumulator 0, warp 3 takes 1
+    const int a = warp - kWarpMMA;
+    const int* ktab = reinterpret_cast<const int*>(gbase + p.sm_ktab);
+    if (p.wide)
+      mma_view_role<true>(p, bars, sbase, ktab, tmem_base, dcols, a, abortf, tmo, lane);
+    else
+      mma_view_role<false>(p, bars, sbase, ktab, tmem_base, dcols, a, abortf, tmo, lane);
+  } else if (warp == kWarpMMA || warp == kWarpMMA1) {
     // with two or more accumulators warp 2 takes the even ones, warp 3 the
     // odd ones; with one, warp 2 takes it and warp 3 has nothing to do
     const int par = warp - kWarpMMA;
@@ -524,7 +694,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   // accumulators (16 columns each: x then x_lo).  Group g fills the K-steps
   // kk with kk % 2 == g of every stage, for all accumulators, so that a warp
   // has the gathers of n_acc rows in flight at once.
-  else if (warp >= kWarpConv0) {
+  else if (VIEW && warp >= kWarpConv0) {
+    view_conversion_role(p, bars, gbase, warp - kWarpConv0, lane, abortf, tmo);
+  } else if (warp >= kWarpConv0) {
     const int cw = warp - kWarpConv0;
     const int half = cw >> 2;
     const int q = warp & 3;
@@ -1059,9 +1231,10 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 static_assert(WarpCfg<EPI_BN_POOL>::kEpiWarps == 2 * kEpiGroup && kBnSlotsPerCta == kEpiGroup,
               "BatchNorm pooling: two groups of 8 channels, one partial slot per lane quarter");
 
-template __global__ void engine_kernel<EPI_STORE>(const __grid_constant__ EngineParams p);
-template __global__ void engine_kernel<EPI_POOL_LSE>(const __grid_constant__ EngineParams p);
-template __global__ void engine_kernel<EPI_BN_POOL>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_STORE, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_POOL_LSE, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_BN_POOL, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_STORE, true>(const __grid_constant__ EngineParams p);
 
 // ---------------------------------------------------------------------------
 // weight pre-pack: W -> [colblock][chunk][kstep][w | w_lo][n_tile x 8] in the
@@ -1087,7 +1260,10 @@ __global__ void pack_weights_kernel(const __grid_constant__ PackParams p) {
     float w = 0.f;
     const int oc_l = nrow / p.nR, ri = nrow % p.nR;
     const int k = j * 8 + e;
-    const int c_l = k / p.nUtot, t = k % p.nUtot;
+    // GEMM-K index k of the chunk -> (channel, tap): channel-major, or, in
+    // view mode, K-step j = (channel octet, tap) with the 8 channels inside
+    const int c_l = p.octet_major ? (j / p.nUtot) * 8 + e : k / p.nUtot;
+    const int t = p.octet_major ? j % p.nUtot : k % p.nUtot;
     const int icl = c * p.cin_chunk + c_l;
     const int ocg = nb * p.ocb + oc_l;  // output channel within the group
     if (oc_l < p.ocb && ocg < p.cout_g && k < p.k_chunk && icl < p.cin_g) {
@@ -1284,31 +1460,30 @@ __global__ void wait_timeout_kernel(int* err, unsigned long long timeout_cycles)
 // ---------------------------------------------------------------------------
 // host-side launch wrappers
 // ---------------------------------------------------------------------------
-cudaError_t engine_set_smem(int epi, int bytes) {
-  switch (epi) {
-    case EPI_STORE:
-      return cudaFuncSetAttribute(engine_kernel<EPI_STORE>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    case EPI_POOL_LSE:
-      return cudaFuncSetAttribute(engine_kernel<EPI_POOL_LSE>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    default:
-      return cudaFuncSetAttribute(engine_kernel<EPI_BN_POOL>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+cudaError_t engine_set_smem(int kid, int bytes) {
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  switch (kid) {
+    case EPI_STORE: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, false>, a, bytes);
+    case EPI_POOL_LSE: return cudaFuncSetAttribute(engine_kernel<EPI_POOL_LSE, false>, a, bytes);
+    case EPI_BN_POOL: return cudaFuncSetAttribute(engine_kernel<EPI_BN_POOL, false>, a, bytes);
+    default: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, true>, a, bytes);
   }
 }
 
-cudaError_t engine_launch(int epi, const EngineParams& p, unsigned grid, size_t smem,
+cudaError_t engine_launch(int kid, const EngineParams& p, unsigned grid, size_t smem,
                           cudaStream_t st) {
-  switch (epi) {
+  switch (kid) {
     case EPI_STORE:
-      engine_kernel<EPI_STORE><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
+      engine_kernel<EPI_STORE, false><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
       break;
     case EPI_POOL_LSE:
-      engine_kernel<EPI_POOL_LSE><<<grid, WarpCfg<EPI_POOL_LSE>::kThreads, smem, st>>>(p);
+      engine_kernel<EPI_POOL_LSE, false><<<grid, WarpCfg<EPI_POOL_LSE>::kThreads, smem, st>>>(p);
+      break;
+    case EPI_BN_POOL:
+      engine_kernel<EPI_BN_POOL, false><<<grid, WarpCfg<EPI_BN_POOL>::kThreads, smem, st>>>(p);
       break;
     default:
-      engine_kernel<EPI_BN_POOL><<<grid, WarpCfg<EPI_BN_POOL>::kThreads, smem, st>>>(p);
+      engine_kernel<EPI_STORE, true><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
       break;
   }
   return cudaGetLastError();

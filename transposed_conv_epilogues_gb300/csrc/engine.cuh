@@ -108,8 +108,12 @@ struct EngineParams {
   int b_resident, b_stages;
   unsigned b_stage_bytes;
 
+  // view mode: A read by the tensor core from channels-last octet slots
+  int view, nslots;
+  unsigned slot_bytes;
+
   // dynamic shared-memory layout (offsets from the 1024-aligned base)
-  unsigned sm_raw, sm_b, sm_ktab, sm_misc, sm_bar;
+  unsigned sm_raw, sm_b, sm_xs, sm_ktab, sm_misc, sm_bar;
 };
 
 struct PackParams {
@@ -123,13 +127,16 @@ struct PackParams {
   int kidx[3][kMaxClassesAxis][kMaxAxisTaps];
   int ocb, n_tile, nb_per_group, n_colblocks;
   int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
+  int octet_major;  // 1: K-step j of a chunk is channel octet j / nUtot at tap j % nUtot
   long long total;  // floats in the packed buffer
 };
 
 // host-side launch wrappers (engine.cu; kernels are launched from the
 // translation unit that defines them)
-cudaError_t engine_set_smem(int epi, int bytes);
-cudaError_t engine_launch(int epi, const EngineParams& p, unsigned grid, size_t smem,
+// kernel id: the epilogue kind, or kEngineView for the view-mode store kernel
+constexpr int kEngineView = 3;
+cudaError_t engine_set_smem(int kid, int bytes);
+cudaError_t engine_launch(int kid, const EngineParams& p, unsigned grid, size_t smem,
                           cudaStream_t st);
 cudaError_t pack_launch(const PackParams& pp, unsigned blocks, cudaStream_t st);
 cudaError_t bn_stats_f2_launch(const float2* part, int nparts, const float* bias,

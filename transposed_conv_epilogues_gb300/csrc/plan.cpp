@@ -91,7 +91,8 @@ SmemLayout smem_layout(const Plan& pl) {
   SmemLayout L;
   L.raw = 0;
   L.b = L.raw + (int64_t)pl.raw_stages * pl.raw_stage_bytes;
-  L.ktab = L.b + (int64_t)pl.b_stages * pl.b_stage_bytes;
+  L.xs = L.b + (int64_t)pl.b_stages * pl.b_stage_bytes;
+  L.ktab = L.xs + (int64_t)pl.nslots * pl.slot_bytes;
   L.misc = L.ktab + round_up((int64_t)pl.ksteps_chunk * 32, 1024);
   L.bar = L.misc + 4096;
   // + 1024 for the barriers and 1024 of slack to align the dynamic base
@@ -384,6 +385,68 @@ int make_plan(const Problem& pb_in, Plan* out) {
     pl.raw_stages = (used + 3 * pl.raw_stage_bytes <= kMaxSmem) ? 3 : 2;
     pl.smem_bytes = smem_layout(pl).total;
     if (pl.smem_bytes > kMaxSmem) return fail(TC3D_ERR_UNSUPPORTED);
+  }
+
+  // ---- view mode: a plain stride-1 conv whose kernel has one tap along the
+  // contiguous axis (no x halo) and whose x lines fill 128-row accumulators
+  // exactly: row r of accumulator a is raw-box position a*B1*B2 + r
+  {
+    const int S2 = pb.S[2];
+    const bool shape_ok = pb.op == OP_CONV && pl.s_in[0] == 1 && pl.s_in[1] == 1 &&
+                          pl.s_in[2] == 1 && pl.nU[2] == 1 && pl.u_min[2] == 0 &&
+                          pl.M[2] == S2 && (S2 == 4 || S2 == 8 || S2 == 16 || S2 == 32) &&
+                          pl.cin_g % 8 == 0 && pl.n_tile <= 128 && pl.nR == 1;
+    if (shape_ok) {
+      Plan v = pl;
+      v.view = 1;
+      v.dbuf = 2;
+      v.wide = 2 * v.n_tile <= 128 ? 1 : 0;
+      v.acc_cols = v.wide ? 2 * v.n_tile : v.n_tile;
+      v.n_acc = 2;
+      v.ks_stage = 0;
+      v.a_stages = 0;
+      v.Q[0] = 1;
+      v.Q[1] = 32 / S2;
+      v.Q[2] = S2;
+      v.Pq[0] = 2;
+      v.Pq[1] = 4;
+      v.Pq[2] = 1;
+      for (int a = 0; a < 3; ++a) {
+        v.T[a] = v.Q[a] * v.Pq[a];
+        v.ntile[a] = (int)ceil_div(v.M[a], v.T[a]);
+        v.box[a] = (int)(v.T[a] + v.u_max[a] - v.u_min[a]);
+      }
+      v.xslack = 0;
+      v.tiles = (int64_t)pb.N * v.ntile[0] * v.ntile[1] * v.ntile[2];
+      const int64_t bvol = (int64_t)v.box[0] * v.box[1] * v.box[2];
+      const int ntaps = nUtot;
+      v.slot_bytes = 2 * bvol * 8 * 4;
+      v.nslots = 2;
+      // weights stay resident: (cin_g / 8) * ntaps K-steps of 64 * n_tile bytes
+      const int64_t wbytes = (int64_t)(v.cin_g / 8) * ntaps * 64 * v.n_tile;
+      const int64_t fixed = 4096 + 1024 + 1024 + 1024 + round_up((int64_t)ntaps * 4, 1024);
+      int best = 0;
+      for (int cc = 8; cc <= v.cin_g; cc += 8) {
+        if (v.cin_g % cc) continue;
+        const int64_t raw = round_up(cc * bvol * 4, 1024);
+        if (2 * raw + v.nslots * v.slot_bytes + wbytes + fixed <= kMaxSmem) best = cc;
+      }
+      if (best > 0 && bvol <= 16383 && v.box[0] <= 256 && v.box[1] <= 256 &&
+          v.tiles < ((int64_t)1 << 31)) {
+        v.cin_chunk = best;
+        v.n_chunks = v.cin_g / best;
+        v.k_chunk = best * ntaps;
+        v.ksteps_chunk = (best / 8) * ntaps;
+        v.raw_stage_bytes = round_up(best * bvol * 4, 1024);
+        v.b_resident = 1;
+        v.b_stage_bytes = 64LL * v.n_tile;
+        v.b_stages = (int)((int64_t)v.n_chunks * v.ksteps_chunk);
+        const int64_t used = 2 * v.raw_stage_bytes + v.nslots * v.slot_bytes + wbytes + fixed;
+        v.raw_stages = used + v.raw_stage_bytes <= kMaxSmem ? 3 : 2;
+        v.smem_bytes = smem_layout(v).total;
+        if (v.smem_bytes <= kMaxSmem && v.n_colblocks == 1) pl = v;
+      }
+    }
   }
 
   // ---- workspace

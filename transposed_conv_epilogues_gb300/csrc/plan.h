@@ -90,6 +90,15 @@ struct Plan {
   int64_t b_stage_bytes;
   int64_t smem_bytes;
 
+  // view mode: every accumulator's 128 rows are 128 consecutive positions of
+  // the raw box, so for each tap the A operand is a shifted window of a
+  // channels-last copy of the box, read by the tensor core from shared
+  // memory.  The copy is kept in slots of one channel octet each ([x | x_lo],
+  // each [2][box volume][4] floats); GEMM-K runs octet-major, tap-minor.
+  int view;
+  int nslots;
+  int64_t slot_bytes;
+
   // workspace (bytes, each region 256-aligned)
   int64_t ws_wpack_off, ws_wpack_bytes;
   int64_t ws_part_off, ws_part_bytes;   // BN partials: fused [Cout][slots] float2, else [N][Cout] double2
@@ -102,7 +111,7 @@ struct Plan {
 // base): raw input stages, weight stages, GEMM-K offset table, epilogue
 // scratch (4 KB), mbarriers (1 KB).  Returns the dynamic smem request.
 struct SmemLayout {
-  int64_t raw, b, ktab, misc, bar, total;
+  int64_t raw, b, xs, ktab, misc, bar, total;
 };
 SmemLayout smem_layout(const Plan& pl);
 
