@@ -35,9 +35,15 @@ struct DeviceState {
   int sm_count = 0;
   int* err = nullptr;  // device address of the error word
   bool smem_set[4] = {false, false, false, false};  // per kernel id
+  // auxiliary stream for the bias slab fill, which runs beside the engine
+  // (fork / join through two events; calls that use it are serialised by
+  // g_fork_mu while they enqueue)
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+std::mutex g_fork_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int device_state(DeviceState** out) {
@@ -55,6 +61,10 @@ int device_state(DeviceState** out) {
     } else if (major != 10 || minor != 3) {
       d.status = TC3D_ERR_DEVICE;  // the kernels are built for sm_103a only
     } else if (error_flag_address(&d.err) != cudaSuccess) {
+      d.status = TC3D_ERR_CUDA;
+    } else if (cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+               cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming) != cudaSuccess) {
       d.status = TC3D_ERR_CUDA;
     }
     if (!g_encode && d.status == TC3D_OK) {
@@ -269,7 +279,7 @@ int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cud
   const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
   int zlo[3];
   for (int a = 0; a < 3; ++a) zlo[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
-  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count * 16, st) ==
+  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count, st) ==
                  cudaSuccess
              ? TC3D_OK
              : TC3D_ERR_CUDA;
@@ -326,9 +336,21 @@ int run(int op, const float* x, const float* w, const float* bias, const float* 
   rc = launch_pack(pl, w, wpack, d->sm_count, st);
   if (rc) return rc;
   if (op != OP_CONVT_BN_POOL) {
+    if (!pl.fill_slab) return launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
+    // The slab fill writes only outputs the engine does not, so it runs beside
+    // the engine on the auxiliary stream: fork after the work queued so far
+    // on st, join before anything queued on st later.
+    std::lock_guard<std::mutex> lk(g_fork_mu);
+    if (cudaEventRecord(d->ev_fork, st) != cudaSuccess) return TC3D_ERR_CUDA;
     rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
     if (rc) return rc;
-    return launch_fill(pl, bias, y, d, st);
+    if (cudaStreamWaitEvent(d->aux, d->ev_fork, 0) != cudaSuccess) return TC3D_ERR_CUDA;
+    rc = launch_fill(pl, bias, y, d, d->aux);
+    if (rc) return rc;
+    if (cudaEventRecord(d->ev_join, d->aux) != cudaSuccess ||
+        cudaStreamWaitEvent(st, d->ev_join, 0) != cudaSuccess)
+      return TC3D_ERR_CUDA;
+    return TC3D_OK;
   }
 
   float2* stat = reinterpret_cast<float2*>(wsb + pl.ws_stat_off);

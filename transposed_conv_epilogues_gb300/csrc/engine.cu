@@ -1413,8 +1413,10 @@ __global__ void bn_pool4_kernel(const float* t, float* y, int N, int Cout, int O
 //   rows (z, y) with z >= zl0, or y >= zl1: the whole x range;
 //   the other rows: x in [zl2, O2).
 // Block row blockIdx.y takes slices; whole rows go one per warp with the
-// lanes along x, the short x tails one element per thread.
-__global__ void __launch_bounds__(256) fill_slab_kernel(float* y, const float* bias, int NC,
+// lanes along x, the short x tails one element per thread.  Blocks are small
+// (128 threads, at most 32 registers each) so that one fits on an SM beside
+// an engine CTA: the fill runs concurrently with the engine.
+__global__ void __launch_bounds__(128, 16) fill_slab_kernel(float* y, const float* bias, int NC,
                                                         int Cout, int O0, int O1, int O2, int zl0,
                                                         int zl1, int zl2) {
   const int n_zrows = (O0 - zl0) * O1;           // rows of the z >= zl0 planes
@@ -1426,7 +1428,7 @@ __global__ void __launch_bounds__(256) fill_slab_kernel(float* y, const float* b
   for (int nc = blockIdx.y; nc < NC; nc += gridDim.y) {
     float* ys = y + (long long)nc * ovol;
     const float b = bias ? __ldg(bias + nc % Cout) : 0.f;
-    for (int r = blockIdx.x * 8 + warp; r < n_full; r += gridDim.x * 8) {
+    for (int r = blockIdx.x * 4 + warp; r < n_full; r += gridDim.x * 4) {
       int z, yy;
       if (r < n_zrows) {
         z = zl0 + r / O1;
@@ -1439,7 +1441,7 @@ __global__ void __launch_bounds__(256) fill_slab_kernel(float* y, const float* b
       float* row = ys + ((long long)z * O1 + yy) * O2;
       for (int x = lane; x < O2; x += 32) row[x] = b;
     }
-    for (int i = blockIdx.x * 256 + threadIdx.x; i < n_tail; i += gridDim.x * 256) {
+    for (int i = blockIdx.x * 128 + threadIdx.x; i < n_tail; i += gridDim.x * 128) {
       const int r = i / wtail, x = zl2 + (i - r * wtail);
       const int z = r / zl1, yy = r - z * zl1;
       ys[((long long)z * O1 + yy) * O2 + x] = b;
@@ -1523,12 +1525,12 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
 
 cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
                              const int zlo[3], unsigned blocks, cudaStream_t st) {
-  // blocks: a target count of CTAs; each slice gets up to 8 (64 warps)
+  // blocks: the CTA count to use (one per SM), spread over slices first
   const int NC = N * Cout;
-  const unsigned per_slice = std::max(1u, std::min(8u, blocks / (unsigned)std::max(1, NC)));
-  const dim3 grid(per_slice, (unsigned)std::min(NC, 65535));
-  fill_slab_kernel<<<grid, 256, 0, st>>>(y, bias, NC, Cout, O[0], O[1], O[2], zlo[0], zlo[1],
-                                         zlo[2]);
+  const unsigned rows = std::max(1u, std::min(blocks, (unsigned)std::min(NC, 65535)));
+  const unsigned per_slice = std::max(1u, blocks / rows);
+  fill_slab_kernel<<<dim3(per_slice, rows), 128, 0, st>>>(y, bias, NC, Cout, O[0], O[1], O[2],
+                                                           zlo[0], zlo[1], zlo[2]);
   return cudaGetLastError();
 }
 
