@@ -207,6 +207,46 @@ def test_deterministic_repeat(tc):
     assert torch.equal(c1, c2)
 
 
+def test_cuda_graph_capture_replays(tc):
+    """Every entry point enqueues only stream-ordered work: the transposed
+    conv's bias slab fill forks onto the library's auxiliary stream and joins
+    back through events.  So a call can be captured into a CUDA graph and
+    replayed, giving the same bits as a direct call."""
+    calls = []
+    x, w, b = make((2, 8, 7, 9, 8), (5, 8, 3, 3, 1), 5)                 # conv, view mode
+    calls.append((tc.OP_CONV3D, (_dev(x), _dev(w), _dev(b)), dict(stride=1, padding=(1, 1, 0))))
+    x, w, b = make((2, 6, 5, 7, 8), (6, 10, 3, 3, 3), 10)               # convT with a bias slab
+    calls.append((tc.OP_CONV_TRANSPOSE3D, (_dev(x), _dev(w), _dev(b)),
+                  dict(stride=2, padding=1, dilation=2)))
+    x, w, b = make((2, 5, 8, 10, 16), (12, 5, 3, 3, 3), 12)
+    calls.append((tc.OP_CONV_MAXPOOL_LSE_RELU, (_dev(x), _dev(w), _dev(b)), dict(stride=1, padding=1)))
+    x, w, b = make((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 16)
+    calls.append((tc.OP_CONVT_BN_AVGPOOL, (_dev(x), _dev(w), _dev(b)), dict(stride=2, padding=1)))
+    fns = {tc.OP_CONV3D: tc.conv3d_fwd, tc.OP_CONV_TRANSPOSE3D: tc.conv_transpose3d_fwd,
+           tc.OP_CONV_MAXPOOL_LSE_RELU: tc.conv_maxpool_lse_relu,
+           tc.OP_CONVT_BN_AVGPOOL: tc.convT_bn_avgpool}
+    side = torch.cuda.Stream()
+    for op, (xd, wd, bd), kw in calls:
+        fn = fns[op]
+        ref = fn(xd, wd, bd, **kw)  # direct call (also initialises the device state)
+        torch.cuda.synchronize()
+        ws = torch.empty(max(tc.workspace_bytes(op, tuple(xd.shape), tuple(wd.shape), **kw), 256),
+                         dtype=torch.uint8, device="cuda")
+        y = torch.full_like(ref, float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn(xd, wd, bd, **kw, out=y, workspace=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), op
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), op
+    assert tc.last_device_error() == tc.TC3D_OK
+
+
 def test_error_leaves_output_untouched(tc):
     x, w, b = make((1, 4, 6, 6, 8), (4, 4, 3, 3, 3), 4)
     y = torch.full(tc.out_shape(0, x.shape, w.shape, 1, 1), 7.0, device="cuda")
