@@ -330,3 +330,26 @@ def test_workload_conv_maxpool_lse_relu_sampled(tc):
     check(flat[idx], orc.conv_maxpool_lse_relu_at(x, w, b, idx, **wl.kwargs()), wl.name)
     # logsumexp over 64 channels >= their max, so ReLU rarely clips here
     assert np.all(flat >= 0.0)
+
+
+# --------------------------------------------------------------------------
+# second workloads at full size (outputs sampled on the device)
+# --------------------------------------------------------------------------
+def test_workload_conv331_p1_sampled(tc):
+    wl, x, w, b = _wl("conv331_p1")
+    y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), **wl.kwargs())
+    assert tuple(y.shape) == (16, 64, 254, 254, 10)
+    n = y.numel()
+    idx = np.concatenate([inputs.sample_indices(206, n, 20000), [0, n - 1]]).astype(np.int64)
+    got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    check(got, orc.conv3d_at(x, w, b, idx, **wl.kwargs()), wl.name)
+
+
+def test_workload_convT_s2p1d2_cin128_sampled(tc):
+    wl, x, w, b = _wl("convT_s2p1d2_cin128")
+    y = tc.conv_transpose3d_fwd(_dev(x), _dev(w), None, **wl.kwargs())
+    assert tuple(y.shape) == (16, 64, 33, 65, 65)
+    n = y.numel()
+    idx = np.concatenate([inputs.sample_indices(207, n, 20000), [0, n - 1]]).astype(np.int64)
+    got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    check(got, orc.conv_transpose3d_at(x, w, None, idx, **wl.kwargs()), wl.name)

@@ -1,4 +1,5 @@
-"""The five benchmark / parity workloads, with their synthetic input recipes.
+"""The five benchmark / parity workloads and two second workloads, with
+their synthetic input recipes.
 
 Shapes follow the four POPCORNBENCH transcript pages:
 
@@ -93,7 +94,21 @@ WORKLOADS = [
              desc="Conv3d 32->64 k3 p1 + MaxPool3d(2) + logsumexp_c + ReLU"),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Second workloads (not part of the default bench step): the (k,k,1) conv at
+# the shape "Kimi-K2.6 l1_p59" itself uses (Cin 3, Cout 64, a [16,3,256,256,10]
+# input; its 2.6 GB output makes it output-write-bound), and the k3 s2 p1 d2
+# transposed conv of "Kimi-K2.6 l1_p77" at a larger input channel count (Cin
+# 128), which makes the GEMM K 3456.  Seeds follow the same rule (i = 6, 7).
+EXTRA_WORKLOADS = [
+    Workload(6, "conv331_p1", "conv3d", (16, 3, 256, 256, 10), (64, 3, 3, 3, 1), True,
+             fan_in=3 * 9, desc="Conv3d (3,3,1) 3->64 at the page's original shape"),
+    Workload(7, "convT_s2p1d2_cin128", "conv_transpose3d", (16, 128, 16, 32, 32),
+             (128, 64, 3, 3, 3), False, stride=(2, 2, 2), padding=(1, 1, 1),
+             dilation=(2, 2, 2), fan_in=128 * 27,
+             desc="ConvTranspose3d 128->64 k3 s2 p1 d2"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def _axis_pairs(L, K, s, p, d, O, transposed):
