@@ -600,35 +600,38 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               tma_load_5d(dst, &p.xmap, xc, yc, zc, ch0, tc.n, bars.raw_full(stage));
             }
           } else {
-            // Box rows (channel, z, y) of box[2] elements: each row's
-            // coordinates are decoded once, lanes run along x, and the loads
-            // of 8 rows are in flight before their shared-memory stores.
-            float* d = reinterpret_cast<float*>(gbase + p.sm_raw + stage * p.raw_stage_bytes);
-            const int nrows = p.cin_chunk * p.box[0] * p.box[1];
+            // Element e of the box (channel-major, x fastest) is copied by
+            // lane e % 32 with a 4-byte cp.async (zero-filled outside the
+            // input), so the copies of the whole box are in flight together.
+            // A lane's box coordinates (cl, i0, i1, i2) advance by 32
+            // elements at a time with carries, without divisions.
+            const uint32_t dst0 = sbase + p.sm_raw + stage * p.raw_stage_bytes;
+            const int total = p.cin_chunk * bvol;
             const long long s12 = (long long)p.S[1] * p.S[2];
-            for (int xb = 0; xb < p.box[2]; xb += 32) {
-              const int i2 = xb + lane;
-              const int gx = xc + i2;
-              const bool xin = i2 < p.box[2] && gx >= 0 && gx < p.S[2];
-              for (int r0 = 0; r0 < nrows; r0 += 8) {
-                float v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                  const int r = r0 + u;
-                  const int i1 = r % p.box[1], rr = r / p.box[1];
-                  const int i0 = rr % p.box[0], cl = rr / p.box[0];
-                  const int gy = yc + i1, gz = zc + i0, ch = ch0 + cl;
-                  v[u] = 0.f;
-                  if (r < nrows && xin && ch < p.C && gy >= 0 && gy < p.S[1] && gz >= 0 &&
-                      gz < p.S[0])
-                    v[u] = __ldg(p.x + (((long long)tc.n * p.C + ch) * p.S[0] + gz) * s12 +
-                                 (long long)gy * p.S[2] + gx);
+            int i2 = lane % p.box[2], r = lane / p.box[2];
+            int i1 = r % p.box[1], i0 = (r / p.box[1]) % p.box[0];
+            int cl = r / (p.box[1] * p.box[0]);
+            for (int e = lane; e < total; e += 32) {
+              const int gx = xc + i2, gy = yc + i1, gz = zc + i0, ch = ch0 + cl;
+              const bool in = ch < p.C && gx >= 0 && gx < p.S[2] && gy >= 0 && gy < p.S[1] &&
+                              gz >= 0 && gz < p.S[0];
+              const float* src = in ? p.x + (((long long)tc.n * p.C + ch) * p.S[0] + gz) * s12 +
+                                          (long long)gy * p.S[2] + gx
+                                    : p.x;
+              cp_async4_zfill(dst0 + 4u * (uint32_t)e, src, in);
+              i2 += 32;
+              while (i2 >= p.box[2]) {
+                i2 -= p.box[2];
+                if (++i1 == p.box[1]) {
+                  i1 = 0;
+                  if (++i0 == p.box[0]) {
+                    i0 = 0;
+                    ++cl;
+                  }
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  if (r0 + u < nrows && i2 < p.box[2]) d[(r0 + u) * p.box[2] + i2] = v[u];
               }
             }
+            cp_async_wait_all();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.raw_full(stage));
           }

@@ -83,6 +83,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
+// 4-byte asynchronous global -> shared copies (no register round trip).  With
+// valid == false nothing is read and the destination word is zero-filled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+// wait until all of this thread's cp.async copies have landed
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // bulk copies (TMA engine)
 // ---------------------------------------------------------------------------
 // 1-D bulk copy global -> shared; dst, src 16-byte aligned, bytes % 16 == 0.
