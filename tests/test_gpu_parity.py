@@ -78,6 +78,10 @@ CONV_CASES = [
     ((2, 8, 6, 20, 4), (4, 8, 1, 3, 1), 1, (0, 1, 0), 1, 1, True),
     ((1, 40, 6, 6, 8), (16, 40, 3, 3, 1), 1, (1, 1, 0), 1, 1, True),  # 5 channel chunks
     ((1, 24, 5, 7, 8), (130, 24, 3, 3, 1), 1, 1, 1, 1, True),         # 2 column blocks: gather path
+    # merged (S1*S2) form of (k,k,1) convs: line segments, channels padded to octets
+    ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1, True),    # Cin 3, shifted windows
+    ((2, 3, 12, 14, 10), (6, 3, 3, 3, 1), 1, 0, 1, 1, True),          # x extent 10
+    ((1, 5, 7, 30, 6), (7, 5, 3, 5, 1), 1, (1, 4, 0), (1, 2, 1), 1, True),  # dilation along y
 ]
 
 

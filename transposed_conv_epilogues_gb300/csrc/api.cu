@@ -449,6 +449,7 @@ std::string describe(const Plan& pl) {
     append(s, ", \"a_stages\": %lld", pl.a_stages);
     append(s, ", \"ks_stage\": %lld", pl.ks_stage);
     append(s, ", \"view\": %lld", pl.view);
+    append(s, ", \"reshaped\": %lld", pl.reshaped);
     append(s, ", \"nslots\": %lld", pl.nslots);
     append(s, ", \"slot_bytes\": %lld", pl.slot_bytes);
     append(s, ", \"wide\": %lld", pl.wide);
@@ -537,7 +538,7 @@ int tc3d_out_shape(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int
   out_dims[0] = N;
   if (op == OP_CONV || op == OP_CONVT) {
     out_dims[1] = Cout;
-    for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.O[a];
+    for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.O_user[a];
   } else {
     out_dims[1] = op == OP_CONV_POOL_LSE ? 1 : Cout;
     for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.P[a];

@@ -537,11 +537,14 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   }
   if (warp == kWarpRaw && lane == 0 && p.use_tma) prefetch_tensormap(&p.xmap);
   if constexpr (VIEW) {
-    // per tap: raw-box position offset of the tap's window
+    // per tap: raw-box position offset of the tap's window.  A box's x start
+    // is rounded down to 16 bytes; tile x origins are multiples of 4, so the
+    // shift it leaves is the same for every tile.
     int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
+    const int xshift = p.u_min[2] - (p.u_min[2] & ~3);
     for (int t = threadIdx.x; t < p.nUtot; t += kThreads) {
       const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
-      ktab[t] = (p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2];
+      ktab[t] = (p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2] + xshift;
     }
   } else {
     // GEMM-K table of one channel chunk: raw-box offset of (channel, tap) pair k

@@ -102,7 +102,7 @@ SmemLayout smem_layout(const Plan& pl) {
   return L;
 }
 
-int make_plan(const Problem& pb_in, Plan* out) {
+static int make_plan_direct(const Problem& pb_in, Plan* out) {
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
   pl.pb = pb_in;
@@ -387,16 +387,25 @@ int make_plan(const Problem& pb_in, Plan* out) {
     if (pl.smem_bytes > kMaxSmem) return fail(TC3D_ERR_UNSUPPORTED);
   }
 
-  // ---- view mode: a plain stride-1 conv whose kernel has one tap along the
-  // contiguous axis (no x halo) and whose x lines fill 128-row accumulators
-  // exactly: row r of accumulator a is raw-box position a*B1*B2 + r
+  // ---- view mode: a plain stride-1 conv whose accumulators are runs of 128
+  // consecutive raw-box positions: row r of accumulator a is position
+  // a*B1*B2 + r (+ the tap's offset).  Two geometries qualify:
+  //   lines:    one tap along x (no x halo) and x lines filling 128 rows
+  //             (x extent 4..32): an accumulator is 128/S2 whole x lines;
+  //   segments: a y extent of 1 (the merged form of a (k,k,1) conv, see
+  //             make_plan): an accumulator is 128 consecutive x positions,
+  //             and an x halo only shifts a tap's window.
+  // Channels are padded to octets with zeros.
   {
     const int S2 = pb.S[2];
-    const bool shape_ok = pb.op == OP_CONV && pl.s_in[0] == 1 && pl.s_in[1] == 1 &&
-                          pl.s_in[2] == 1 && pl.nU[2] == 1 && pl.u_min[2] == 0 &&
-                          pl.M[2] == S2 && (S2 == 4 || S2 == 8 || S2 == 16 || S2 == 32) &&
-                          pl.cin_g % 8 == 0 && pl.n_tile <= 128 && pl.nR == 1;
-    if (shape_ok) {
+    const bool base_ok = pb.op == OP_CONV && pl.s_in[0] == 1 && pl.s_in[1] == 1 &&
+                         pl.s_in[2] == 1 && pl.n_tile <= 128 && pl.nR == 1 &&
+                         pl.n_colblocks == 1;
+    const bool lines = base_ok && pl.nU[2] == 1 && pl.u_min[2] == 0 && pl.M[2] == S2 &&
+                       (S2 == 4 || S2 == 8 || S2 == 16 || S2 == 32);
+    const bool segments = base_ok && !lines && pb.S[1] == 1 && pl.nU[1] == 1 &&
+                          pl.u_min[1] == 0 && pl.M[1] == 1;
+    if (lines || segments) {
       Plan v = pl;
       v.view = 1;
       v.dbuf = 2;
@@ -405,46 +414,51 @@ int make_plan(const Problem& pb_in, Plan* out) {
       v.n_acc = 2;
       v.ks_stage = 0;
       v.a_stages = 0;
-      v.Q[0] = 1;
-      v.Q[1] = 32 / S2;
-      v.Q[2] = S2;
-      v.Pq[0] = 2;
-      v.Pq[1] = 4;
-      v.Pq[2] = 1;
+      if (lines) {
+        v.Q[0] = 1, v.Q[1] = 32 / S2, v.Q[2] = S2;
+        v.Pq[0] = 2, v.Pq[1] = 4, v.Pq[2] = 1;
+      } else {
+        v.Q[0] = 1, v.Q[1] = 1, v.Q[2] = 32;
+        v.Pq[0] = 2, v.Pq[1] = 1, v.Pq[2] = 4;
+      }
       for (int a = 0; a < 3; ++a) {
         v.T[a] = v.Q[a] * v.Pq[a];
         v.ntile[a] = (int)ceil_div(v.M[a], v.T[a]);
-        v.box[a] = (int)(v.T[a] + v.u_max[a] - v.u_min[a]);
+        v.box[a] = box_extent(v, a, v.T[a]);
       }
-      v.xslack = 0;
+      v.xslack = x_slack(v, v.T[2]);
       v.tiles = (int64_t)pb.N * v.ntile[0] * v.ntile[1] * v.ntile[2];
       const int64_t bvol = (int64_t)v.box[0] * v.box[1] * v.box[2];
       const int ntaps = nUtot;
       v.slot_bytes = 2 * bvol * 8 * 4;
       v.nslots = 2;
-      // weights stay resident: (cin_g / 8) * ntaps K-steps of 64 * n_tile bytes
-      const int64_t wbytes = (int64_t)(v.cin_g / 8) * ntaps * 64 * v.n_tile;
       const int64_t fixed = 4096 + 1024 + 1024 + 1024 + round_up((int64_t)ntaps * 4, 1024);
+      const int cin_pad = (int)round_up(v.cin_g, 8);
       int best = 0;
-      for (int cc = 8; cc <= v.cin_g; cc += 8) {
-        if (v.cin_g % cc) continue;
+      int64_t best_w = 0;
+      for (int cc = 8; cc <= cin_pad; cc += 8) {
+        // weights stay resident: chunks x octets x taps K-steps of 64 * n_tile bytes
+        const int64_t wbytes = ceil_div(v.cin_g, cc) * (cc / 8) * ntaps * 64LL * v.n_tile;
         const int64_t raw = round_up(cc * bvol * 4, 1024);
-        if (2 * raw + v.nslots * v.slot_bytes + wbytes + fixed <= kMaxSmem) best = cc;
+        if (2 * raw + v.nslots * v.slot_bytes + wbytes + fixed <= kMaxSmem) {
+          best = cc;
+          best_w = wbytes;
+        }
       }
       if (best > 0 && bvol <= 16383 && v.box[0] <= 256 && v.box[1] <= 256 &&
-          v.tiles < ((int64_t)1 << 31)) {
+          v.box[2] <= 256 && v.tiles < ((int64_t)1 << 31)) {
         v.cin_chunk = best;
-        v.n_chunks = v.cin_g / best;
+        v.n_chunks = (int)ceil_div(v.cin_g, best);
         v.k_chunk = best * ntaps;
         v.ksteps_chunk = (best / 8) * ntaps;
         v.raw_stage_bytes = round_up(best * bvol * 4, 1024);
         v.b_resident = 1;
         v.b_stage_bytes = 64LL * v.n_tile;
         v.b_stages = (int)((int64_t)v.n_chunks * v.ksteps_chunk);
-        const int64_t used = 2 * v.raw_stage_bytes + v.nslots * v.slot_bytes + wbytes + fixed;
+        const int64_t used = 2 * v.raw_stage_bytes + v.nslots * v.slot_bytes + best_w + fixed;
         v.raw_stages = used + v.raw_stage_bytes <= kMaxSmem ? 3 : 2;
         v.smem_bytes = smem_layout(v).total;
-        if (v.smem_bytes <= kMaxSmem && v.n_colblocks == 1) pl = v;
+        if (v.smem_bytes <= kMaxSmem) pl = v;
       }
     }
   }
@@ -476,4 +490,41 @@ int make_plan(const Problem& pb_in, Plan* out) {
   return TC3D_OK;
 }
 
+// A conv whose kernel has one tap along the contiguous axis, with no padding
+// there, is the same conv over a merged (S1 * S2) axis: x as [N, C, S0, 1,
+// S1*S2] with kernel (k0, 1, k1), dilation (d0, 1, d1*S2) and padding
+// (p0, 0, p1*S2) -- a tap along S1 shifts the merged index by whole lines
+// of S2, and indices outside the merged line are exactly the padded ones.
+// The output is y itself, read as [N, Cout, O0, 1, O1*S2].  The merged form
+// is used when it runs in view mode; the plan then keeps the caller's
+// output extents in O_user.
+int make_plan(const Problem& pb, Plan* out) {
+  if (pb.op == OP_CONV && pb.k[2] == 1 && pb.pad[2] == 0 && pb.stride[0] == 1 &&
+      pb.stride[1] == 1 && pb.stride[2] == 1 && pb.groups == 1 &&
+      validate(pb, false) == TC3D_OK && (int64_t)pb.S[1] * pb.S[2] < (1 << 30)) {
+    Problem m = pb;
+    m.S[1] = 1;
+    m.S[2] = pb.S[1] * pb.S[2];
+    m.k[1] = 1;
+    m.k[2] = pb.k[1];
+    m.pad[1] = 0;
+    m.pad[2] = pb.pad[1] * pb.S[2];
+    m.dil[1] = 1;
+    m.dil[2] = pb.dil[1] * pb.S[2];
+    Plan pm;
+    if (make_plan_direct(m, &pm) == TC3D_OK && pm.view) {
+      pm.reshaped = 1;
+      pm.O_user[0] = pm.O[0];
+      pm.O_user[1] = conv_len(pb.S[1], pb.k[1], 1, pb.pad[1], pb.dil[1]);
+      pm.O_user[2] = pb.S[2];
+      *out = pm;
+      return TC3D_OK;
+    }
+  }
+  const int st = make_plan_direct(pb, out);
+  for (int a = 0; a < 3; ++a) out->O_user[a] = out->O[a];
+  return st;
+}
+
 }  // namespace tc3d
+

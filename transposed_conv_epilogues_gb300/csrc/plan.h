@@ -98,6 +98,10 @@ struct Plan {
   int view;
   int nslots;
   int64_t slot_bytes;
+  // 1: planned in the merged (S1*S2) form of a (k,k,1) conv (see make_plan);
+  // O_user are then the caller's output extents, O the merged ones
+  int reshaped;
+  int64_t O_user[3];
 
   // workspace (bytes, each region 256-aligned)
   int64_t ws_wpack_off, ws_wpack_bytes;
