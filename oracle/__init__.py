@@ -18,7 +18,9 @@ Definitions and their sources (the four POPCORNBENCH transcript pages):
   receive-form derivation); ``conv_transpose3d_scatter`` -- the scatter view
   of the same page, an independent second formulation.
 * ``maxpool3d_2`` / ``logsumexp_channels`` / ``relu`` -- "Kimi-K2.6 l2_p43".
-* ``batchnorm3d_train`` / ``avgpool3d_2`` -- "Kimi-K2.6 l2_p72".
+* ``batchnorm3d_train`` / ``avgpool3d_2`` -- "Kimi-K2.6 l2_p72";
+  ``batchnorm3d_eval`` -- the same page's fused kernel, which normalises with
+  running statistics (evaluation mode).
 
 Parity pins: every function is pinned by ``tests/test_oracle.py`` (sizes from
 the pages, adjoint identity, impulse response, slice-wise 2-D conv, per-voxel
@@ -92,6 +94,9 @@ def _load():
         "oracle_batchnorm3d_train": [D, D, I, I, L, D, D, F, D, D],
         "oracle_convT_bn_avgpool": [D, D, D, D, D, F, D] + geom + [I3, I, I],
         "oracle_convT_bn_avgpool_at": [D, D, D, D, D, F] + geom + [I3, I, _I64P, L, D, D, D, I],
+        "oracle_batchnorm3d_eval": [D, D, I, I, L, D, D, D, D, F],
+        "oracle_convT_bneval_avgpool": [D, D, D, D, D, D, D, F, D] + geom + [I3, I, I],
+        "oracle_convT_bneval_avgpool_at": [D, D, D, D, D, D, D, F] + geom + [I3, I, _I64P, L, D, I],
         "oracle_conv_maxpool_lse_relu": [D, D, D, D] + geom + [I, I],
         "oracle_conv_maxpool_lse_relu_at": [D, D, D] + geom + [I, _I64P, L, D, I],
     }
@@ -338,6 +343,69 @@ def convT_bn_avgpool_at(x, w, b, idx, gamma=None, beta=None, eps=1e-5, stride=1,
         idx.ctypes.data_as(_I64P), ctypes.c_int64(idx.size), out.ctypes.data_as(_DP), mean.ctypes.data_as(_DP),
         var.ctypes.data_as(_DP), _threads(nthreads)), "convT_bn_avgpool_at")
     return (out, mean, var) if return_stats else out
+
+
+def batchnorm3d_eval(t, running_mean, running_var, gamma=None, beta=None, eps=1e-5):
+    """BatchNorm3d in evaluation mode: (t - running_mean) / sqrt(running_var + eps)
+    * gamma + beta per channel ("Kimi-K2.6 l2_p72", its fused kernel's form)."""
+    t, tp = _d(t)
+    rm, rmp = _d(running_mean)
+    rv, rvp = _d(running_var)
+    g, gp = _d(gamma)
+    be, bep = _d(beta)
+    N, C = t.shape[:2]
+    L = int(np.prod(t.shape[2:]))
+    out = np.empty_like(t)
+    _check(_load().oracle_batchnorm3d_eval(tp, out.ctypes.data_as(_DP), N, C, ctypes.c_int64(L),
+                                           rmp, rvp, gp, bep, ctypes.c_double(eps)),
+           "batchnorm3d_eval")
+    return out
+
+
+def convT_bneval_avgpool(x, w, b, running_mean, running_var, gamma=None, beta=None, eps=1e-5,
+                         stride=1, padding=0, dilation=1, output_padding=0, groups=1,
+                         nthreads=None):
+    """ConvTranspose3d -> BatchNorm3d (running stats) -> AvgPool3d(2) -> AvgPool3d(2)."""
+    x, xp = _d(x)
+    w, wp = _d(w)
+    b, bp = _d(b)
+    rm, rmp = _d(running_mean)
+    rv, rvp = _d(running_var)
+    g, gp = _d(gamma)
+    be, bep = _d(beta)
+    N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
+    shp = convT_out_shape(x.shape, w.shape, stride, padding, dilation, output_padding, groups)
+    out_shape = shp[:2] + tuple(o // 2 // 2 for o in shp[2:])
+    y = np.empty(out_shape, np.float64)
+    _check(_load().oracle_convT_bneval_avgpool(
+        xp, wp, bp, rmp, rvp, gp, bep, ctypes.c_double(eps), y.ctypes.data_as(_DP), N, Cin, S0,
+        S1, S2, shp[1], k0, k1, k2, _i3(stride), _i3(padding), _i3(dilation),
+        _i3(output_padding), groups, _threads(nthreads)), "convT_bneval_avgpool")
+    return y
+
+
+def convT_bneval_avgpool_at(x, w, b, running_mean, running_var, idx, gamma=None, beta=None,
+                            eps=1e-5, stride=1, padding=0, dilation=1, output_padding=0,
+                            groups=1, nthreads=None):
+    x, xp = _d(x)
+    w, wp = _d(w)
+    b, bp = _d(b)
+    rm, rmp = _d(running_mean)
+    rv, rvp = _d(running_var)
+    g, gp = _d(gamma)
+    be, bep = _d(beta)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+    N, Cin, S0, S1, S2, k0, k1, k2 = _geom(x, w)
+    _check_w(x, w, groups, True)
+    Cout = w.shape[1] * groups
+    out = np.empty(idx.shape, np.float64)
+    _check(_load().oracle_convT_bneval_avgpool_at(
+        xp, wp, bp, rmp, rvp, gp, bep, ctypes.c_double(eps), N, Cin, S0, S1, S2, Cout, k0, k1,
+        k2, _i3(stride), _i3(padding), _i3(dilation), _i3(output_padding), groups,
+        idx.ctypes.data_as(_I64P), ctypes.c_int64(idx.size), out.ctypes.data_as(_DP),
+        _threads(nthreads)), "convT_bneval_avgpool_at")
+    return out
 
 
 def conv_maxpool_lse_relu(x, w, b=None, stride=1, padding=0, dilation=1, groups=1,

@@ -481,6 +481,54 @@ int oracle_convT_bn_avgpool(const double *x, const double *w, const double *b, c
     return rc;
 }
 
+int oracle_batchnorm3d_eval(const double *t, double *out, int N, int C, int64_t L,
+                            const double *rmean, const double *rvar, const double *gamma,
+                            const double *beta, double eps) {
+    if (!t || !out || !rmean || !rvar || N <= 0 || C <= 0 || L <= 0 || !(eps >= 0.0)) return -1;
+    for (int c = 0; c < C; ++c) {
+        const double g = gamma ? gamma[c] : 1.0, be = beta ? beta[c] : 0.0;
+        const double inv = 1.0 / sqrt(rvar[c] + eps);
+        for (int n = 0; n < N; ++n) {
+            const double *tc = t + ((int64_t)n * C + c) * L;
+            double *oc = out + ((int64_t)n * C + c) * L;
+            for (int64_t i = 0; i < L; ++i) oc[i] = (tc[i] - rmean[c]) * inv * g + be;
+        }
+    }
+    return 0;
+}
+
+int oracle_convT_bneval_avgpool(const double *x, const double *w, const double *b,
+                                const double *rmean, const double *rvar, const double *gamma,
+                                const double *beta, double eps, double *y, int N, int Cin,
+                                int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                                const int stride[3], const int pad[3], const int dil[3],
+                                const int out_pad[3], int groups, int nthreads) {
+    prob_t P;
+    if (!y || fill_prob(&P, x, w, b, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil,
+                        out_pad, groups, 1))
+        return -1;
+    const int64_t O0 = P.O[0], O1 = P.O[1], O2 = P.O[2];
+    const int64_t Q0 = O0 / 2, Q1 = O1 / 2, Q2 = O2 / 2;
+    if (Q0 / 2 <= 0 || Q1 / 2 <= 0 || Q2 / 2 <= 0) return -1;
+    const int64_t nc = (int64_t)N * Cout;
+    double *t = (double *)malloc(sizeof(double) * (size_t)(nc * O0 * O1 * O2));
+    double *u = (double *)malloc(sizeof(double) * (size_t)(nc * O0 * O1 * O2));
+    if (!t || !u) {
+        free(t);
+        free(u);
+        return -1;
+    }
+    int rc = oracle_conv_transpose3d(x, w, b, t, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad,
+                                     dil, out_pad, groups, nthreads);
+    if (!rc)
+        rc = oracle_batchnorm3d_eval(t, u, N, Cout, O0 * O1 * O2, rmean, rvar, gamma, beta, eps);
+    if (!rc) rc = oracle_avgpool3d_2(u, t, N, Cout, (int)O0, (int)O1, (int)O2);
+    if (!rc) rc = oracle_avgpool3d_2(t, y, N, Cout, (int)Q0, (int)Q1, (int)Q2);
+    free(t);
+    free(u);
+    return rc;
+}
+
 /* per-(n, c) slice statistics for the sampled BN composite */
 typedef struct {
     const prob_t *P;
@@ -610,6 +658,31 @@ int oracle_convT_bn_avgpool_at(const double *x, const double *w, const double *b
     free(s2);
     free(mean);
     free(var);
+    return 0;
+}
+
+int oracle_convT_bneval_avgpool_at(const double *x, const double *w, const double *b,
+                                   const double *rmean, const double *rvar, const double *gamma,
+                                   const double *beta, double eps, int N, int Cin, int S0, int S1,
+                                   int S2, int Cout, int k0, int k1, int k2, const int stride[3],
+                                   const int pad[3], const int dil[3], const int out_pad[3],
+                                   int groups, const int64_t *idx, int64_t count, double *out,
+                                   int nthreads) {
+    prob_t P;
+    if (!rmean || !rvar ||
+        fill_prob(&P, x, w, b, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad,
+                  groups, 1) ||
+        !(eps >= 0.0))
+        return -1;
+    const int64_t R0 = P.O[0] / 2 / 2, R1 = P.O[1] / 2 / 2, R2 = P.O[2] / 2 / 2;
+    if (R0 <= 0 || R1 <= 0 || R2 <= 0) return -1;
+    if (check_idx(idx, count, (int64_t)N * Cout * R0 * R1 * R2) || (count && !out)) return -1;
+    P.idx = idx;
+    P.out = out;
+    /* the literal two-stage pooling of BN(convT) at every sampled output, with
+     * the running statistics in place of batch statistics */
+    bnpool_ctx bc = {&P, rmean, rvar, gamma, beta, eps};
+    par_for(count, nthreads, 4, bnpool_range, &bc);
     return 0;
 }
 

@@ -104,6 +104,37 @@ int oracle_batchnorm3d_train(const double *t, double *out, int N, int C,
                              int64_t L, const double *gamma, const double *beta,
                              double eps, double *mean_out, double *var_out);
 
+/* BatchNorm3d forward in evaluation mode (the l2_p72 page's own fused
+ * kernel, which read running statistics): per channel c,
+ * out = (t - rmean[c]) / sqrt(rvar[c] + eps) * gamma[c] + beta[c].
+ * gamma/beta may be NULL (1 and 0). */
+int oracle_batchnorm3d_eval(const double *t, double *out, int N, int C,
+                            int64_t L, const double *rmean, const double *rvar,
+                            const double *gamma, const double *beta, double eps);
+
+/* Composite: ConvTranspose3d(+bias) -> BatchNorm3d (running stats, eval
+ * mode) -> AvgPool3d(2) -> AvgPool3d(2), each step literally, in that order.
+ * y [N, Cout, P0, P1, P2] with P = floor(floor(O/2)/2). */
+int oracle_convT_bneval_avgpool(const double *x, const double *w, const double *b,
+                                const double *rmean, const double *rvar,
+                                const double *gamma, const double *beta, double eps,
+                                double *y, int N, int Cin, int S0, int S1, int S2,
+                                int Cout, int k0, int k1, int k2, const int stride[3],
+                                const int pad[3], const int dil[3],
+                                const int out_pad[3], int groups, int nthreads);
+
+/* Same composite at `count` flat indices of y (each pooled output from its
+ * 64 transposed-conv points; no statistics are needed). */
+int oracle_convT_bneval_avgpool_at(const double *x, const double *w, const double *b,
+                                   const double *rmean, const double *rvar,
+                                   const double *gamma, const double *beta, double eps,
+                                   int N, int Cin, int S0, int S1, int S2, int Cout,
+                                   int k0, int k1, int k2, const int stride[3],
+                                   const int pad[3], const int dil[3],
+                                   const int out_pad[3], int groups,
+                                   const int64_t *idx, int64_t count, double *out,
+                                   int nthreads);
+
 /* Composite: ConvTranspose3d(+bias) -> BatchNorm3d (batch stats) ->
  * AvgPool3d(2) -> AvgPool3d(2), each step literally, in that order (l2_p72).
  * y [N, Cout, P0, P1, P2] with P = floor(floor(O/2)/2). */

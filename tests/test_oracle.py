@@ -351,6 +351,52 @@ def test_bn_commutes_with_avgpool(oracle):
     assert _rel(a, b) <= 1e-13
 
 
+def test_batchnorm_eval_closed_forms(oracle):
+    """Evaluation-mode BN (running statistics, l2_p72's fused kernel):
+    identity statistics give the input back exactly, eps = 0 with a perfect
+    square variance gives a hand-checkable affine map, and running statistics
+    equal to the batch moments reproduce training mode."""
+    t = 3.0 + 2.0 * rng.standard_normal((3, 4, 2, 5, 3))
+    C = t.shape[1]
+    eps = 1e-5
+    ident = oracle.batchnorm3d_eval(t, np.zeros(C), np.ones(C), None, None, 0.0)
+    np.testing.assert_array_equal(ident, t)
+    rm = np.array([2.0, -1.0, 0.5, 0.0])
+    rv = np.array([4.0, 0.25, 1.0, 16.0])
+    g = np.array([1.5, -2.0, 0.0, 1.0])
+    be = np.array([0.0, 1.0, 3.0, -4.0])
+    out = oracle.batchnorm3d_eval(t, rm, rv, g, be, 0.0)
+    sd = np.array([2.0, 0.5, 1.0, 4.0])
+    want = (t - rm[None, :, None, None, None]) / sd[None, :, None, None, None] \
+        * g[None, :, None, None, None] + be[None, :, None, None, None]
+    np.testing.assert_allclose(out, want, rtol=1e-15, atol=1e-15)
+    assert np.all(out[:, 2] == 3.0)  # gamma 0: the channel is beta alone
+    tr, mean, var = oracle.batchnorm3d_train(t, g, be, eps, return_stats=True)
+    ev = oracle.batchnorm3d_eval(t, mean, var, g, be, eps)
+    np.testing.assert_allclose(ev, tr, rtol=1e-13, atol=1e-13)
+
+
+def test_convT_bneval_avgpool_reductions(oracle):
+    """The eval composite reduces to the pinned pieces: identity statistics
+    give avgpool(avgpool(convT)), and the batch moments as running
+    statistics give the training-mode composite."""
+    x = rng.standard_normal((2, 3, 5, 6, 5))
+    W = rng.standard_normal((3, 4, 3, 3, 3))
+    b = rng.standard_normal(4)
+    g = rng.standard_normal(4)
+    be = rng.standard_normal(4)
+    kt = dict(stride=2, padding=1)
+    C = 4
+    y = oracle.convT_bneval_avgpool(x, W, b, np.zeros(C), np.ones(C), None, None, 0.0, **kt)
+    ref = oracle.avgpool3d_2(oracle.avgpool3d_2(oracle.conv_transpose3d(x, W, b, **kt)))
+    assert _rel(y, ref) <= 1e-14
+    full = oracle.conv_transpose3d(x, W, b, **kt)
+    mean, var = full.mean(axis=(0, 2, 3, 4)), full.var(axis=(0, 2, 3, 4))
+    ev = oracle.convT_bneval_avgpool(x, W, b, mean, var, g, be, 1e-5, **kt)
+    tr = oracle.convT_bn_avgpool(x, W, b, g, be, 1e-5, **kt)
+    assert _rel(ev, tr) <= 1e-12
+
+
 # --------------------------------------------------------------------------
 # sampled evaluators equal the full ones
 # --------------------------------------------------------------------------
@@ -383,6 +429,13 @@ def test_sampled_equal_full(oracle):
     full = oracle.conv_transpose3d(xs, Wt, bt, **kt)
     np.testing.assert_allclose(mean, full.mean(axis=(0, 2, 3, 4)), rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(var, full.var(axis=(0, 2, 3, 4)), rtol=1e-12)
+    rm = rng.standard_normal(6)
+    rv = rng.uniform(0.5, 2.0, 6)
+    g = rng.standard_normal(6)
+    be = rng.standard_normal(6)
+    e = oracle.convT_bneval_avgpool(xs, Wt, bt, rm, rv, g, be, 1e-5, **kt)
+    es = oracle.convT_bneval_avgpool_at(xs, Wt, bt, rm, rv, np.arange(e.size), g, be, 1e-5, **kt)
+    assert _rel(es, e.ravel()) <= 1e-12
 
 
 # --------------------------------------------------------------------------
@@ -441,6 +494,26 @@ def test_convT_bn_avgpool_vs_torch(oracle):
     t = F.batch_norm(t, None, None, _t(g), _t(be), training=True, eps=1e-5)
     t = F.avg_pool3d(F.avg_pool3d(t, 2), 2)
     assert _rel(y, t.numpy()) <= 1e-12
+
+
+def test_convT_bneval_avgpool_vs_torch(oracle):
+    x = rng.standard_normal((2, 3, 7, 8, 9))
+    W = rng.standard_normal((3, 6, 3, 2, 3))
+    b = rng.standard_normal(6)
+    rm = rng.standard_normal(6)
+    rv = rng.uniform(0.2, 3.0, 6)
+    g = rng.standard_normal(6)
+    be = rng.standard_normal(6)
+    kt = dict(stride=(2, 2, 1), padding=(1, 0, 1), output_padding=(1, 0, 0))
+    y = oracle.convT_bneval_avgpool(x, W, b, rm, rv, g, be, 1e-5, **kt)
+    t = F.conv_transpose3d(_t(x), _t(W), _t(b), (2, 2, 1), (1, 0, 1), (1, 0, 0))
+    t = F.batch_norm(t, _t(rm), _t(rv), _t(g), _t(be), training=False, eps=1e-5)
+    t = F.avg_pool3d(F.avg_pool3d(t, 2), 2)
+    assert _rel(y, t.numpy()) <= 1e-12
+    rb = oracle.batchnorm3d_eval(x, rm[:3], rv[:3], g[:3], be[:3], 1e-3)
+    tb = F.batch_norm(_t(x), _t(rm[:3]), _t(rv[:3]), _t(g[:3]), _t(be[:3]), training=False,
+                      eps=1e-3)
+    assert _rel(rb, tb.numpy()) <= 1e-14
 
 
 def test_conv_maxpool_lse_relu_vs_torch(oracle):
