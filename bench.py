@@ -131,6 +131,7 @@ def recorded_traffic(kernel_workload):
 # CPU oracle on bounded samples (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 ORACLE_SAMPLES = {"conv331": 20000000, "convT_s2p1d2": 6000000, "convT_bn_avgpool": 20000000,
+                  "convT_bneval_avgpool": 20000000,
                   "conv_maxpool_lse_relu": 2000000}
 
 
@@ -198,7 +199,11 @@ def run_ours(args):
     names = args.workloads.split(",")
     wls = [W.BY_NAME[n] for n in names]
     host = {n: W.BY_NAME[n].make_inputs() for n in names}
+    # evaluation-mode BatchNorm: running mean / variance, gamma, beta
+    host_bn = {wl.name: wl.make_bn_eval_params() for wl in wls
+               if wl.op == "convT_bneval_avgpool"}
     dev_in = {}
+    dev_bn = {n: tuple(torch.from_numpy(a).to(dev) for a in v) for n, v in host_bn.items()}
     outs = {}
     for wl in wls:
         x, w, b = host[wl.name]
@@ -207,14 +212,14 @@ def run_ours(args):
         outs[wl.name] = torch.empty(W.y_shape(wl), dtype=torch.float32, device=dev)
 
     op_of = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2,
-             "convT_bn_avgpool": 3}
+             "convT_bn_avgpool": 3, "convT_bneval_avgpool": 4}
     wss = {}
     for wl in wls:
         nb = tc.workspace_bytes(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
                                 wl.dilation, wl.output_padding, wl.groups)
         wss[wl.name] = torch.empty(nb, dtype=torch.uint8, device=dev)
 
-    def call(wl, x, w, b, out):
+    def call(wl, x, w, b, out, bn=None):
         kw = dict(stride=wl.stride, padding=wl.padding, dilation=wl.dilation, groups=wl.groups,
                   out=out, workspace=wss[wl.name])
         if wl.op == "conv3d":
@@ -223,11 +228,18 @@ def run_ours(args):
             return tc.conv_transpose3d_fwd(x, w, b, output_padding=wl.output_padding, **kw)
         if wl.op == "conv_maxpool_lse_relu":
             return tc.conv_maxpool_lse_relu(x, w, b, **kw)
+        if wl.op == "convT_bneval_avgpool":
+            rm, rv, g, be = bn if bn is not None else dev_bn[wl.name]
+            return tc.convT_bneval_avgpool(x, w, b, rm, rv, g, be, wl.eps,
+                                           output_padding=wl.output_padding, **kw)
         return tc.convT_bn_avgpool(x, w, b, None, None, wl.eps,
                                    output_padding=wl.output_padding, **kw)
 
+    # library launches per call: weight pack + engine (+ the transposed
+    # conv's bias slab fill; + BatchNorm finalize and apply for batch
+    # statistics; + the running-statistics affine for evaluation mode)
     launches_per_call = {"conv3d": 2, "conv_transpose3d": 3, "conv_maxpool_lse_relu": 2,
-                         "convT_bn_avgpool": 4}
+                         "convT_bn_avgpool": 4, "convT_bneval_avgpool": 3}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = {wl.name: [] for wl in wls}
@@ -311,8 +323,11 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     pinned_in = {}
+    pinned_bn = {n: tuple(torch.from_numpy(a).pin_memory() for a in v)
+                 for n, v in host_bn.items()}
     pinned_out = {}
-    h2d = d2h = 0
+    h2d = sum(a.numel() * 4 for v in pinned_bn.values() for a in v)
+    d2h = 0
     for wl in wls:
         pinned_in[wl.name] = tuple(None if a is None else torch.from_numpy(a).pin_memory()
                                    for a in host[wl.name])
@@ -331,7 +346,9 @@ def run_ours(args):
         for wl in wls:
             d = tuple(None if a is None else a.to(dev, non_blocking=True)
                       for a in pinned_in[wl.name])
-            y = call(wl, *d, None)
+            bn = (tuple(a.to(dev, non_blocking=True) for a in pinned_bn[wl.name])
+                  if wl.name in pinned_bn else None)
+            y = call(wl, *d, None, bn)
             pinned_out[wl.name].copy_(y, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -350,7 +367,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "tf32x3",
         "data": "synthetic: seeded splitmix64, x ~ N(0,1), w and bias ~ U(+-1/sqrt(fan_in))",
         "config": {
-            "workload": "+".join(names) + " (the four full-size configs, one call each)",
+            "workload": "+".join(names) + (" (the four full-size configs, one call each)"
+                                           if names == BENCH_WORKLOADS else " (one call each)"),
             "per_workload": per,
             "l2": "flushed by a 256 MB device write before every timed call",
             "parallelism": "replicas" if world > 1 else "single GPU",

@@ -21,6 +21,11 @@
  *                              -> AvgPool3d(2) ("Kimi-K2.6 l2_p72", problem
  *                              statement; the two pools are one 4x4x4 pool
  *                              by that page's pooling derivation).
+ *   tc3d_convT_bneval_avgpool  the same pipeline with BatchNorm3d in
+ *                              evaluation mode: the running mean and
+ *                              variance replace the batch statistics (the
+ *                              same page's first fused kernel, which reads
+ *                              running_mean / running_var).
  *
  * Common conventions for every entry point:
  *  - Tensors are contiguous NCDHW fp32 in device memory.  Spatial axes are
@@ -31,7 +36,8 @@
  *    (per-axis values).  output_padding may be NULL (zeros) and must be
  *    zeros for the convolutions; for transposed convolutions each entry
  *    must be smaller than max(stride, dilation) of its axis.
- *  - bias, gamma, beta may be NULL (meaning 0, 1, 0).
+ *  - bias, gamma, beta may be NULL (meaning 0, 1, 0).  BatchNorm parameter
+ *    and statistics arrays are [Cout] fp32.
  *  - workspace: caller-owned device memory of at least the size
  *    tc3d_workspace_bytes reports for the same arguments, 256-byte aligned.
  *    It holds the tensor-core-packed weights (and, for the fused BatchNorm,
@@ -73,6 +79,7 @@ extern "C" {
 #define TC3D_OP_CONV_TRANSPOSE3D 1
 #define TC3D_OP_CONV_MAXPOOL_LSE_RELU 2
 #define TC3D_OP_CONVT_BN_AVGPOOL 3
+#define TC3D_OP_CONVT_BNEVAL_AVGPOOL 4
 
 /* y[n,oc,o] = bias[oc] + sum_{ic in group(oc), k} w[oc,ic',k] *
  *             x[n, ic, o*stride - pad + dilation*k]   (zero outside x)
@@ -114,6 +121,23 @@ int tc3d_convT_bn_avgpool(const float* x, const float* w, const float* bias, con
                           const int stride[3], const int pad[3], const int dilation[3],
                           const int output_padding[3], int groups, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
+
+/* t = conv_transpose3d (as above); per channel c,
+ * b = (t - running_mean[c]) / sqrt(running_var[c] + eps) * gamma[c] + beta[c];
+ * y = AvgPool3d(2)(AvgPool3d(2)(b)), floor mode.  y: as tc3d_convT_bn_avgpool.
+ * running_mean, running_var: [Cout] fp32 device arrays, read only (not
+ * updated: evaluation mode keeps them fixed); both required (TC3D_ERR_NULL
+ * otherwise).  gamma, beta may be NULL.  eps >= 0.  When the transposed conv
+ * has stride 2 on every axis and all 8 output-parity classes carry taps, the
+ * whole pipeline is one engine pass that stores final values; otherwise the
+ * transposed-conv output goes through the workspace. */
+int tc3d_convT_bneval_avgpool(const float* x, const float* w, const float* bias,
+                              const float* running_mean, const float* running_var,
+                              const float* gamma, const float* beta, float eps, float* y, int N,
+                              int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                              const int stride[3], const int pad[3], const int dilation[3],
+                              const int output_padding[3], int groups, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Scratch size of tc3d_conv_maxpool_lse_relu_noalloc (1 MiB). */
 #define TC3D_NOALLOC_SCRATCH_BYTES (1 << 20)

@@ -73,7 +73,8 @@ def test_out_shapes_vs_oracle(lib, oracle):
 
 def test_workload_shapes(lib):
     from transposed_conv_epilogues_gb300.workloads import WORKLOADS
-    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3}
+    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3,
+           "convT_bneval_avgpool": 4}
     expect = {1: (2, 8, 14, 14, 4), 2: (16, 64, 126, 126, 8), 3: (16, 64, 33, 65, 65),
               4: (64, 16, 15, 15, 15), 5: (4, 1, 16, 64, 64)}
     for wl in WORKLOADS:
@@ -138,8 +139,37 @@ def test_convT_bn_avgpool_argument_errors(lib):
     assert call(_geom(s=(2, 2, 2)), eps=-1.0) == tc.TC3D_ERR_SHAPE
 
 
+def test_convT_bneval_avgpool_argument_errors(lib):
+    fn = lib.tc3d_convT_bneval_avgpool
+    P = ctypes.c_void_p
+    dummy = P(256)
+
+    def call(geom, eps=1e-5, ws=256, x=P(256), rm=P(2048), rv=P(4096)):
+        return fn(x, P(512), None, rm, rv, None, None, ctypes.c_float(eps), P(1024), *geom,
+                  dummy if ws else None, ctypes.c_size_t(ws), None)
+
+    g2 = _geom(s=(2, 2, 2))
+    assert call(_geom(S=(2, 2, 2), s=(2, 2, 2), p=(1, 1, 1))) == tc.TC3D_ERR_SHAPE  # 3 -> 0
+    assert call(g2, x=None) == tc.TC3D_ERR_NULL
+    assert call(g2, rm=None) == tc.TC3D_ERR_NULL
+    assert call(g2, rv=None) == tc.TC3D_ERR_NULL
+    assert call(g2, ws=0) == tc.TC3D_ERR_WORKSPACE
+    assert call(g2, eps=-1.0) == tc.TC3D_ERR_SHAPE
+    big = 1 << 24
+    assert call(g2, ws=big, rm=P(2050)) == tc.TC3D_ERR_ALIGN
+    # same plan as the batch-statistics op, but no partial-sum region
+    a = tc.plan_describe(3, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1)
+    b = tc.plan_describe(4, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1)
+    assert b["fused"] == a["fused"] == 1 and b["tiles"] == a["tiles"]
+    wa = tc.workspace_bytes(3, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1)
+    wb = tc.workspace_bytes(4, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1)
+    assert wb < wa
+    assert tc.out_shape(4, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1) == tc.out_shape(
+        3, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1) == (2, 16, 3, 3, 3)
+
+
 def test_workspace_bytes(lib):
-    for op in range(4):
+    for op in range(5):
         n = tc.workspace_bytes(op, (2, 4, 9, 9, 9), (4, 4, 3, 3, 3), 2 if op % 2 else 1, 1)
         assert n >= 256 and n % 256 == 0
 
@@ -209,7 +239,8 @@ def test_parity_tables_match_pages(lib, name, L, s, p, d):
 def test_plans_of_workloads(lib):
     """Structural facts of the five workloads' plans."""
     from transposed_conv_epilogues_gb300.workloads import BY_NAME
-    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3}
+    ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3,
+           "convT_bneval_avgpool": 4}
 
     def plan(n):
         wl = BY_NAME[n]

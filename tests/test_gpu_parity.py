@@ -161,6 +161,56 @@ def test_convT_bn_avgpool_small(tc, case):
     check(y, orc.convT_bn_avgpool(x, w, b, g, be, 1e-5, s, p, d, op, G), f"bn-pool {case}")
 
 
+def _running_stats(cout, seed):
+    # running statistics of the scale the BN input has (|t| ~ 0.5): means
+    # around 0, variances in [0.05, 0.5] so the normalisation amplifies
+    rm = 0.2 * inputs.normal(seed, (cout,))
+    rv = inputs.uniform(seed + 1, (cout,), 0.05, 0.5)
+    return rm, rv
+
+
+@pytest.mark.parametrize("case", BN_CASES)
+def test_convT_bneval_avgpool_small(tc, case):
+    """Evaluation-mode BatchNorm (running statistics): the fused cases store
+    final values from the engine, the others pool the workspace output."""
+    xs, ws, s, p, d, op, G, affine = case
+    cout = ws[1] * G
+    x, w, b = make(xs, ws, cout, True, seed=13)
+    rm, rv = _running_stats(cout, 77)
+    g = inputs.uniform(99, (cout,), 0.5, 1.5) if affine else None
+    be = inputs.uniform(98, (cout,), -0.5, 0.5) if affine else None
+    y = tc.convT_bneval_avgpool(_dev(x), _dev(w), _dev(b), _dev(rm), _dev(rv), _dev(g), _dev(be),
+                                1e-5, s, p, d, op, G).cpu().numpy()
+    check(y, orc.convT_bneval_avgpool(x, w, b, rm, rv, g, be, 1e-5, s, p, d, op, G),
+          f"bn-eval-pool {case}")
+
+
+def test_convT_bneval_matches_train_with_batch_stats(tc):
+    """With the batch moments passed as running statistics, evaluation mode
+    gives the training-mode result (both against the oracle, and each other)."""
+    x, w, b = make((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 16, True, seed=21)
+    full = orc.conv_transpose3d(x, w, b, 2, 1)
+    # float32, as the library takes them (rounding moves the result ~1e-7)
+    rm = full.mean(axis=(0, 2, 3, 4)).astype(np.float32)
+    rv = full.var(axis=(0, 2, 3, 4)).astype(np.float32)
+    ev = tc.convT_bneval_avgpool(_dev(x), _dev(w), _dev(b), _dev(rm), _dev(rv), None, None,
+                                 1e-5, 2, 1).cpu().numpy()
+    tr = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), None, None, 1e-5, 2, 1).cpu().numpy()
+    ref = orc.convT_bn_avgpool(x, w, b, None, None, 1e-5, 2, 1)
+    check(ev, ref, "eval with batch stats")
+    check(tr, ref, "train")
+
+
+def test_convT_bneval_rejects_missing_stats(tc):
+    x, w, b = make((1, 3, 6, 6, 6), (3, 4, 3, 3, 3), 4)
+    with pytest.raises(ValueError):
+        tc.convT_bneval_avgpool(_dev(x), _dev(w), _dev(b), None, None, stride=2, padding=1)
+    rm, rv = _running_stats(4, 5)
+    with pytest.raises(ValueError):  # wrong length: checked before the C call
+        tc.convT_bneval_avgpool(_dev(x), _dev(w), _dev(b), _dev(rm[:3]), _dev(rv), stride=2,
+                                padding=1)
+
+
 def test_uniform01_inputs(tc):
     """torch.rand-style inputs (all positive) as on the pages."""
     x, w, b = make((2, 6, 9, 8, 12), (8, 6, 3, 3, 3), 8, True, seed=31, xdist="uniform01")
@@ -226,16 +276,21 @@ def test_cuda_graph_capture_replays(tc):
     calls.append((tc.OP_CONV_MAXPOOL_LSE_RELU, (_dev(x), _dev(w), _dev(b)), dict(stride=1, padding=1)))
     x, w, b = make((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 16)
     calls.append((tc.OP_CONVT_BN_AVGPOOL, (_dev(x), _dev(w), _dev(b)), dict(stride=2, padding=1)))
+    rm, rv = _running_stats(16, 3)
+    calls.append((tc.OP_CONVT_BNEVAL_AVGPOOL, (_dev(x), _dev(w), _dev(b)),
+                  dict(running_mean=_dev(rm), running_var=_dev(rv), stride=2, padding=1)))
     fns = {tc.OP_CONV3D: tc.conv3d_fwd, tc.OP_CONV_TRANSPOSE3D: tc.conv_transpose3d_fwd,
            tc.OP_CONV_MAXPOOL_LSE_RELU: tc.conv_maxpool_lse_relu,
-           tc.OP_CONVT_BN_AVGPOOL: tc.convT_bn_avgpool}
+           tc.OP_CONVT_BN_AVGPOOL: tc.convT_bn_avgpool,
+           tc.OP_CONVT_BNEVAL_AVGPOOL: tc.convT_bneval_avgpool}
     side = torch.cuda.Stream()
     for op, (xd, wd, bd), kw in calls:
         fn = fns[op]
         ref = fn(xd, wd, bd, **kw)  # direct call (also initialises the device state)
         torch.cuda.synchronize()
-        ws = torch.empty(max(tc.workspace_bytes(op, tuple(xd.shape), tuple(wd.shape), **kw), 256),
-                         dtype=torch.uint8, device="cuda")
+        geo = {k: v for k, v in kw.items() if k not in ("running_mean", "running_var")}
+        ws = torch.empty(max(tc.workspace_bytes(op, tuple(xd.shape), tuple(wd.shape), **geo),
+                             256), dtype=torch.uint8, device="cuda")
         y = torch.full_like(ref, float("nan"))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
@@ -322,6 +377,22 @@ def test_workload_convT_bn_avgpool_sampled(tc):
     # BatchNorm with gamma 1, beta 0: each channel of the pooled output has
     # mean ~ 0 (pooling averages whole windows of the normalised tensor)
     assert np.all(np.abs(y.mean(axis=(0, 2, 3, 4))) < 0.05)
+
+
+def test_workload_convT_bneval_avgpool_sampled(tc):
+    """The transposed-conv + BN + pool workload in evaluation mode."""
+    wl, x, w, b = _wl("convT_bn_avgpool")
+    rm, rv = _running_stats(16, 505)
+    g = inputs.uniform(506, (16,), 0.5, 1.5)
+    be = inputs.uniform(507, (16,), -0.5, 0.5)
+    y = tc.convT_bneval_avgpool(_dev(x), _dev(w), _dev(b), _dev(rm), _dev(rv), _dev(g), _dev(be),
+                                wl.eps, **wl.kwargs()).cpu().numpy()
+    assert y.shape == (64, 16, 15, 15, 15)
+    flat = y.ravel()
+    idx = inputs.sample_indices(505, flat.size, 20000)
+    idx = np.concatenate([idx, [0, flat.size - 1]])
+    ref = orc.convT_bneval_avgpool_at(x, w, b, rm, rv, idx, g, be, wl.eps, **wl.kwargs())
+    check(flat[idx], ref, wl.name + " eval")
 
 
 def test_workload_conv_maxpool_lse_relu_sampled(tc):

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI, without the ``tc3d_`` prefix):
 * ``conv_maxpool_lse_relu(x, w, bias, stride, padding, dilation, groups)``
 * ``convT_bn_avgpool(x, w, bias, gamma, beta, eps, stride, padding, dilation,
   output_padding, groups)``
+* ``convT_bneval_avgpool(x, w, bias, running_mean, running_var, gamma, beta, eps,
+  stride, padding, dilation, output_padding, groups)``
 
 Host-only queries: ``out_shape``, ``workspace_bytes``, ``plan_describe``,
 ``status_string``; device diagnostics: ``last_device_error``,
@@ -30,6 +32,7 @@ OP_CONV3D = 0
 OP_CONV_TRANSPOSE3D = 1
 OP_CONV_MAXPOOL_LSE_RELU = 2
 OP_CONVT_BN_AVGPOOL = 3
+OP_CONVT_BNEVAL_AVGPOOL = 4
 
 TC3D_OK = 0
 TC3D_ERR_NULL = -1
@@ -47,7 +50,7 @@ EXPORTED = [
     "tc3d_conv3d_fwd", "tc3d_conv_transpose3d_fwd", "tc3d_conv_maxpool_lse_relu",
     "tc3d_convT_bn_avgpool", "tc3d_workspace_bytes", "tc3d_out_shape", "tc3d_plan_describe",
     "tc3d_last_device_error", "tc3d_set_wait_timeout_ns", "tc3d_selftest_wait_timeout",
-    "tc3d_status_string", "tc3d_conv_maxpool_lse_relu_noalloc",
+    "tc3d_status_string", "tc3d_conv_maxpool_lse_relu_noalloc", "tc3d_convT_bneval_avgpool",
 ]
 
 _lib = None
@@ -83,6 +86,8 @@ def load(path: str | Path | None = None):
     lib.tc3d_conv_maxpool_lse_relu_noalloc.restype = _I
     lib.tc3d_convT_bn_avgpool.argtypes = [_P, _P, _P, _P, _P, ctypes.c_float, _P] + geom + tail
     lib.tc3d_convT_bn_avgpool.restype = _I
+    lib.tc3d_convT_bneval_avgpool.argtypes = ([_P] * 7 + [ctypes.c_float, _P]) + geom + tail
+    lib.tc3d_convT_bneval_avgpool.restype = _I
     lib.tc3d_workspace_bytes.argtypes = [_I] + geom + [ctypes.POINTER(ctypes.c_size_t)]
     lib.tc3d_workspace_bytes.restype = _I
     lib.tc3d_out_shape.argtypes = [_I] + geom + [ctypes.POINTER(ctypes.c_int64)]
@@ -126,7 +131,7 @@ def _geom(x_shape, w_shape, transposed, stride, padding, dilation, output_paddin
 
 
 def _is_transposed(op):
-    return op in (OP_CONV_TRANSPOSE3D, OP_CONVT_BN_AVGPOOL)
+    return op in (OP_CONV_TRANSPOSE3D, OP_CONVT_BN_AVGPOOL, OP_CONVT_BNEVAL_AVGPOOL)
 
 
 def out_shape(op, x_shape, w_shape, stride=1, padding=0, dilation=1, output_padding=0, groups=1):
@@ -243,14 +248,25 @@ def _run(op, x, w, bias, stride, padding, dilation, output_padding, groups, out,
             rc = lib.tc3d_conv_maxpool_lse_relu(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), *g,
                                                 *tail)
         else:
-            gamma, beta, eps = extra
-            _check_tensor(gamma, "gamma", dev)
-            _check_tensor(beta, "beta", dev)
-            rc = lib.tc3d_convT_bn_avgpool(_ptr(x), _ptr(w), _ptr(bias), _ptr(gamma), _ptr(beta),
-                                           ctypes.c_float(eps), _ptr(out), *g, *tail)
+            gamma, beta, eps, rmean, rvar = extra
+            for t, n in ((gamma, "gamma"), (beta, "beta"), (rmean, "running_mean"),
+                         (rvar, "running_var")):
+                _check_tensor(t, n, dev)
+                if t is not None and t.numel() != shp[1]:
+                    raise ValueError(f"{n} has {t.numel()} elements, expected {shp[1]}")
+            if op == OP_CONVT_BN_AVGPOOL:
+                rc = lib.tc3d_convT_bn_avgpool(_ptr(x), _ptr(w), _ptr(bias), _ptr(gamma),
+                                               _ptr(beta), ctypes.c_float(eps), _ptr(out), *g,
+                                               *tail)
+            else:
+                if rmean is None or rvar is None:
+                    raise ValueError("running_mean and running_var are required")
+                rc = lib.tc3d_convT_bneval_avgpool(_ptr(x), _ptr(w), _ptr(bias), _ptr(rmean),
+                                                   _ptr(rvar), _ptr(gamma), _ptr(beta),
+                                                   ctypes.c_float(eps), _ptr(out), *g, *tail)
     if rc:
         raise Tc3dError(rc, ["conv3d_fwd", "conv_transpose3d_fwd", "conv_maxpool_lse_relu",
-                             "convT_bn_avgpool"][op])
+                             "convT_bn_avgpool", "convT_bneval_avgpool"][op])
     return out
 
 
@@ -280,7 +296,17 @@ def convT_bn_avgpool(x, w, bias=None, gamma=None, beta=None, eps=1e-5, stride=1,
                      stream=None):
     """ConvTranspose3d -> BatchNorm3d (batch stats) -> AvgPool3d(2) -> AvgPool3d(2)."""
     return _run(OP_CONVT_BN_AVGPOOL, x, w, bias, stride, padding, dilation, output_padding,
-                groups, out, workspace, stream, extra=(gamma, beta, float(eps)))
+                groups, out, workspace, stream, extra=(gamma, beta, float(eps), None, None))
+
+
+def convT_bneval_avgpool(x, w, bias=None, running_mean=None, running_var=None, gamma=None,
+                         beta=None, eps=1e-5, stride=1, padding=0, dilation=1, output_padding=0,
+                         groups=1, out=None, workspace=None, stream=None):
+    """ConvTranspose3d -> BatchNorm3d (running stats, evaluation mode) -> AvgPool3d(2)
+    -> AvgPool3d(2).  running_mean / running_var are read, never updated."""
+    return _run(OP_CONVT_BNEVAL_AVGPOOL, x, w, bias, stride, padding, dilation, output_padding,
+                groups, out, workspace, stream,
+                extra=(gamma, beta, float(eps), running_mean, running_var))
 
 
 def last_device_error(stream=None) -> int:

@@ -286,7 +286,8 @@ int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cud
 }
 
 int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, const float* bias,
-                  float* y, float2* partials, DeviceState* d, cudaStream_t st) {
+                  float* y, float2* partials, DeviceState* d, cudaStream_t st,
+                  const float2* bn_affine = nullptr) {
   if (pl.tiles == 0) return TC3D_OK;
   EngineParams ep;
   fill_params(pl, &ep);
@@ -295,6 +296,7 @@ int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, c
   ep.bias = bias;
   ep.y = y;
   ep.partials = partials;
+  ep.bn_affine = bn_affine;
   ep.err = d->err;
   encode_xmap(pl, x, &ep);
   const unsigned grid = (unsigned)engine_grid(pl, d->sm_count);
@@ -316,18 +318,34 @@ int common_checks(const float* x, const float* w, const float* y, const float* b
   return TC3D_OK;
 }
 
-int run(int op, const float* x, const float* w, const float* bias, const float* gamma,
-        const float* beta, float eps, float* y, int N, int Cin, int S0, int S1, int S2, int Cout,
-        int k0, int k1, int k2, const int stride[3], const int pad[3], const int dil[3],
-        const int out_pad[3], int groups, void* ws, size_t ws_bytes, cudaStream_t st) {
+// BatchNorm arguments of the two BN-pool entry points (running_mean and
+// running_var only for evaluation mode)
+struct BnArgs {
+  const float* gamma = nullptr;
+  const float* beta = nullptr;
+  const float* rmean = nullptr;
+  const float* rvar = nullptr;
+  float eps = 0.f;
+};
+
+int run(int op, const float* x, const float* w, const float* bias, const BnArgs& bn, float* y,
+        int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+        const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
+        int groups, void* ws, size_t ws_bytes, cudaStream_t st) {
   Plan pl;
   int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
                     &pl);
   if (rc) return rc;
-  if (op == OP_CONVT_BN_POOL && !(eps >= 0.0f)) return TC3D_ERR_SHAPE;
+  const float* gamma = bn.gamma;
+  const float* beta = bn.beta;
+  const float eps = bn.eps;
+  if (is_bn_op(op) && !(eps >= 0.0f)) return TC3D_ERR_SHAPE;
+  if (op == OP_CONVT_BN_EVAL && (!bn.rmean || !bn.rvar)) return TC3D_ERR_NULL;
   rc = common_checks(x, w, y, bias, ws, ws_bytes, pl);
   if (rc) return rc;
-  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return TC3D_ERR_ALIGN;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
+      (bn.rmean && !aligned(bn.rmean, 4)) || (bn.rvar && !aligned(bn.rvar, 4)))
+    return TC3D_ERR_ALIGN;
   DeviceState* d = nullptr;
   rc = device_state(&d);
   if (rc) return rc;
@@ -335,7 +353,7 @@ int run(int op, const float* x, const float* w, const float* bias, const float* 
   float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
   rc = launch_pack(pl, w, wpack, d->sm_count, st);
   if (rc) return rc;
-  if (op != OP_CONVT_BN_POOL) {
+  if (!is_bn_op(op)) {
     if (!pl.fill_slab) return launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
     // The slab fill writes only outputs the engine does not, so it runs beside
     // the engine on the auxiliary stream: fork after the work queued so far
@@ -357,6 +375,24 @@ int run(int op, const float* x, const float* w, const float* bias, const float* 
   const long long pvol = (long long)pl.P[0] * pl.P[1] * pl.P[2];
   const unsigned blocks =
       (unsigned)std::min<long long>((pl.y_elems + 255) / 256, (long long)d->sm_count * 8);
+  if (op == OP_CONVT_BN_EVAL) {
+    // running statistics: the affine map is known before the convolution,
+    // so the fused epilogue stores final values (bias folded into the shift)
+    if (bn_eval_affine_launch(bn.rmean, bn.rvar, gamma, beta, pl.fused ? bias : nullptr, eps,
+                              Cout, stat, st) != cudaSuccess)
+      return TC3D_ERR_CUDA;
+    if (pl.fused) return launch_engine(pl, EPI_BN_POOL, x, wpack, bias, y, nullptr, d, st, stat);
+    float* full = reinterpret_cast<float*>(wsb + pl.ws_full_off);
+    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st);
+    if (rc) return rc;
+    rc = launch_fill(pl, bias, full, d, st);
+    if (rc) return rc;
+    const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
+    const int P[3] = {(int)pl.P[0], (int)pl.P[1], (int)pl.P[2]};
+    return bn_pool4_launch(full, y, N, Cout, O, P, stat, blocks, st) == cudaSuccess
+               ? TC3D_OK
+               : TC3D_ERR_CUDA;
+  }
   if (pl.fused) {
     float2* part = reinterpret_cast<float2*>(wsb + pl.ws_part_off);
     rc = launch_engine(pl, EPI_BN_POOL, x, wpack, bias, y, part, d, st);
@@ -480,7 +516,7 @@ int tc3d_conv3d_fwd(const float* x, const float* w, const float* bias, float* y,
                     int S0, int S1, int S2, int Cout, int k0, int k1, int k2, const int stride[3],
                     const int pad[3], const int dilation[3], const int output_padding[3],
                     int groups, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return run(OP_CONV, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout, k0, k1, k2,
+  return run(OP_CONV, x, w, bias, BnArgs(), y, N, Cin, S0, S1, S2, Cout, k0, k1, k2,
              stride, pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
 }
 
@@ -489,7 +525,7 @@ int tc3d_conv_transpose3d_fwd(const float* x, const float* w, const float* bias,
                               const int stride[3], const int pad[3], const int dilation[3],
                               const int output_padding[3], int groups, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream) {
-  return run(OP_CONVT, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout, k0, k1,
+  return run(OP_CONVT, x, w, bias, BnArgs(), y, N, Cin, S0, S1, S2, Cout, k0, k1,
              k2, stride, pad, dilation, output_padding, groups, workspace, workspace_bytes,
              stream);
 }
@@ -499,7 +535,7 @@ int tc3d_conv_maxpool_lse_relu(const float* x, const float* w, const float* bias
                                const int stride[3], const int pad[3], const int dilation[3],
                                const int output_padding[3], int groups, void* workspace,
                                size_t workspace_bytes, cudaStream_t stream) {
-  return run(OP_CONV_POOL_LSE, x, w, bias, nullptr, nullptr, 0.f, y, N, Cin, S0, S1, S2, Cout,
+  return run(OP_CONV_POOL_LSE, x, w, bias, BnArgs(), y, N, Cin, S0, S1, S2, Cout,
              k0, k1, k2, stride, pad, dilation, output_padding, groups, workspace,
              workspace_bytes, stream);
 }
@@ -510,9 +546,29 @@ int tc3d_convT_bn_avgpool(const float* x, const float* w, const float* bias, con
                           const int pad[3], const int dilation[3], const int output_padding[3],
                           int groups, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream) {
-  return run(OP_CONVT_BN_POOL, x, w, bias, gamma, beta, eps, y, N, Cin, S0, S1, S2, Cout, k0, k1,
-             k2, stride, pad, dilation, output_padding, groups, workspace, workspace_bytes,
-             stream);
+  BnArgs bn;
+  bn.gamma = gamma;
+  bn.beta = beta;
+  bn.eps = eps;
+  return run(OP_CONVT_BN_POOL, x, w, bias, bn, y, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride,
+             pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
+}
+
+int tc3d_convT_bneval_avgpool(const float* x, const float* w, const float* bias,
+                              const float* running_mean, const float* running_var,
+                              const float* gamma, const float* beta, float eps, float* y, int N,
+                              int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                              const int stride[3], const int pad[3], const int dilation[3],
+                              const int output_padding[3], int groups, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  BnArgs bn;
+  bn.gamma = gamma;
+  bn.beta = beta;
+  bn.rmean = running_mean;
+  bn.rvar = running_var;
+  bn.eps = eps;
+  return run(OP_CONVT_BN_EVAL, x, w, bias, bn, y, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride,
+             pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
 }
 
 int tc3d_workspace_bytes(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,

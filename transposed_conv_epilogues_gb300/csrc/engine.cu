@@ -140,6 +140,42 @@ __device__ __forceinline__ int scatter8_index(int lane) {
 
 // Sum 8 values over the 8 lanes of a 2x2x2 pool window (lane bits 0, 3, 4);
 // lane ends with the total of value index 4*b0 + 2*b3 + b4.
+// BN-pool class sums of one row for 8 channels.  u holds, per channel h,
+// the 8 parity classes r = 4 r0 + 2 r1 + r2 of the row.  Class r lies inside
+// the output iff 2m + r < O on every axis; a row inside M has 2m < O, so
+// class r is in iff f_i = [2 m_i + 1 < O_i] holds on every axis with r_i = 1.
+// Its weight is f0^r0 f1^r1 f2^r2, and the sums nest as a tree of FMAs over
+// those 0/1 weights.  ps[h]: the row's sum (a row whose 4x4x4 window is
+// stored has every class inside, so this is then the plain sum of the 8);
+// with STATS, the sums and sums of squares also run into s1/s2 with the
+// row's weight fr (0 for rows past M).
+template <bool STATS>
+__device__ __forceinline__ void bn_class_sums(const uint32_t (&u)[64], int nch, float f0, float f1,
+                                              float f2, float fr, float (&ps)[8], float (&s1)[8],
+                                              float (&s2)[8]) {
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    ps[h] = 0.f;
+    if (h >= 4 && nch <= 4) continue;
+    float a[4], c[4];  // per (r0, r1): classes r2 = 0, 1 combined
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float ve = __uint_as_float(u[h * 8 + 2 * k]);
+      const float vo = __uint_as_float(u[h * 8 + 2 * k + 1]);
+      const float w = f2 * vo;
+      a[k] = ve + w;
+      if (STATS) c[k] = fmaf(w, vo, ve * ve);
+    }
+    const float sum = fmaf(f0, fmaf(f1, a[3], a[2]), fmaf(f1, a[1], a[0]));
+    ps[h] = sum;
+    if (STATS) {
+      const float sq = fmaf(f0, fmaf(f1, c[3], c[2]), fmaf(f1, c[1], c[0]));
+      s1[h] = fmaf(fr, sum, s1[h]);
+      s2[h] = fmaf(fr, sq, s2[h]);
+    }
+  }
+}
+
 __device__ __forceinline__ float reduce_scatter8_window_sum(const float (&v)[8], int lane) {
   float w4[4], w2[2];
   const bool b0 = lane & 1, b3 = lane & 8, b4 = lane & 16;
@@ -836,6 +872,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       s1[i] = 0.f;
       s2[i] = 0.f;
     }
+    // running statistics: the affine map is known, no partial sums
+    const bool bn_eval = EPI == EPI_BN_POOL && p.bn_affine != nullptr;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
       // pool-LSE running state per accumulator (channels this lane holds)
@@ -1136,12 +1174,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols + 8 * ch0);
             int mm[3];
             const bool rv = row_global(p, tc.o, a, q, lane, mm);
-            // Class r = 4 r0 + 2 r1 + r2 lies inside the output iff 2m + r < O
-            // on every axis.  A row inside M always has 2m < O, so class r is
-            // in iff f_i = [2 m_i + 1 < O_i] holds on every axis with r_i = 1:
-            // its weight is f0^r0 f1^r1 f2^r2, and the class sums below nest
-            // as a tree of FMAs over those 0/1 weights.  Rows past M drop out
-            // through the weight fr of their running sums.
+            // class weights of this row (see bn_class_sums)
             const float f0 = 2 * mm[0] + 1 < p.O[0] ? 1.f : 0.f;
             const float f1 = 2 * mm[1] + 1 < p.O[1] ? 1.f : 0.f;
             const float f2 = 2 * mm[2] + 1 < p.O[2] ? 1.f : 0.f;
@@ -1151,40 +1184,28 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             if (nch > 4) tmem_ld32(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
             tmem_wait_ld();
             float ps[8];
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-              ps[h] = 0.f;
-              if (h >= 4 && nch <= 4) continue;
-              float a[4], c[4];  // per (r0, r1): classes r2 = 0, 1 combined
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float ve = __uint_as_float(u[h * 8 + 2 * k]);
-                const float vo = __uint_as_float(u[h * 8 + 2 * k + 1]);
-                const float w = f2 * vo;
-                a[k] = ve + w;
-                c[k] = fmaf(w, vo, ve * ve);
-              }
-              const float sum = fmaf(f0, fmaf(f1, a[3], a[2]), fmaf(f1, a[1], a[0]));
-              const float sq = fmaf(f0, fmaf(f1, c[3], c[2]), fmaf(f1, c[1], c[0]));
-              // a row whose window is stored has every class inside the
-              // output (its window index is below P on every axis), so this
-              // is then the plain sum over the 8 classes
-              ps[h] = sum;
-              s1[h] = fmaf(fr, sum, s1[h]);
-              s2[h] = fmaf(fr, sq, s2[h]);
-            }
+            if (bn_eval)
+              bn_class_sums<false>(u, nch, f0, f1, f2, fr, ps, s1, s2);
+            else
+              bn_class_sums<true>(u, nch, f0, f1, f2, fr, ps, s1, s2);
             // pooled sums over the 8 rows of each 4x4x4 window
             const float pw = reduce_scatter8_window_sum(ps, lane);
             const int w0 = mm[0] >> 1, w1 = mm[1] >> 1, w2 = mm[2] >> 1;
             const int oc_l = ch0 + window8_index(lane);
             if (w0 < p.P[0] && w1 < p.P[1] && w2 < p.P[2] && oc_l < ocb_valid) {
               const int oc = oc0 + oc_l;
-              const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+              float v;
+              if (bn_eval) {
+                const float2 ab = __ldg(p.bn_affine + oc);
+                v = fmaf(pw * (1.0f / 64.0f), ab.x, ab.y);
+              } else {
+                v = pw * (1.0f / 64.0f) + (p.bias ? __ldg(p.bias + oc) : 0.f);
+              }
               p.y[(((long long)tc.n * p.Cout + oc) * p.P[0] + w0) * p.P[1] * p.P[2] +
-                  (long long)w1 * p.P[2] + w2] = pw * (1.0f / 64.0f) + b;
+                  (long long)w1 * p.P[2] + w2] = v;
             }
           }
-          if (p.n_colblocks > 1) {
+          if (p.n_colblocks > 1 && !bn_eval) {
             // BatchNorm partial sums of this tile: all lanes, then the 4
             // quarters of both groups
             const float t1 = reduce_scatter8_sum(s1, lane);
@@ -1224,7 +1245,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       }
     }
     if constexpr (EPI == EPI_BN_POOL) {
-      if (ok && p.n_colblocks == 1) {
+      if (ok && p.n_colblocks == 1 && !bn_eval) {
         // slot: CTA-major, then lane quarter; each channel's slots are all
         // written by the 4 warps of the group that takes it
         const float t1 = reduce_scatter8_sum(s1, lane);
@@ -1397,6 +1418,18 @@ __global__ void bn_apply_kernel(float* y, long long n, long long inner, int Cout
   }
 }
 
+// running statistics (evaluation mode): per channel scale and shift
+__global__ void bn_eval_affine_kernel(const float* rmean, const float* rvar, const float* gamma,
+                                      const float* beta, const float* bias, float eps, int Cout,
+                                      float2* stat) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= Cout) return;
+  const double g = gamma ? (double)gamma[c] : 1.0, be = beta ? (double)beta[c] : 0.0;
+  const double b = bias ? (double)bias[c] : 0.0;
+  const double scale = g / sqrt((double)rvar[c] + (double)eps);
+  stat[c] = make_float2((float)scale, (float)(be + (b - (double)rmean[c]) * scale));
+}
+
 // unfused path: y = scale * mean of the 4x4x4 window + shift
 __global__ void bn_pool4_kernel(const float* t, float* y, int N, int Cout, int O0, int O1, int O2,
                                 int P0, int P1, int P2, const float2* stat) {
@@ -1523,6 +1556,22 @@ cudaError_t bn_stats_f2_launch(const float2* part, int nparts, const float* bias
 cudaError_t bn_apply_launch(float* y, long long n, long long inner, int Cout, const float2* stat,
                             unsigned blocks, cudaStream_t st) {
   bn_apply_kernel<<<blocks, 256, 0, st>>>(y, n, inner, Cout, stat);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_eval_affine_launch(const float* rmean, const float* rvar, const float* gamma,
+                                  const float* beta, const float* bias, float eps, int Cout,
+                                  float2* stat, cudaStream_t st) {
+  bn_eval_affine_kernel<<<(unsigned)((Cout + 127) / 128), 128, 0, st>>>(rmean, rvar, gamma, beta,
+                                                                        bias, eps, Cout, stat);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_pool4_launch(const float* full, float* y, int N, int Cout, const int O[3],
+                            const int P[3], const float2* stat, unsigned blocks,
+                            cudaStream_t st) {
+  bn_pool4_kernel<<<blocks, 256, 0, st>>>(full, y, N, Cout, O[0], O[1], O[2], P[0], P[1], P[2],
+                                          stat);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,11 @@ struct EngineParams {
 
   // dynamic shared-memory layout (offsets from the 1024-aligned base)
   unsigned sm_raw, sm_b, sm_xs, sm_ktab, sm_misc, sm_bar;
+
+  // BN-pool with running statistics: per channel (scale, shift), the bias
+  // folded into shift; the epilogue then stores final values and no partial
+  // sums.  nullptr: batch statistics.
+  const float2* bn_affine;
 };
 
 struct PackParams {
@@ -144,6 +149,14 @@ cudaError_t bn_stats_f2_launch(const float2* part, int nparts, const float* bias
                                int Cout, float2* stat, cudaStream_t st);
 cudaError_t bn_apply_launch(float* y, long long n, long long inner, int Cout, const float2* stat,
                             unsigned blocks, cudaStream_t st);
+// running statistics: stat[c] = (scale, shift) with scale = gamma/sqrt(var +
+// eps), shift = beta + (bias - mean) * scale (bias may be nullptr)
+cudaError_t bn_eval_affine_launch(const float* rmean, const float* rvar, const float* gamma,
+                                  const float* beta, const float* bias, float eps, int Cout,
+                                  float2* stat, cudaStream_t st);
+// unfused pooling: y = mean of each 4x4x4 window of full * scale + shift
+cudaError_t bn_pool4_launch(const float* full, float* y, int N, int Cout, const int O[3],
+                            const int P[3], const float2* stat, unsigned blocks, cudaStream_t st);
 cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N, int Cout,
                               const int O[3], const int P[3], const float* gamma,
                               const float* beta, float eps, float2* stat, unsigned blocks,

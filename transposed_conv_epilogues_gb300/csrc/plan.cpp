@@ -107,7 +107,7 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
   std::memset(&pl, 0, sizeof(pl));
   pl.pb = pb_in;
   const Problem& pb = pl.pb;
-  const bool transposed = pb.op == OP_CONVT || pb.op == OP_CONVT_BN_POOL;
+  const bool transposed = pb.op == OP_CONVT || is_bn_op(pb.op);
   pl.transposed = transposed;
   pl.status = TC3D_OK;
   auto fail = [&](int st) {
@@ -115,7 +115,7 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     *out = pl;
     return st;
   };
-  if (pb.op < OP_CONV || pb.op > OP_CONVT_BN_POOL) return fail(TC3D_ERR_UNSUPPORTED);
+  if (pb.op < OP_CONV || pb.op > OP_CONVT_BN_EVAL) return fail(TC3D_ERR_UNSUPPORTED);
   int st = validate(pb, transposed);
   if (st) return fail(st);
   pl.cin_g = pb.Cin / pb.groups;
@@ -219,7 +219,7 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     }
   }
   pl.nR = pl.nRaxis[0] * pl.nRaxis[1] * pl.nRaxis[2];
-  if (pb.op == OP_CONVT_BN_POOL) {
+  if (is_bn_op(pb.op)) {
     // fused BatchNorm + 4x4x4 pooling: a row is a 2x2x2 output block with all
     // 8 parity classes carrying taps, so a 4^3 window is 2x2x2 rows
     pl.fused = pb.stride[0] == 2 && pb.stride[1] == 2 && pb.stride[2] == 2 && pl.nR == 8;
@@ -469,11 +469,13 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     pl.ws_wpack_off = off;
     pl.ws_wpack_bytes = (int64_t)pl.n_colblocks * pl.n_chunks * pl.ksteps_chunk * 64 * pl.n_tile;
     off = round_up(off + pl.ws_wpack_bytes, 256);
-    if (pb.op == OP_CONVT_BN_POOL) {
+    if (is_bn_op(pb.op)) {
       pl.ws_part_off = off;
-      // fused: enough slots for any grid; unfused: per (n, c) double sums
+      // batch statistics: fused, enough slots for any grid; unfused, per
+      // (n, c) double sums.  Running statistics need no partial sums.
       const int64_t slots = bn_part_slots(pl, std::min<int64_t>(pl.tiles, kMaxGrid));
-      pl.ws_part_bytes = pl.fused ? slots * pb.Cout * 8 : (int64_t)pb.N * pb.Cout * 16;
+      if (pb.op == OP_CONVT_BN_POOL)
+        pl.ws_part_bytes = pl.fused ? slots * pb.Cout * 8 : (int64_t)pb.N * pb.Cout * 16;
       off = round_up(off + pl.ws_part_bytes, 256);
       pl.ws_stat_off = off;
       pl.ws_stat_bytes = (int64_t)pb.Cout * 8;

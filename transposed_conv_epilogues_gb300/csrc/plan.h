@@ -13,13 +13,17 @@ enum OpKind : int {
   OP_CONV = 0,             // conv3d_fwd
   OP_CONVT = 1,            // conv_transpose3d_fwd
   OP_CONV_POOL_LSE = 2,    // conv_maxpool_lse_relu
-  OP_CONVT_BN_POOL = 3,    // convT_bn_avgpool
+  OP_CONVT_BN_POOL = 3,    // convT_bn_avgpool (batch statistics)
+  OP_CONVT_BN_EVAL = 4,    // convT_bneval_avgpool (running statistics)
 };
+
+inline bool is_bn_op(int op) { return op == OP_CONVT_BN_POOL || op == OP_CONVT_BN_EVAL; }
 
 enum EpiKind : int {
   EPI_STORE = 0,     // bias add + store every output (all parity classes)
   EPI_POOL_LSE = 1,  // MaxPool3d(2) + channel logsumexp + ReLU
-  EPI_BN_POOL = 2,   // 4x4x4 pooled sums + per-tile BatchNorm partial sums
+  EPI_BN_POOL = 2,   // 4x4x4 pooled sums + per-tile BatchNorm partial sums, or,
+                     // with the BatchNorm affine known up front, the final values
 };
 
 constexpr int kMaxAxisTaps = 16;    // per-axis kernel extent limit
@@ -105,7 +109,8 @@ struct Plan {
 
   // workspace (bytes, each region 256-aligned)
   int64_t ws_wpack_off, ws_wpack_bytes;
-  int64_t ws_part_off, ws_part_bytes;   // BN partials: fused [Cout][slots] float2, else [N][Cout] double2
+  int64_t ws_part_off, ws_part_bytes;   // BN partials (batch statistics only): fused
+                                        // [Cout][slots] float2, else [N][Cout] double2
   int64_t ws_stat_off, ws_stat_bytes;   // BN scale/shift [Cout] float2
   int64_t ws_full_off, ws_full_bytes;   // unfused fallback: full convT output
   int64_t ws_total;

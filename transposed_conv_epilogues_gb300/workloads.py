@@ -1,4 +1,4 @@
-"""The five benchmark / parity workloads and two second workloads, with
+"""The five benchmark / parity workloads and three second workloads, with
 their synthetic input recipes.
 
 Shapes follow the four POPCORNBENCH transcript pages:
@@ -37,7 +37,8 @@ from . import inputs
 class Workload:
     index: int
     name: str
-    op: str  # "conv3d" | "conv_transpose3d" | "convT_bn_avgpool" | "conv_maxpool_lse_relu"
+    op: str  # "conv3d" | "conv_transpose3d" | "convT_bn_avgpool" | "convT_bneval_avgpool"
+    #          | "conv_maxpool_lse_relu"
     x_shape: tuple
     w_shape: tuple
     bias: bool
@@ -52,7 +53,7 @@ class Workload:
 
     @property
     def transposed(self) -> bool:
-        return self.op in ("conv_transpose3d", "convT_bn_avgpool")
+        return self.op in ("conv_transpose3d", "convT_bn_avgpool", "convT_bneval_avgpool")
 
     @property
     def cout(self) -> int:
@@ -69,6 +70,18 @@ class Workload:
         w = inputs.uniform(1000 * i + 2, self.w_shape, -bound, bound)
         b = inputs.uniform(1000 * i + 3, (self.cout,), -bound, bound) if self.bias else None
         return x, w, b
+
+    def make_bn_eval_params(self):
+        """(running_mean, running_var, gamma, beta) float32 [Cout] arrays of
+        the evaluation-mode BatchNorm: means ~ 0.2 N(0,1), variances
+        ~ U(0.05, 0.5) (the scale of the transposed-conv output), gamma
+        ~ U(0.5, 1.5), beta ~ U(-0.5, 0.5); seeds 1000*i+4 .. 1000*i+7."""
+        i, c = self.index, self.cout
+        rm = (0.2 * inputs.normal(1000 * i + 4, (c,))).astype(np.float32)
+        rv = inputs.uniform(1000 * i + 5, (c,), 0.05, 0.5)
+        g = inputs.uniform(1000 * i + 6, (c,), 0.5, 1.5)
+        be = inputs.uniform(1000 * i + 7, (c,), -0.5, 0.5)
+        return rm, rv, g, be
 
     def kwargs(self) -> dict:
         kw = dict(stride=self.stride, padding=self.padding, dilation=self.dilation,
@@ -98,7 +111,10 @@ WORKLOADS = [
 # the shape "Kimi-K2.6 l1_p59" itself uses (Cin 3, Cout 64, a [16,3,256,256,10]
 # input; its 2.6 GB output makes it output-write-bound), and the k3 s2 p1 d2
 # transposed conv of "Kimi-K2.6 l1_p77" at a larger input channel count (Cin
-# 128), which makes the GEMM K 3456.  Seeds follow the same rule (i = 6, 7).
+# 128), which makes the GEMM K 3456, and the transposed-conv + BN + pool
+# pipeline of "Kimi-K2.6 l2_p72" with BatchNorm in evaluation mode (running
+# statistics, as that page's first fused kernel reads them) at the same shape.
+# Seeds follow the same rule (i = 6, 7, 8).
 EXTRA_WORKLOADS = [
     Workload(6, "conv331_p1", "conv3d", (16, 3, 256, 256, 10), (64, 3, 3, 3, 1), True,
              fan_in=3 * 9, desc="Conv3d (3,3,1) 3->64 at the page's original shape"),
@@ -106,6 +122,9 @@ EXTRA_WORKLOADS = [
              (128, 64, 3, 3, 3), False, stride=(2, 2, 2), padding=(1, 1, 1),
              dilation=(2, 2, 2), fan_in=128 * 27,
              desc="ConvTranspose3d 128->64 k3 s2 p1 d2"),
+    Workload(8, "convT_bneval_avgpool", "convT_bneval_avgpool", (64, 3, 32, 32, 32),
+             (3, 16, 3, 3, 3), True, stride=(2, 2, 2), padding=(1, 1, 1), fan_in=16 * 27,
+             desc="ConvTranspose3d 3->16 k3 s2 p1 + BN(running stats) + AvgPool3d(2) x2"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
@@ -164,15 +183,18 @@ def y_shape(wl: Workload):
     N = wl.x_shape[0]
     if wl.op == "conv_maxpool_lse_relu":
         return (N, 1) + tuple(o // 2 for o in O)
-    if wl.op == "convT_bn_avgpool":
-        return (N, wl.cout) + tuple(o // 4 for o in O)
+    if wl.op in ("convT_bn_avgpool", "convT_bneval_avgpool"):
+        return (N, wl.cout) + tuple(o // 2 // 2 for o in O)
     return (N, wl.cout) + O
 
 
 def algorithmic_bytes(wl: Workload) -> int:
-    """Read x and the weights (and bias) once, write y once; fused
-    intermediates count zero."""
+    """Read x and the weights (and bias, and the BatchNorm running
+    statistics and affine parameters) once, write y once; fused intermediates
+    count zero."""
     n = int(np.prod(wl.x_shape)) + int(np.prod(wl.w_shape)) + int(np.prod(y_shape(wl)))
     if wl.bias:
         n += wl.cout
+    if wl.op == "convT_bneval_avgpool":
+        n += 4 * wl.cout
     return 4 * n
