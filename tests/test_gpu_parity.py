@@ -139,11 +139,22 @@ def test_conv_maxpool_lse_relu_small(tc, case):
 
 BN_CASES = [
     # x shape, w shape, stride, pad, dil, output_padding, groups, gamma/beta
-    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # fused
+    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # fused (algebraic in eval)
     ((2, 7, 9, 8, 10), (7, 5, 3, 3, 3), 2, 1, 1, (0, 1, 1), 1, True),  # fused, ragged
     ((2, 4, 6, 7, 8), (4, 3, 3, 3, 3), 2, 1, 1, 0, 2, True),          # fused, groups
     ((1, 5, 10, 12, 9), (5, 40, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # fused, 3 column blocks
     ((4, 3, 24, 24, 24), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),     # fused, more tiles than CTAs
+    ((4, 5, 24, 24, 24), (5, 16, 3, 3, 3), 2, 1, 1, 0, 1, True),     # fused, 5 channels, many tiles
+    # the algebraic path (patch Gram statistics + summed-weight pooled conv):
+    # batch statistics where the fused epilogue cannot run (one parity class
+    # per axis); running statistics always (the eval test reuses these)
+    ((2, 3, 8, 7, 9), (3, 4, 1, 1, 1), 2, 0, 1, (1, 0, 1), 1, True),  # k 1
+    ((2, 4, 7, 8, 6), (4, 5, 2, 2, 2), 2, 0, 2, 1, 1, True),          # k 2, dilation 2
+    ((3, 1, 20, 22, 24), (1, 6, 1, 1, 1), 2, 0, 1, 1, 1, False),      # many thin-box units
+    ((2, 2, 9, 7, 10), (2, 4, 3, 3, 3), 2, 0, 1, 0, 1, True),         # pad 0
+    ((1, 4, 5, 6, 7), (4, 3, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # 32-entry patch
+    ((2, 1, 9, 8, 7), (1, 4, 2, 3, 5), 2, (0, 1, 2), (1, 1, 3), 1, 1, True),  # widened pad
+    ((3, 2, 6, 5, 9), (2, 3, 2, 4, 3), 2, (0, 1, 1), 1, (1, 0, 0), 1, False),
     ((2, 3, 9, 5, 6), (3, 4, 3, 3, 3), (1, 2, 2), 1, 1, 0, 1, True),  # unfused: stride 1 axis
     ((2, 3, 6, 6, 6), (3, 4, 3, 3, 3), 2, 1, 2, 0, 1, True),          # unfused: dilation 2
 ]
@@ -183,6 +194,18 @@ def test_convT_bneval_avgpool_small(tc, case):
                                 1e-5, s, p, d, op, G).cpu().numpy()
     check(y, orc.convT_bneval_avgpool(x, w, b, rm, rv, g, be, 1e-5, s, p, d, op, G),
           f"bn-eval-pool {case}")
+
+
+def test_convT_bn_avgpool_gram_path_many_units(tc):
+    """Batch statistics from patch Gram matrices at a size with many work
+    units per box (a one-class-per-axis transposed conv: k 2, dilation 2,
+    a 32-entry patch), every output against the oracle."""
+    x, w, b = make((8, 4, 32, 32, 32), (4, 8, 2, 2, 2), 8, True, seed=61)
+    assert tc.plan_describe(3, x.shape, w.shape, 2, 0, 2)["pool_path"] == 1
+    g = inputs.uniform(62, (8,), 0.5, 1.5)
+    be = inputs.uniform(63, (8,), -0.5, 0.5)
+    y = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), _dev(g), _dev(be), 1e-5, 2, 0, 2)
+    check(y.cpu().numpy(), orc.convT_bn_avgpool(x, w, b, g, be, 1e-5, 2, 0, 2), "gram path")
 
 
 def test_convT_bneval_matches_train_with_batch_stats(tc):

@@ -1,6 +1,6 @@
 """Build libtc3d.so in-tree with nvcc for sm_103a (GB300).
 
-The three translation units compile in parallel, then link into
+The translation units compile in parallel, then link into
 ``transposed_conv_epilogues_gb300/libtc3d.so`` (static CUDA runtime, no -lcuda:
 the tensor-map encoder is fetched through the runtime's driver entry point).
 """
@@ -18,8 +18,8 @@ CSRC = PKG / "csrc"
 BUILD = ROOT / "_build"
 LIB = PKG / "libtc3d.so"
 
-SOURCES = ["engine.cu", "api.cu", "plan.cpp", "noalloc.cu"]
-HEADERS = ["engine.cuh", "plan.h", "ptx.cuh"]
+SOURCES = ["engine.cu", "api.cu", "plan.cpp", "noalloc.cu", "pool.cu"]
+HEADERS = ["engine.cuh", "plan.h", "ptx.cuh", "pool.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -15,6 +15,7 @@
 #include "../../include/tc3d.h"
 #include "engine.cuh"
 #include "plan.h"
+#include "pool.cuh"
 
 using namespace tc3d;
 
@@ -35,6 +36,7 @@ struct DeviceState {
   int sm_count = 0;
   int* err = nullptr;  // device address of the error word
   bool smem_set[4] = {false, false, false, false};  // per kernel id
+  bool gram_smem_set = false;
   // auxiliary stream for the bias slab fill, which runs beside the engine
   // (fork / join through two events; calls that use it are serialised by
   // g_fork_mu while they enqueue)
@@ -84,6 +86,7 @@ Problem make_problem(int op, int N, int Cin, int S0, int S1, int S2, int Cout, i
                      int k2, const int stride[3], const int pad[3], const int dil[3],
                      const int out_pad[3], int groups) {
   Problem pb;
+  std::memset(&pb, 0, sizeof(pb));
   pb.op = op;
   pb.N = N;
   pb.Cin = Cin;
@@ -309,11 +312,11 @@ int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, c
 }
 
 int common_checks(const float* x, const float* w, const float* y, const float* bias,
-                  const void* ws, size_t ws_bytes, const Plan& pl) {
+                  const void* ws, size_t ws_bytes, int64_t ws_total) {
   if (!x || !w || !y) return TC3D_ERR_NULL;
   if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
     return TC3D_ERR_ALIGN;
-  if (!ws || ws_bytes < (size_t)pl.ws_total) return TC3D_ERR_WORKSPACE;
+  if (!ws || ws_bytes < (size_t)ws_total) return TC3D_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return TC3D_ERR_ALIGN;
   return TC3D_OK;
 }
@@ -328,20 +331,169 @@ struct BnArgs {
   float eps = 0.f;
 };
 
+// Plans of one call: the engine plan of the operation and, for the BN-pool
+// ops, the algebraic path when it applies (it then replaces the engine plan's
+// launches and sets the workspace size).
+struct CallPlan {
+  Plan pl;
+  PoolPlan pp;
+  bool pool_ok = false;  // the algebraic path applies
+  bool pool = false;     // and is taken
+  int64_t ws_total = 0;
+};
+
+int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+              const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
+              int groups, CallPlan* cp) {
+  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
+                    &cp->pl);
+  if (rc) return rc;
+  // the algebraic path: always for running statistics; for batch statistics
+  // only where the fused engine epilogue cannot run (its Gram statistics
+  // measured slower than that epilogue on the 64 x 3 x 32^3 workload, and
+  // much faster than the full-output fallback)
+  cp->pool_ok = is_bn_op(op) && make_pool_plan(cp->pl, &cp->pp) == TC3D_OK;
+  cp->pool = cp->pool_ok && (op == OP_CONVT_BN_EVAL || !cp->pl.fused);
+  cp->ws_total = cp->pool ? cp->pp.ws_total : cp->pl.ws_total;
+  return TC3D_OK;
+}
+
+// The algebraic BN-pool path: [Gram matrices, their reduction,] finalize
+// (statistics, folded weights and bias), weight pack, pooled convolution.
+int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const float* bias,
+             const BnArgs& bn, float* y, void* ws, DeviceState* d, cudaStream_t st) {
+  const Plan& pl = cp.pl;
+  const PoolPlan& pp = cp.pp;
+  const Problem& pb = pl.pb;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* wpack = reinterpret_cast<float*>(wsb + pp.ws_wpack_off);
+  float* w2 = reinterpret_cast<float*>(wsb + pp.ws_w2_off);
+  float* b2 = reinterpret_cast<float*>(wsb + pp.ws_b2_off);
+  double* gsum = nullptr;
+  if (op == OP_CONVT_BN_POOL) {
+    GramParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.x = x;
+    gp.part = reinterpret_cast<float*>(wsb + pp.ws_gpart_off);
+    gp.N = pb.N;
+    gp.C = pb.Cin;
+    gp.D = pp.D;
+    gp.V = pp.D / pb.Cin;
+    gp.nb = (pp.D + 7) / 8;
+    gp.nblk = gp.nb * (gp.nb + 1) / 2;
+    for (int a = 0; a < 3; ++a) {
+      gp.L[a] = pb.S[a];
+      gp.nU[a] = pp.nU[a];
+      for (int i = 0; i < kMaxAxisTaps; ++i) gp.U[a][i] = pp.U[a][i];
+    }
+    gp.nbox = pp.nbox;
+    gp.vec16 = aligned(x, 16) && pb.S[2] % 4 == 0;
+    // CTAs per box in proportion to its cost, two per SM in all; each box at
+    // least 8 and never more than its units
+    int64_t cost[kGramMaxBoxes], all = 0;
+    for (int b = 0; b < pp.nbox; ++b) {
+      for (int a = 0; a < 3; ++a) {
+        gp.box_lo[b][a] = pp.box_lo[b][a];
+        gp.box_ext[b][a] = pp.box_hi[b][a] - pp.box_lo[b][a];
+        gp.box_perm[b][a] = pp.box_perm[b][a];
+      }
+      gp.box_Tn[b] = pp.box_Tn[b];
+      gp.box_T1[b] = pp.box_T1[b];
+      gp.box_T2[b] = pp.box_T2[b];
+      gp.box_W1[b] = pp.box_W1[b];
+      gp.box_W2p[b] = pp.box_W2p[b];
+      const int A0 = pp.box_perm[b][0], A1 = pp.box_perm[b][1], A2 = pp.box_perm[b][2];
+      gp.box_nt1[b] = (gp.box_ext[b][A1] + pp.box_T1[b] - 1) / pp.box_T1[b];
+      gp.box_nt2[b] = (gp.box_ext[b][A2] + pp.box_T2[b] - 1) / pp.box_T2[b];
+      gp.box_units[b] = (int64_t)((pb.N + pp.box_Tn[b] - 1) / pp.box_Tn[b]) * gp.box_ext[b][A0] *
+                        gp.box_nt1[b] * gp.box_nt2[b];
+      // rows, plus the unit's staging: a word per staged slab float, a
+      // quarter word where rows move as 16-byte copies
+      const int64_t slab = (int64_t)pp.box_Tn[b] * pb.Cin * pp.nU[A0] * pp.box_W1[b] * pp.box_W2p[b];
+      const int z2s = pp.box_lo[b][2] + pp.U[2][0];
+      const bool v16 = gp.vec16 && A2 == 2 && z2s >= 0 && z2s % 4 == 0 &&
+                       (gp.box_nt2[b] == 1 || pp.box_T2[b] % 4 == 0);
+      cost[b] = pp.box_rows[b] + gp.box_units[b] * (v16 ? slab / 4 : slab);
+      all += cost[b];
+    }
+    // all CTAs resident at once: two per SM, the per-box minimum of 8 included
+    const int64_t budget =
+        std::min<int64_t>(kGramMaxCtas, 2LL * d->sm_count) - 8LL * pp.nbox;
+    gp.box_cta0[0] = 0;
+    for (int b = 0; b < pp.nbox; ++b) {
+      // at least 8 CTAs (or one per unit): thin boxes are latency-bound
+      const int64_t share = std::max<int64_t>(8, budget * cost[b] / std::max<int64_t>(all, 1));
+      gp.box_cta0[b + 1] =
+          gp.box_cta0[b] + (int)std::max<int64_t>(1, std::min<int64_t>(gp.box_units[b], share));
+    }
+    gsum = reinterpret_cast<double*>(wsb + pp.ws_gsum_off);
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (!d->gram_smem_set) {
+        if (gram_set_smem() != cudaSuccess) return TC3D_ERR_CUDA;
+        d->gram_smem_set = true;
+      }
+    }
+    if (gram_launch(gp, (unsigned)gp.box_cta0[pp.nbox], st) != cudaSuccess ||
+        gram_reduce_launch(gp.part, gp.box_cta0, pp.nbox, pp.cls_coef, pp.ncls, gsum, st) !=
+            cudaSuccess)
+      return TC3D_ERR_CUDA;
+  }
+  PoolFinParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.w = w;
+  fp.bias = bias;
+  fp.gamma = bn.gamma;
+  fp.beta = bn.beta;
+  fp.rmean = bn.rmean;
+  fp.rvar = bn.rvar;
+  fp.gcls = gsum;
+  fp.w2 = w2;
+  fp.b2 = b2;
+  fp.eps = bn.eps;
+  fp.count = (double)pb.N * (double)pl.O[0] * (double)pl.O[1] * (double)pl.O[2];
+  fp.Cin = pb.Cin;
+  fp.Cout = pb.Cout;
+  fp.V = pp.D / pb.Cin;
+  for (int a = 0; a < 3; ++a) {
+    fp.k[a] = pb.k[a];
+    fp.pad[a] = pb.pad[a];
+    fp.dil[a] = pb.dil[a];
+    fp.nU[a] = pp.nU[a];
+    fp.e_min[a] = pp.e_min[a];
+    fp.Ke[a] = pp.Ke[a];
+    for (int r = 0; r < 2; ++r) {
+      fp.ntap[a][r] = pp.ntap[a][r];
+      for (int i = 0; i < kMaxAxisTaps; ++i) {
+        fp.tap_k[a][r][i] = pp.tap_k[a][r][i];
+        fp.tap_u[a][r][i] = pp.tap_u[a][r][i];
+      }
+    }
+  }
+  fp.ncls = pp.ncls;
+  for (int c = 0; c < 8; ++c)
+    for (int a = 0; a < 3; ++a) fp.cls_r[c][a] = pp.cls_r[c][a];
+  if (pool_finalize_launch(fp, st) != cudaSuccess) return TC3D_ERR_CUDA;
+  int rc = launch_pack(pp.cplan, w2, wpack, d->sm_count, st);
+  if (rc) return rc;
+  return launch_engine(pp.cplan, pp.cplan.epi, x, wpack, b2, y, nullptr, d, st);
+}
+
 int run(int op, const float* x, const float* w, const float* bias, const BnArgs& bn, float* y,
         int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
         const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
         int groups, void* ws, size_t ws_bytes, cudaStream_t st) {
-  Plan pl;
-  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
-                    &pl);
+  CallPlan cp;
+  int rc = plan_call(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
+                     &cp);
   if (rc) return rc;
+  const Plan& pl = cp.pl;
   const float* gamma = bn.gamma;
   const float* beta = bn.beta;
   const float eps = bn.eps;
   if (is_bn_op(op) && !(eps >= 0.0f)) return TC3D_ERR_SHAPE;
   if (op == OP_CONVT_BN_EVAL && (!bn.rmean || !bn.rvar)) return TC3D_ERR_NULL;
-  rc = common_checks(x, w, y, bias, ws, ws_bytes, pl);
+  rc = common_checks(x, w, y, bias, ws, ws_bytes, cp.ws_total);
   if (rc) return rc;
   if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
       (bn.rmean && !aligned(bn.rmean, 4)) || (bn.rvar && !aligned(bn.rvar, 4)))
@@ -349,6 +501,7 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
   DeviceState* d = nullptr;
   rc = device_state(&d);
   if (rc) return rc;
+  if (cp.pool) return run_pool(op, cp, x, w, bias, bn, y, ws, d, st);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
   rc = launch_pack(pl, w, wpack, d->sm_count, st);
@@ -575,11 +728,11 @@ int tc3d_workspace_bytes(int op, int N, int Cin, int S0, int S1, int S2, int Cou
                          int k2, const int stride[3], const int pad[3], const int dilation[3],
                          const int output_padding[3], int groups, size_t* bytes) {
   if (!bytes) return TC3D_ERR_NULL;
-  Plan pl;
-  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
-                    output_padding, groups, &pl);
+  CallPlan cp;
+  int rc = plan_call(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                     output_padding, groups, &cp);
   if (rc) return rc;
-  *bytes = (size_t)pl.ws_total;
+  *bytes = (size_t)cp.ws_total;
   return TC3D_OK;
 }
 
@@ -605,12 +758,72 @@ int tc3d_out_shape(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int
 int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
                        int k2, const int stride[3], const int pad[3], const int dilation[3],
                        const int output_padding[3], int groups, char* buf, size_t buflen) {
-  Plan pl;
-  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
-                    output_padding, groups, &pl);
+  CallPlan cp;
+  int rc = plan_call(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                     output_padding, groups, &cp);
+  Plan& pl = cp.pl;
   if (rc == TC3D_ERR_NULL) pl.status = rc;
   if (buf && buflen) {
     std::string s = describe(pl);
+    if (pl.status == TC3D_OK && is_bn_op(op)) {
+      // the algebraic path: patch size, boxes, classes, the pooled conv
+      s.pop_back();
+      append(s, ", \"pool_path\": %lld", cp.pool ? 1 : 0);
+      append(s, ", \"pool_ok\": %lld", cp.pool_ok ? 1 : 0);
+      if (cp.pool_ok) {
+        const PoolPlan& pp = cp.pp;
+        append(s, ", \"pool_D\": %lld", pp.D);
+        append(s, ", \"pool_nbox\": %lld", pp.nbox);
+        append(s, ", \"pool_ncls\": %lld", pp.ncls);
+        char b[160];
+        snprintf(b, sizeof(b), ", \"pool_M\": [%d, %d, %d], \"pool_Ke\": [%d, %d, %d]", pp.M[0],
+                 pp.M[1], pp.M[2], pp.Ke[0], pp.Ke[1], pp.Ke[2]);
+        s += b;
+        snprintf(b, sizeof(b), ", \"pool_e_min\": [%d, %d, %d]", pp.e_min[0], pp.e_min[1],
+                 pp.e_min[2]);
+        s += b;
+        append(s, ", \"pool_conv_tiles\": %lld", pp.cplan.tiles);
+        // tables: offsets U, per axis and class the (tap, offset index)
+        // pairs, the boxes, and per class its sign on each box
+        s += ", \"pool_U\": [";
+        for (int a = 0; a < 3; ++a) {
+          s += a ? ", [" : "[";
+          for (int i = 0; i < pp.nU[a]; ++i) append(s, i ? ", %lld" : "%lld", pp.U[a][i]);
+          s += "]";
+        }
+        s += "], \"pool_taps\": [";
+        for (int a = 0; a < 3; ++a) {
+          s += a ? ", [" : "[";
+          for (int r = 0; r < 2; ++r) {
+            s += r ? ", [" : "[";
+            for (int i = 0; i < pp.ntap[a][r]; ++i) {
+              snprintf(b, sizeof(b), "%s[%d, %d]", i ? ", " : "", pp.tap_k[a][r][i],
+                       pp.tap_u[a][r][i]);
+              s += b;
+            }
+            s += "]";
+          }
+          s += "]";
+        }
+        s += "], \"pool_boxes\": [";
+        for (int i = 0; i < pp.nbox; ++i) {
+          snprintf(b, sizeof(b), "%s[%d, %d, %d, %d, %d, %d]", i ? ", " : "", pp.box_lo[i][0],
+                   pp.box_lo[i][1], pp.box_lo[i][2], pp.box_hi[i][0], pp.box_hi[i][1],
+                   pp.box_hi[i][2]);
+          s += b;
+        }
+        s += "], \"pool_cls\": [";
+        for (int c = 0; c < pp.ncls; ++c) {
+          snprintf(b, sizeof(b), "%s[[%d, %d, %d], [", c ? ", " : "", pp.cls_r[c][0],
+                   pp.cls_r[c][1], pp.cls_r[c][2]);
+          s += b;
+          for (int i = 0; i < pp.nbox; ++i) append(s, i ? ", %lld" : "%lld", pp.cls_coef[c][i]);
+          s += "]]";
+        }
+        s += "]";
+      }
+      s += "}";
+    }
     size_t n = std::min(buflen - 1, s.size());
     std::memcpy(buf, s.data(), n);
     buf[n] = 0;

@@ -129,6 +129,10 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     if (pl.O[a] <= 0) return fail(TC3D_ERR_SHAPE);
     if (pl.O[a] > (1 << 30)) return fail(TC3D_ERR_UNSUPPORTED);
   }
+  for (int a = 0; a < 3; ++a) {
+    if (pb.out_ext[a] < 0 || pb.out_ext[a] > pl.O[a]) return fail(TC3D_ERR_UNSUPPORTED);
+    if (pb.out_ext[a] > 0) pl.O[a] = pb.out_ext[a];
+  }
   int64_t ovol = pl.O[0] * pl.O[1] * pl.O[2];
   if (pb.op == OP_CONV || pb.op == OP_CONVT) {
     pl.y_elems = (int64_t)pb.N * pb.Cout * ovol;
@@ -502,6 +506,7 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
 // output extents in O_user.
 int make_plan(const Problem& pb, Plan* out) {
   if (pb.op == OP_CONV && pb.k[2] == 1 && pb.pad[2] == 0 && pb.stride[0] == 1 &&
+      pb.out_ext[0] == 0 && pb.out_ext[1] == 0 && pb.out_ext[2] == 0 &&
       pb.stride[1] == 1 && pb.stride[2] == 1 && pb.groups == 1 &&
       validate(pb, false) == TC3D_OK && (int64_t)pb.S[1] * pb.S[2] < (1 << 30)) {
     Problem m = pb;
@@ -528,5 +533,198 @@ int make_plan(const Problem& pb, Plan* out) {
   return st;
 }
 
-}  // namespace tc3d
+int make_pool_plan(const Plan& bn, PoolPlan* out) {
+  PoolPlan& pp = *out;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.status = TC3D_ERR_UNSUPPORTED;
+  const Problem& pb = bn.pb;
+  if (bn.status != TC3D_OK || !is_bn_op(pb.op) || pb.groups != 1) return pp.status;
+  for (int a = 0; a < 3; ++a)
+    if (pb.stride[a] != 2) return pp.status;
+  // offsets and taps per axis and class: class r, tap k reads m + (r + p - d k)/2
+  int V = 1;
+  for (int a = 0; a < 3; ++a) {
+    const int p = pb.pad[a], d = pb.dil[a];
+    int umin = 1 << 30, umax = -(1 << 30);
+    for (int r = 0; r < 2; ++r)
+      for (int k = 0; k < pb.k[a]; ++k) {
+        const int t = r + p - d * k;
+        if (t % 2 == 0) {
+          umin = std::min(umin, t / 2);
+          umax = std::max(umax, t / 2);
+        }
+      }
+    if (umin > umax || umax - umin + 1 > kMaxAxisTaps) return pp.status;
+    int used[kMaxAxisTaps] = {0};
+    for (int r = 0; r < 2; ++r)
+      for (int k = 0; k < pb.k[a]; ++k) {
+        const int t = r + p - d * k;
+        if (t % 2 == 0) used[t / 2 - umin] = 1;
+      }
+    int idx[kMaxAxisTaps];
+    pp.nU[a] = 0;
+    for (int u = umin; u <= umax; ++u)
+      if (used[u - umin]) {
+        idx[u - umin] = pp.nU[a];
+        pp.U[a][pp.nU[a]++] = u;
+      }
+    for (int r = 0; r < 2; ++r) {
+      pp.ntap[a][r] = 0;
+      for (int k = 0; k < pb.k[a]; ++k) {
+        const int t = r + p - d * k;
+        if (t % 2 == 0) {
+          const int i = pp.ntap[a][r]++;
+          pp.tap_k[a][r][i] = k;
+          pp.tap_u[a][r][i] = idx[t / 2 - umin];
+        }
+      }
+    }
+    V *= pp.nU[a];
+  }
+  pp.D = pb.Cin * V;
+  if (pp.D > kGramMaxD) return pp.status;
 
+  // rows: class r has rows m < ceil((O - r)/2); the box is the largest of them
+  int slab_axis[3], nslab = 0;
+  for (int a = 0; a < 3; ++a) {
+    int64_t Mr[2];
+    for (int r = 0; r < 2; ++r) Mr[r] = pp.ntap[a][r] ? ceil_div(bn.O[a] - r, 2) : 0;
+    pp.M[a] = (int)std::max(Mr[0], Mr[1]);
+    if (pp.M[a] <= 0) return pp.status;
+    for (int r = 0; r < 2; ++r)
+      if (pp.ntap[a][r] && Mr[r] < pp.M[a]) {  // at most one row fewer
+        slab_axis[nslab++] = a;
+        break;
+      }
+  }
+  // boxes: subsets S of the slab axes; on an axis in S only the last row
+  pp.nbox = 1 << nslab;
+  for (int b = 0; b < pp.nbox; ++b) {
+    int64_t rows = pb.N;
+    for (int a = 0; a < 3; ++a) {
+      pp.box_lo[b][a] = 0;
+      pp.box_hi[b][a] = pp.M[a];
+    }
+    for (int i = 0; i < nslab; ++i)
+      if (b >> i & 1) pp.box_lo[b][slab_axis[i]] = pp.M[slab_axis[i]] - 1;
+    for (int a = 0; a < 3; ++a) rows *= pp.box_hi[b][a] - pp.box_lo[b][a];
+    pp.box_rows[b] = rows;
+  }
+  // classes with taps on every axis, and their inclusion-exclusion signs
+  pp.ncls = 0;
+  for (int r0 = 0; r0 < 2; ++r0)
+    for (int r1 = 0; r1 < 2; ++r1)
+      for (int r2 = 0; r2 < 2; ++r2) {
+        const int r[3] = {r0, r1, r2};
+        if (!pp.ntap[0][r0] || !pp.ntap[1][r1] || !pp.ntap[2][r2]) continue;
+        const int c = pp.ncls++;
+        int short_mask = 0;  // slab axes on which this class ends one row early
+        for (int i = 0; i < nslab; ++i) {
+          const int a = slab_axis[i];
+          if (ceil_div(bn.O[a] - r[a], 2) < pp.M[a]) short_mask |= 1 << i;
+        }
+        for (int a = 0; a < 3; ++a) pp.cls_r[c][a] = r[a];
+        for (int b = 0; b < pp.nbox; ++b) {
+          int bits = 0;
+          for (int i = 0; i < nslab; ++i) bits += b >> i & 1;
+          pp.cls_coef[c][b] = (b & ~short_mask) ? 0 : (bits & 1 ? -1 : 1);
+        }
+      }
+
+  // Gram work units: per box, a0 = its thinnest axis (the first of equals),
+  // a2 = the longest of the other two (the later of equals), a1 the third; a
+  // unit is Tn samples at one m_a0 and a tile of T1 x T2 rows of
+  // (m_a1, m_a2), whose x slabs must fit one buffer
+  for (int b = 0; b < pp.nbox; ++b) {
+    int ext[3], a0 = 0;
+    for (int a = 0; a < 3; ++a) ext[a] = pp.box_hi[b][a] - pp.box_lo[b][a];
+    for (int a = 1; a < 3; ++a)
+      if (ext[a] < ext[a0]) a0 = a;
+    int a1 = a0 == 0 ? 1 : 0, a2 = a0 == 2 ? 1 : 2;
+    if (ext[a1] > ext[a2]) std::swap(a1, a2);
+    pp.box_perm[b][0] = a0;
+    pp.box_perm[b][1] = a1;
+    pp.box_perm[b][2] = a2;
+    const int span1 = pp.U[a1][pp.nU[a1] - 1] - pp.U[a1][0];
+    const int span2 = pp.U[a2][pp.nU[a2] - 1] - pp.U[a2][0];
+    const int T2 = std::min(ext[a2], 64);
+    // row stride: 4 x an odd number, so that rows are 16-byte copies and the
+    // 32 lines a warp reads (each lane at its own rotated start) fall in
+    // distinct banks
+    int W2p = (T2 + span2 + 3) / 4 * 4;
+    if ((W2p / 4) % 2 == 0) W2p += 4;
+    const int64_t planes = (int64_t)pb.Cin * pp.nU[a0];
+    const int64_t t1 = kGramSlabFloats / (planes * W2p) - span1;
+    if (t1 < 1) return pp.status;
+    pp.box_T2[b] = T2;
+    pp.box_W2p[b] = W2p;
+    pp.box_T1[b] = (int)std::min<int64_t>(t1, ext[a1]);
+    pp.box_W1[b] = pp.box_T1[b] + span1;
+    // thin boxes: several samples per unit, as many slabs as fit, but at
+    // least 8 units per box so that several CTAs can share it
+    pp.box_Tn[b] = (int)std::max<int64_t>(
+        1, std::min<int64_t>({(int64_t)(pb.N + 7) / 8,
+                              kGramSlabFloats / (planes * pp.box_W1[b] * W2p)}));
+  }
+
+  // pooled conv: window z = 4q + j reads input 2q + e, e = (j + p - d k)/2
+  for (int a = 0; a < 3; ++a) {
+    const int p = pb.pad[a], d = pb.dil[a];
+    int emin = 1 << 30, emax = -(1 << 30);
+    for (int j = 0; j < 4; ++j)
+      for (int k = 0; k < pb.k[a]; ++k) {
+        const int t = j + p - d * k;
+        if (t % 2 == 0) {
+          emin = std::min(emin, t / 2);
+          emax = std::max(emax, t / 2);
+        }
+      }
+    if (emin > emax || emin > 0) return pp.status;
+    // offsets below e_min have no (j, k) pair: leading taps of weight 0 widen
+    // the left padding until the conv formula yields all P windows
+    while (conv_len(pb.S[a], emax - emin + 1, 2, -emin, 1) < bn.P[a] &&
+           emax - emin + 1 < kMaxAxisTaps)
+      --emin;
+    if (emax - emin + 1 > kMaxAxisTaps) return pp.status;
+    pp.e_min[a] = emin;
+    pp.Ke[a] = emax - emin + 1;
+  }
+  Problem c;
+  std::memset(&c, 0, sizeof(c));
+  c.op = OP_CONV;
+  c.N = pb.N;
+  c.Cin = pb.Cin;
+  c.Cout = pb.Cout;
+  c.groups = 1;
+  for (int a = 0; a < 3; ++a) {
+    c.S[a] = pb.S[a];
+    c.k[a] = pp.Ke[a];
+    c.stride[a] = 2;
+    c.pad[a] = -pp.e_min[a];
+    c.dil[a] = 1;
+    c.out_ext[a] = (int)bn.P[a];
+  }
+  pp.conv = c;
+  if (make_plan(c, &pp.cplan) != TC3D_OK) return pp.status;
+
+  // workspace: the pooled conv's packed weights first, then this path's own
+  int64_t off = pp.cplan.ws_total;
+  pp.ws_wpack_off = pp.cplan.ws_wpack_off;
+  pp.ws_w2_off = off;
+  pp.ws_w2_bytes = (int64_t)pb.Cout * pb.Cin * pp.Ke[0] * pp.Ke[1] * pp.Ke[2] * 4;
+  off = round_up(off + pp.ws_w2_bytes, 256);
+  pp.ws_b2_off = off;
+  off = round_up(off + (int64_t)pb.Cout * 4, 256);
+  if (pb.op == OP_CONVT_BN_POOL) {
+    pp.ws_gpart_off = off;
+    pp.ws_gpart_bytes = (int64_t)kGramMaxCtas * kGramEntries * 4;
+    off = round_up(off + pp.ws_gpart_bytes, 256);
+    pp.ws_gsum_off = off;
+    off = round_up(off + (int64_t)kGramMaxBoxes * kGramEntries * 8, 256);
+  }
+  pp.ws_total = off;
+  pp.status = TC3D_OK;
+  return pp.status;
+}
+
+}  // namespace tc3d

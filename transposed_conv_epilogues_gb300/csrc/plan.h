@@ -38,6 +38,9 @@ constexpr int kBnSlotsPerCta = 4;   // BatchNorm partial slots per CTA (one per 
 struct Problem {
   int op;
   int N, Cin, S[3], Cout, k[3], stride[3], pad[3], dil[3], out_pad[3], groups;
+  // internal convolutions only: output extents below the formula's (0: the
+  // formula's own); rows past them are not computed
+  int out_ext[3];
 };
 
 // Everything a launch needs, derived from a Problem.  Row space: for every
@@ -138,6 +141,69 @@ inline int64_t bn_part_slots(const Plan& pl, int64_t grid) {
 }
 
 int make_plan(const Problem& pb, Plan* plan);
+
+// ---------------------------------------------------------------------------
+// Algebraic path of the BN-pool pipelines (transposed conv with stride 2 on
+// every axis, groups 1, few input channels).
+//
+// Pooled output.  A 4x4x4 window q covers z = 4q + j (j = 0..3) per axis.
+// Output z takes tap k from input (z + p - d k)/2, so the window's sum reads
+// input 2q + e with e = (j + p - d k)/2: the pooled sums are a stride-2
+// convolution of x with summed weights W'[e] = sum of W[k] over the (j, k)
+// pairs giving e ("Kimi-K2.6 l2_p72", its observation that one pooled output
+// depends on a 3x3x3 input footprint).  With the BatchNorm scale folded in,
+// that convolution writes final outputs.
+//
+// Batch statistics.  Row m of the transposed conv holds output 2m + r of
+// every class r; class r reads inputs m + u for its offsets u.  Let P(m) be
+// the vector of x over (channel, u0, u1, u2) for the union of offsets, D
+// entries.  Then the class sum of t is w_r . s_r and the class sum of t^2 is
+// w_r^T G_r w_r, with s_r = sum P(m) and G_r = sum P(m) P(m)^T over the rows
+// class r has.  The rows of a class are the box [0, M) less, on axes where the
+// class ends one row early, the last plane: G_r follows by inclusion-exclusion
+// over at most 8 boxes (the full box and its last planes, edges, corner).
+constexpr int kGramMaxD = 32;                                   // patch entries
+constexpr int kGramEntries = kGramMaxD * kGramMaxD + kGramMaxD; // G then s
+constexpr int kGramMaxCtas = 1024;                              // partial slots
+constexpr int kGramMaxBoxes = 8;
+constexpr int kGramSlabFloats = 12288;                          // one x slab buffer (48 KB)
+
+struct PoolPlan {
+  int status;     // 0: the algebraic path applies
+  int D;          // patch entries Cin * nU0 * nU1 * nU2 (<= kGramMaxD)
+  int nU[3];
+  int U[3][kMaxAxisTaps];              // union of input offsets per axis
+  // per axis, class r in {0, 1}: taps (kernel index, index into U)
+  int ntap[3][2];
+  int tap_k[3][2][kMaxAxisTaps], tap_u[3][2][kMaxAxisTaps];
+  int M[3];                            // row grid of the transposed conv
+  int nbox;
+  int box_lo[kGramMaxBoxes][3], box_hi[kGramMaxBoxes][3];
+  int64_t box_rows[kGramMaxBoxes];
+  int ncls;                            // classes with taps on every axis
+  int cls_r[8][3];
+  int cls_coef[8][kGramMaxBoxes];      // inclusion-exclusion sign per box
+  // Gram work units per box: the box's axes as (a0, a1, a2), a0 its thinnest;
+  // a unit is Tn samples n at one m_a0 with a T1 x T2 tile of (m_a1, m_a2),
+  // its x slab [Tn][Cin * nU_a0 planes][W1][W2p] floats
+  int box_perm[kGramMaxBoxes][3];
+  int box_Tn[kGramMaxBoxes];
+  int box_T1[kGramMaxBoxes], box_T2[kGramMaxBoxes];
+  int box_W1[kGramMaxBoxes], box_W2p[kGramMaxBoxes];
+  int e_min[3], Ke[3];                 // pooled conv taps: e in [e_min, e_min + Ke)
+  Problem conv;                        // the pooled conv (stride 2, pad -e_min)
+  Plan cplan;                          // its engine plan
+  int64_t ws_wpack_off;                // = cplan.ws_wpack_off
+  int64_t ws_w2_off, ws_w2_bytes;      // summed, scaled weights [Cout][Cin][Ke0][Ke1][Ke2]
+  int64_t ws_b2_off;                   // folded bias [Cout]
+  int64_t ws_gpart_off, ws_gpart_bytes;// per-CTA Gram partials [kGramMaxCtas][kGramEntries] f32
+  int64_t ws_gsum_off;                 // per-class combined Gram [8][kGramEntries] f64
+  int64_t ws_total;
+};
+
+// Fill *pp for a BN-pool plan (op OP_CONVT_BN_POOL / OP_CONVT_BN_EVAL).
+// Returns pp->status: 0 when the algebraic path applies.
+int make_pool_plan(const Plan& bn, PoolPlan* pp);
 
 // Integer output length of one axis.
 int64_t conv_len(int64_t L, int k, int s, int p, int d);
