@@ -21,6 +21,9 @@
  *                              -> AvgPool3d(2) ("Kimi-K2.6 l2_p72", problem
  *                              statement; the two pools are one 4x4x4 pool
  *                              by that page's pooling derivation).
+ *   tc3d_conv3d_fwd_ndhwc      tc3d_conv3d_fwd with x and y channels-last
+ *                              (NDHWC), the layout "Kimi-K2.6 l2_p43"
+ *                              weighs against NCDHW.
  *   tc3d_convT_bneval_avgpool  the same pipeline with BatchNorm3d in
  *                              evaluation mode: the running mean and
  *                              variance replace the batch statistics (the
@@ -80,15 +83,32 @@ extern "C" {
 #define TC3D_OP_CONV_MAXPOOL_LSE_RELU 2
 #define TC3D_OP_CONVT_BN_AVGPOOL 3
 #define TC3D_OP_CONVT_BNEVAL_AVGPOOL 4
+#define TC3D_OP_CONV3D_NDHWC 5
 
 /* y[n,oc,o] = bias[oc] + sum_{ic in group(oc), k} w[oc,ic',k] *
  *             x[n, ic, o*stride - pad + dilation*k]   (zero outside x)
- * y: [N, Cout, O0, O1, O2], O = floor((S + 2p - d(k-1) - 1)/s) + 1. */
+ * y: [N, Cout, O0, O1, O2], O = floor((S + 2p - d(k-1) - 1)/s) + 1.
+ * Grouped convs with few channels per group (Cin/groups * Cout/groups <= 16;
+ * stride and dilation 1 or 2 and at most 7 taps along the last axis) run in
+ * a direct fp32 CUDA-core kernel; everything else in the tensor-core engine. */
 int tc3d_conv3d_fwd(const float* x, const float* w, const float* bias, float* y, int N,
                     int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
                     const int stride[3], const int pad[3], const int dilation[3],
                     const int output_padding[3], int groups, void* workspace,
                     size_t workspace_bytes, cudaStream_t stream);
+
+/* tc3d_conv3d_fwd on channels-last tensors: x [N, S0, S1, S2, Cin],
+ * y [N, O0, O1, O2, Cout] (w and bias as for tc3d_conv3d_fwd).  Convs with
+ * few channels per group (Cin/groups * Cout/groups <= 16, stride and
+ * dilation 1 or 2 and at most 7 taps along the last axis) run in a direct
+ * fp32 kernel that reads NDHWC natively; others transpose x to NCDHW in the
+ * workspace, run the engine and transpose y back.  tc3d_workspace_bytes /
+ * tc3d_out_shape take TC3D_OP_CONV3D_NDHWC (out_dims in NDHWC order). */
+int tc3d_conv3d_fwd_ndhwc(const float* x, const float* w, const float* bias, float* y, int N,
+                          int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                          const int stride[3], const int pad[3], const int dilation[3],
+                          const int output_padding[3], int groups, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
 
 /* y[n,oc,z] = bias[oc] + sum_{ic in group(oc), k : s | (z+p-d k)} w[ic,oc',k] *
  *             x[n, ic, (z + p - d k)/s]   (terms with the quotient outside x dropped)

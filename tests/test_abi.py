@@ -168,8 +168,37 @@ def test_convT_bneval_avgpool_argument_errors(lib):
         3, (2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1) == (2, 16, 3, 3, 3)
 
 
+def test_direct_and_ndhwc_plans(lib):
+    """Grouped convs with few channels per group take the direct kernel;
+    channels-last shapes and workspace through the transposes."""
+    dw = tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8)
+    assert dw["direct"] == 1 and dw["ndhwc"] == 0
+    assert tc.plan_describe(0, (2, 8, 7, 9, 8), (12, 4, 3, 3, 3), 1, 1, 1, 0, 2)["direct"] == 0
+    assert tc.plan_describe(0, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)["direct"] == 0
+    # 8 taps along x, or stride 3 there: not the direct kernel
+    assert tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 8), 1, 1, 1, 0, 8)["direct"] == 0
+    assert tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 3, 1, 1, 0, 8)["direct"] == 0
+    nd = tc.plan_describe(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)
+    assert nd["ndhwc"] == 1 and nd["direct"] == 0
+    assert tc.out_shape(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1) == (2, 9, 10, 12, 7)
+    dense = tc.workspace_bytes(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)
+    assert dense >= tc.workspace_bytes(0, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1) + \
+        4 * (2 * 5 * 9 * 10 * 12 + 2 * 7 * 9 * 10 * 12)
+    assert tc.workspace_bytes(5, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
+
+
+def test_ndhwc_argument_errors(lib):
+    fn = lib.tc3d_conv3d_fwd_ndhwc
+    P = ctypes.c_void_p
+    ok = (P(256), P(512), None, P(1024))
+    assert _call(lib, fn, (None, P(512), None, P(1024)), _geom()) == tc.TC3D_ERR_NULL
+    assert _call(lib, fn, ok, _geom(N=0)) == tc.TC3D_ERR_SHAPE
+    assert _call(lib, fn, ok, _geom(Cin=3, G=2)) == tc.TC3D_ERR_GROUPS
+    assert _call(lib, fn, ok, _geom(Cin=4, Cout=6, G=2), ws=0) == tc.TC3D_ERR_WORKSPACE
+
+
 def test_workspace_bytes(lib):
-    for op in range(5):
+    for op in range(6):
         n = tc.workspace_bytes(op, (2, 4, 9, 9, 9), (4, 4, 3, 3, 3), 2 if op % 2 else 1, 1)
         assert n >= 256 and n % 256 == 0
 

@@ -68,7 +68,8 @@ CONV_CASES = [
     ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, 1, 1, 1, True),         # (k,k,1), pad on k=1 axis
     ((1, 6, 7, 8, 9), (40, 6, 1, 1, 1), 1, 0, 1, 1, False),          # k = 1
     ((1, 4, 6, 6, 8), (200, 4, 3, 1, 3), 1, (1, 0, 1), 1, 1, True),  # 2 column blocks
-    ((2, 8, 7, 9, 8), (8, 2, 3, 3, 3), 1, 1, 1, 4, True),            # groups 4
+    ((2, 8, 7, 9, 8), (8, 2, 3, 3, 3), 1, 1, 1, 4, True),            # groups 4 (direct kernel)
+    ((2, 8, 7, 9, 8), (12, 4, 3, 3, 3), 1, 1, 1, 2, True),           # groups 2, 4x6 per group: engine
     ((1, 3, 13, 12, 16), (5, 3, 5, 3, 5), (1, 2, 1), 2, 2, 1, True),  # k5 dil 2
     ((3, 17, 6, 5, 20), (9, 17, 2, 3, 2), 1, 0, 1, 1, True),         # Cin 17: 2 chunks
     # view mode: one tap along x, x lines filling 128-row accumulators
@@ -243,6 +244,46 @@ def test_uniform01_inputs(tc):
     check(tc.convT_bn_avgpool(_dev(xt), _dev(wt), _dev(bt), None, None, 1e-5, 2, 1)
           .cpu().numpy(), orc.convT_bn_avgpool(xt, wt, bt, None, None, 1e-5, 2, 1),
           "bn-pool uniform01")
+
+
+# --------------------------------------------------------------------------
+# grouped / depthwise convs in the direct kernel, and channels-last layout
+# --------------------------------------------------------------------------
+DIRECT_CASES = [
+    # x shape, w shape, stride, pad, dil, groups
+    ((2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 8),                  # depthwise k3
+    ((1, 6, 7, 9, 17), (12, 1, 3, 3, 5), (1, 2, 2), (1, 0, 2), 1, 6),   # depthwise x2, stride 2 on x
+    ((2, 4, 8, 6, 11), (4, 2, 2, 3, 3), 1, (0, 1, 2), (1, 1, 2), 2),    # dilation 2 on x
+    ((1, 9, 5, 6, 23), (9, 3, 1, 3, 7), (2, 1, 2), (0, 1, 3), (1, 2, 2), 3),  # 7 taps, s2 d2
+    ((3, 4, 4, 5, 6), (8, 1, 3, 1, 2), 1, 1, 1, 4),                    # ragged, k2 = 2
+]
+
+
+@pytest.mark.parametrize("case", DIRECT_CASES)
+def test_direct_grouped_conv(tc, case):
+    xs, ws, s, p, d, G = case
+    x, w, b = make(xs, ws, ws[0], True, seed=71)
+    assert tc.plan_describe(0, xs, ws, s, p, d, 0, G)["direct"] == 1
+    y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), s, p, d, G).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, s, p, d, G), f"direct {case}")
+
+
+NDHWC_CASES = DIRECT_CASES[:3] + [
+    # not for the direct kernel: through the engine with layout transposes
+    ((2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1, 1, 1),
+    ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1),           # (k,k,1): merged form
+    ((1, 8, 6, 7, 9), (12, 4, 3, 2, 3), (1, 2, 1), 1, 1, 2),
+]
+
+
+@pytest.mark.parametrize("case", NDHWC_CASES)
+def test_conv3d_ndhwc(tc, case):
+    xs, ws, s, p, d, G = case
+    x, w, b = make(xs, ws, ws[0], True, seed=72)
+    x_cl = np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))
+    y = tc.conv3d_fwd_ndhwc(_dev(x_cl), _dev(w), _dev(b), s, p, d, G).cpu().numpy()
+    ref = orc.conv3d(x, w, b, s, p, d, G).transpose(0, 2, 3, 4, 1)
+    check(y, ref, f"ndhwc {case}")
 
 
 # --------------------------------------------------------------------------

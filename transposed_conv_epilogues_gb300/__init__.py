@@ -8,6 +8,7 @@ CPU or PyTorch fallback: if the library cannot be loaded, every call raises.
 Entry points (same names as the C ABI, without the ``tc3d_`` prefix):
 
 * ``conv3d_fwd(x, w, bias, stride, padding, dilation, groups)``
+* ``conv3d_fwd_ndhwc(x, w, bias, stride, padding, dilation, groups)`` (x, y channels-last)
 * ``conv_transpose3d_fwd(x, w, bias, stride, padding, dilation, output_padding, groups)``
 * ``conv_maxpool_lse_relu(x, w, bias, stride, padding, dilation, groups)``
 * ``convT_bn_avgpool(x, w, bias, gamma, beta, eps, stride, padding, dilation,
@@ -33,6 +34,7 @@ OP_CONV_TRANSPOSE3D = 1
 OP_CONV_MAXPOOL_LSE_RELU = 2
 OP_CONVT_BN_AVGPOOL = 3
 OP_CONVT_BNEVAL_AVGPOOL = 4
+OP_CONV3D_NDHWC = 5
 
 TC3D_OK = 0
 TC3D_ERR_NULL = -1
@@ -51,6 +53,7 @@ EXPORTED = [
     "tc3d_convT_bn_avgpool", "tc3d_workspace_bytes", "tc3d_out_shape", "tc3d_plan_describe",
     "tc3d_last_device_error", "tc3d_set_wait_timeout_ns", "tc3d_selftest_wait_timeout",
     "tc3d_status_string", "tc3d_conv_maxpool_lse_relu_noalloc", "tc3d_convT_bneval_avgpool",
+    "tc3d_conv3d_fwd_ndhwc",
 ]
 
 _lib = None
@@ -78,7 +81,8 @@ def load(path: str | Path | None = None):
     lib = ctypes.CDLL(str(p))
     geom = [_I] * 9 + [_I3, _I3, _I3, _I3, _I]  # N Cin S0 S1 S2 Cout k0 k1 k2 | s p d op | groups
     tail = [_P, ctypes.c_size_t, _P]  # workspace, bytes, stream
-    for name in ("tc3d_conv3d_fwd", "tc3d_conv_transpose3d_fwd", "tc3d_conv_maxpool_lse_relu"):
+    for name in ("tc3d_conv3d_fwd", "tc3d_conv_transpose3d_fwd", "tc3d_conv_maxpool_lse_relu",
+                 "tc3d_conv3d_fwd_ndhwc"):
         f = getattr(lib, name)
         f.argtypes = [_P, _P, _P, _P] + geom + tail
         f.restype = _I
@@ -226,22 +230,26 @@ def _run(op, x, w, bias, stride, padding, dilation, output_padding, groups, out,
         _check_tensor(t, n, dev)
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x and w must be 5-D (NCDHW / [*, *, k0, k1, k2])")
-    _check_weight(op, x.shape, w.shape, bias, groups)
-    shp = out_shape(op, x.shape, w.shape, stride, padding, dilation, output_padding, groups)
+    # shapes in NCDHW terms (channels-last x is [N, S0, S1, S2, C])
+    xs = tuple(x.shape)
+    if op == OP_CONV3D_NDHWC:
+        xs = (xs[0], xs[4], xs[1], xs[2], xs[3])
+    _check_weight(op, xs, w.shape, bias, groups)
+    shp = out_shape(op, xs, w.shape, stride, padding, dilation, output_padding, groups)
     if out is None:
         out = torch.empty(shp, dtype=torch.float32, device=dev)
     elif tuple(out.shape) != shp:
         raise ValueError(f"out has shape {tuple(out.shape)}, expected {shp}")
-    nbytes = workspace_bytes(op, x.shape, w.shape, stride, padding, dilation, output_padding,
-                             groups)
+    nbytes = workspace_bytes(op, xs, w.shape, stride, padding, dilation, output_padding, groups)
     ws = _workspace(nbytes, dev, workspace)
-    g = _geom(x.shape, w.shape, _is_transposed(op), stride, padding, dilation, output_padding,
-              groups)
+    g = _geom(xs, w.shape, _is_transposed(op), stride, padding, dilation, output_padding, groups)
     tail = (ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel() * ws.element_size()),
             _stream(stream, dev))
     with torch.cuda.device(dev):
         if op == OP_CONV3D:
             rc = lib.tc3d_conv3d_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), *g, *tail)
+        elif op == OP_CONV3D_NDHWC:
+            rc = lib.tc3d_conv3d_fwd_ndhwc(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), *g, *tail)
         elif op == OP_CONV_TRANSPOSE3D:
             rc = lib.tc3d_conv_transpose3d_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), *g, *tail)
         elif op == OP_CONV_MAXPOOL_LSE_RELU:
@@ -266,7 +274,8 @@ def _run(op, x, w, bias, stride, padding, dilation, output_padding, groups, out,
                                                    ctypes.c_float(eps), _ptr(out), *g, *tail)
     if rc:
         raise Tc3dError(rc, ["conv3d_fwd", "conv_transpose3d_fwd", "conv_maxpool_lse_relu",
-                             "convT_bn_avgpool", "convT_bneval_avgpool"][op])
+                             "convT_bn_avgpool", "convT_bneval_avgpool",
+                             "conv3d_fwd_ndhwc"][op])
     return out
 
 
@@ -274,6 +283,14 @@ def conv3d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, out=N
                workspace=None, stream=None):
     """Conv3d forward; w [Cout, Cin/groups, k0, k1, k2]."""
     return _run(OP_CONV3D, x, w, bias, stride, padding, dilation, 0, groups, out, workspace,
+                stream)
+
+
+def conv3d_fwd_ndhwc(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, out=None,
+                     workspace=None, stream=None):
+    """Conv3d forward on channels-last tensors: x [N, S0, S1, S2, Cin] ->
+    y [N, O0, O1, O2, Cout]; w [Cout, Cin/groups, k0, k1, k2]."""
+    return _run(OP_CONV3D_NDHWC, x, w, bias, stride, padding, dilation, 0, groups, out, workspace,
                 stream)
 
 

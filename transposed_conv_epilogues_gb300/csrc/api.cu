@@ -15,6 +15,7 @@
 #include "../../include/tc3d.h"
 #include "engine.cuh"
 #include "plan.h"
+#include "direct.cuh"
 #include "pool.cuh"
 
 using namespace tc3d;
@@ -339,15 +340,28 @@ struct CallPlan {
   PoolPlan pp;
   bool pool_ok = false;  // the algebraic path applies
   bool pool = false;     // and is taken
+  bool ndhwc = false;    // channels-last x and y (OP_CONV_NDHWC)
+  bool direct = false;   // the direct CUDA-core conv kernel
+  Problem upb;           // the caller's problem (the engine plan may use a merged form)
+  int64_t ws_xt_off = 0, ws_yt_off = 0;  // channels-last through the engine: NCDHW copies
   int64_t ws_total = 0;
 };
 
 int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
               const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
               int groups, CallPlan* cp) {
-  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
-                    &cp->pl);
+  cp->ndhwc = op == OP_CONV_NDHWC;
+  int rc = plan_for(cp->ndhwc ? OP_CONV : op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad,
+                    dil, out_pad, groups, &cp->pl);
   if (rc) return rc;
+  cp->upb = make_problem(cp->ndhwc ? OP_CONV : op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride,
+                         pad, dil, out_pad, groups);
+  // the direct kernel: grouped convs with few channels per group (the
+  // engine's GEMM-N would be mostly padding), and any such conv in
+  // channels-last layout
+  const Problem& pb = cp->upb;
+  if (pb.op == OP_CONV && (pb.groups > 1 || cp->ndhwc))
+    cp->direct = direct_eligible(cp->pl.cin_g, cp->pl.cout_g, pb.stride[2], pb.dil[2], pb.k[2]);
   // the algebraic path: always for running statistics; for batch statistics
   // only where the fused engine epilogue cannot run (its Gram statistics
   // measured slower than that epilogue on the 64 x 3 x 32^3 workload, and
@@ -355,7 +369,47 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
   cp->pool_ok = is_bn_op(op) && make_pool_plan(cp->pl, &cp->pp) == TC3D_OK;
   cp->pool = cp->pool_ok && (op == OP_CONVT_BN_EVAL || !cp->pl.fused);
   cp->ws_total = cp->pool ? cp->pp.ws_total : cp->pl.ws_total;
+  if (cp->direct) {
+    cp->ws_total = 256;  // nothing is staged
+  } else if (cp->ndhwc) {
+    // channels-last through the engine: x and y transposed to NCDHW copies
+    const int64_t xs = (int64_t)pb.N * pb.Cin * pb.S[0] * pb.S[1] * pb.S[2] * 4;
+    cp->ws_xt_off = (cp->ws_total + 255) / 256 * 256;
+    cp->ws_yt_off = (cp->ws_xt_off + xs + 255) / 256 * 256;
+    cp->ws_total = cp->ws_yt_off + cp->pl.y_elems * 4;
+  }
   return TC3D_OK;
+}
+
+// The direct conv kernel (grouped convs with few channels per group; NCDHW
+// or channels-last)
+int run_direct(const CallPlan& cp, const float* x, const float* w, const float* bias, float* y,
+               DeviceState* d, cudaStream_t st) {
+  const Plan& pl = cp.pl;
+  const Problem& pb = cp.upb;
+  DirectParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.x = x;
+  dp.w = w;
+  dp.bias = bias;
+  dp.y = y;
+  dp.N = pb.N;
+  dp.C = pb.Cin;
+  dp.Cout = pb.Cout;
+  dp.cin_g = pl.cin_g;
+  dp.cout_g = pl.cout_g;
+  for (int a = 0; a < 3; ++a) {
+    dp.S[a] = pb.S[a];
+    dp.k[a] = pb.k[a];
+    dp.s[a] = pb.stride[a];
+    dp.p[a] = pb.pad[a];
+    dp.d[a] = pb.dil[a];
+    dp.O[a] = (int)pl.O_user[a];
+  }
+  dp.nrun2 = (dp.O[2] + kDirectRun - 1) / kDirectRun;
+  dp.items = (long long)pb.N * pb.Cout * dp.O[0] * dp.O[1] * dp.nrun2;
+  return direct_conv_launch(dp, cp.ndhwc, d->sm_count, st) == cudaSuccess ? TC3D_OK
+                                                                         : TC3D_ERR_CUDA;
 }
 
 // The algebraic BN-pool path: [Gram matrices, their reduction,] finalize
@@ -502,6 +556,24 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
   rc = device_state(&d);
   if (rc) return rc;
   if (cp.pool) return run_pool(op, cp, x, w, bias, bn, y, ws, d, st);
+  if (cp.direct) return run_direct(cp, x, w, bias, y, d, st);
+  if (cp.ndhwc) {
+    // channels-last through the engine: x -> NCDHW, the conv, y -> NDHWC
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    float* xt = reinterpret_cast<float*>(wsb + cp.ws_xt_off);
+    float* yt = reinterpret_cast<float*>(wsb + cp.ws_yt_off);
+    const Problem& pb = pl.pb;
+    const long long sv = (long long)pb.S[0] * pb.S[1] * pb.S[2];
+    const long long ov = (long long)pl.O[0] * pl.O[1] * pl.O[2];
+    if (transpose_launch(x, xt, pb.N, sv, pb.Cin, st) != cudaSuccess) return TC3D_ERR_CUDA;
+    float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
+    rc = launch_pack(pl, w, wpack, d->sm_count, st);
+    if (rc) return rc;
+    rc = launch_engine(pl, pl.epi, xt, wpack, bias, yt, nullptr, d, st);
+    if (rc) return rc;
+    return transpose_launch(yt, y, pb.N, pb.Cout, ov, st) == cudaSuccess ? TC3D_OK
+                                                                         : TC3D_ERR_CUDA;
+  }
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
   rc = launch_pack(pl, w, wpack, d->sm_count, st);
@@ -724,6 +796,15 @@ int tc3d_convT_bneval_avgpool(const float* x, const float* w, const float* bias,
              pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
 }
 
+int tc3d_conv3d_fwd_ndhwc(const float* x, const float* w, const float* bias, float* y, int N,
+                          int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
+                          const int stride[3], const int pad[3], const int dilation[3],
+                          const int output_padding[3], int groups, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  return run(OP_CONV_NDHWC, x, w, bias, BnArgs(), y, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride,
+             pad, dilation, output_padding, groups, workspace, workspace_bytes, stream);
+}
+
 int tc3d_workspace_bytes(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, int k1,
                          int k2, const int stride[3], const int pad[3], const int dilation[3],
                          const int output_padding[3], int groups, size_t* bytes) {
@@ -740,12 +821,16 @@ int tc3d_out_shape(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int
                    int k2, const int stride[3], const int pad[3], const int dilation[3],
                    const int output_padding[3], int groups, int64_t out_dims[5]) {
   if (!out_dims) return TC3D_ERR_NULL;
-  Plan pl;
-  int rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
-                    output_padding, groups, &pl);
+  CallPlan cp;
+  int rc = plan_call(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dilation,
+                     output_padding, groups, &cp);
   if (rc) return rc;
+  const Plan& pl = cp.pl;
   out_dims[0] = N;
-  if (op == OP_CONV || op == OP_CONVT) {
+  if (op == OP_CONV_NDHWC) {  // channels-last y: [N, O0, O1, O2, Cout]
+    for (int a = 0; a < 3; ++a) out_dims[1 + a] = pl.O_user[a];
+    out_dims[4] = Cout;
+  } else if (op == OP_CONV || op == OP_CONVT) {
     out_dims[1] = Cout;
     for (int a = 0; a < 3; ++a) out_dims[2 + a] = pl.O_user[a];
   } else {
@@ -765,6 +850,12 @@ int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout,
   if (rc == TC3D_ERR_NULL) pl.status = rc;
   if (buf && buflen) {
     std::string s = describe(pl);
+    if (pl.status == TC3D_OK && (op == OP_CONV || op == OP_CONV_NDHWC)) {
+      s.pop_back();
+      append(s, ", \"direct\": %lld", cp.direct ? 1 : 0);
+      append(s, ", \"ndhwc\": %lld", cp.ndhwc ? 1 : 0);
+      s += "}";
+    }
     if (pl.status == TC3D_OK && is_bn_op(op)) {
       // the algebraic path: patch size, boxes, classes, the pooled conv
       s.pop_back();

@@ -15,6 +15,7 @@ enum OpKind : int {
   OP_CONV_POOL_LSE = 2,    // conv_maxpool_lse_relu
   OP_CONVT_BN_POOL = 3,    // convT_bn_avgpool (batch statistics)
   OP_CONVT_BN_EVAL = 4,    // convT_bneval_avgpool (running statistics)
+  OP_CONV_NDHWC = 5,       // conv3d_fwd_ndhwc (planned as OP_CONV; x and y channels-last)
 };
 
 inline bool is_bn_op(int op) { return op == OP_CONVT_BN_POOL || op == OP_CONVT_BN_EVAL; }
