@@ -131,7 +131,8 @@ def recorded_traffic(kernel_workload):
 # CPU oracle on bounded samples (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 ORACLE_SAMPLES = {"conv331": 20000000, "convT_s2p1d2": 6000000, "convT_bn_avgpool": 20000000,
-                  "convT_bneval_avgpool": 20000000,
+                  "convT_bneval_avgpool": 20000000, "dwconv_k3": 20000000,
+                  "dwconv_k3_ndhwc": 20000000, "conv_k3_ndhwc": 2000000,
                   "conv_maxpool_lse_relu": 2000000}
 
 
@@ -157,7 +158,7 @@ def oracle_sample_run(names, scale=1.0, inputs_cache=None):
                 inputs_cache[n] = (x, w, b)
         O = W.out_spatial(wl)
         total = wl.x_shape[0] * wl.cout * int(np.prod(O))
-        cnt = max(1, int(ORACLE_SAMPLES[n] * scale))
+        cnt = max(1, int(ORACLE_SAMPLES.get(n, 2000000) * scale))
         idx = inputs.sample_indices(9000 + wl.index, total, cnt)
         kw = dict(stride=wl.stride, padding=wl.padding, dilation=wl.dilation, groups=wl.groups)
         t0 = time.perf_counter()
@@ -203,16 +204,20 @@ def run_ours(args):
     host_bn = {wl.name: wl.make_bn_eval_params() for wl in wls
                if wl.op == "convT_bneval_avgpool"}
     dev_in = {}
+    host_call = {}  # inputs in the layout of the call (the oracle keeps NCDHW)
     dev_bn = {n: tuple(torch.from_numpy(a).to(dev) for a in v) for n, v in host_bn.items()}
     outs = {}
     for wl in wls:
         x, w, b = host[wl.name]
+        if wl.op == "conv3d_ndhwc":  # the same values, channels-last
+            x = np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))
+        host_call[wl.name] = (x, w, b)
         dev_in[wl.name] = tuple(None if a is None else torch.from_numpy(a).to(dev)
                                 for a in (x, w, b))
         outs[wl.name] = torch.empty(W.y_shape(wl), dtype=torch.float32, device=dev)
 
     op_of = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2,
-             "convT_bn_avgpool": 3, "convT_bneval_avgpool": 4}
+             "convT_bn_avgpool": 3, "convT_bneval_avgpool": 4, "conv3d_ndhwc": 5}
     wss = {}
     for wl in wls:
         nb = tc.workspace_bytes(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
@@ -224,6 +229,8 @@ def run_ours(args):
                   out=out, workspace=wss[wl.name])
         if wl.op == "conv3d":
             return tc.conv3d_fwd(x, w, b, **kw)
+        if wl.op == "conv3d_ndhwc":
+            return tc.conv3d_fwd_ndhwc(x, w, b, **kw)
         if wl.op == "conv_transpose3d":
             return tc.conv_transpose3d_fwd(x, w, b, output_padding=wl.output_padding, **kw)
         if wl.op == "conv_maxpool_lse_relu":
@@ -238,8 +245,18 @@ def run_ours(args):
     # library launches per call: weight pack + engine (+ the transposed
     # conv's bias slab fill; + BatchNorm finalize and apply for batch
     # statistics; + the running-statistics affine for evaluation mode)
-    launches_per_call = {"conv3d": 2, "conv_transpose3d": 3, "conv_maxpool_lse_relu": 2,
-                         "convT_bn_avgpool": 4, "convT_bneval_avgpool": 3}
+    # (the convT_bneval path: finalize + pack + pooled conv; grouped convs
+    # with few channels per group: one direct launch; channels-last through
+    # the engine: transpose + pack + engine + transpose)
+    def launches(wl):
+        if wl.op in ("conv3d", "conv3d_ndhwc"):
+            pl = tc.plan_describe(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
+                                  wl.dilation, wl.output_padding, wl.groups)
+            if pl.get("direct"):
+                return 1
+            return 4 if wl.op == "conv3d_ndhwc" else 2
+        return {"conv_transpose3d": 3, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 4,
+                "convT_bneval_avgpool": 3}[wl.op]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = {wl.name: [] for wl in wls}
@@ -330,7 +347,7 @@ def run_ours(args):
     d2h = 0
     for wl in wls:
         pinned_in[wl.name] = tuple(None if a is None else torch.from_numpy(a).pin_memory()
-                                   for a in host[wl.name])
+                                   for a in host_call[wl.name])
         pinned_out[wl.name] = torch.empty(W.y_shape(wl), dtype=torch.float32).pin_memory()
         h2d += sum(a.numel() * 4 for a in pinned_in[wl.name] if a is not None)
         d2h += pinned_out[wl.name].numel() * 4
@@ -378,7 +395,7 @@ def run_ours(args):
         "e2e": {"value": round(world * total_flops / (e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * sum(launches_per_call[wl.op] for wl in wls),
+        "gpu_launches": args.steps * sum(launches(wl) for wl in wls),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -269,7 +269,7 @@ def test_plans_of_workloads(lib):
     """Structural facts of the five workloads' plans."""
     from transposed_conv_epilogues_gb300.workloads import BY_NAME
     ops = {"conv3d": 0, "conv_transpose3d": 1, "conv_maxpool_lse_relu": 2, "convT_bn_avgpool": 3,
-           "convT_bneval_avgpool": 4}
+           "convT_bneval_avgpool": 4, "conv3d_ndhwc": 5}
 
     def plan(n):
         wl = BY_NAME[n]
@@ -286,3 +286,7 @@ def test_plans_of_workloads(lib):
     for n in BY_NAME:
         pl = plan(n)
         assert pl["status"] == 0 and pl["smem_bytes"] <= 227 * 1024
+    # grouped / channels-last workloads: depthwise in the direct kernel, the
+    # dense channels-last conv through the engine
+    assert plan("dwconv_k3")["direct"] == 1 and plan("dwconv_k3_ndhwc")["direct"] == 1
+    assert plan("conv_k3_ndhwc")["direct"] == 0 and plan("conv_k3_ndhwc")["ndhwc"] == 1

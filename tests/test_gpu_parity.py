@@ -256,6 +256,12 @@ DIRECT_CASES = [
     ((2, 4, 8, 6, 11), (4, 2, 2, 3, 3), 1, (0, 1, 2), (1, 1, 2), 2),    # dilation 2 on x
     ((1, 9, 5, 6, 23), (9, 3, 1, 3, 7), (2, 1, 2), (0, 1, 3), (1, 2, 2), 3),  # 7 taps, s2 d2
     ((3, 4, 4, 5, 6), (8, 1, 3, 1, 2), 1, 1, 1, 4),                    # ragged, k2 = 2
+    # the shared-memory tiled form (one input channel per group): a 3x3 filter
+    # plane unrolled, stride 2 along x, a channel multiplier of 2, several
+    # y/x tiles and output-plane chunks
+    ((2, 4, 9, 40, 70), (4, 1, 3, 3, 3), 1, 1, 1, 4),
+    ((1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3),
+    ((2, 2, 6, 33, 66), (2, 1, 3, 5, 2), 1, (1, 2, 0), (1, 1, 2), 2),
 ]
 
 
@@ -457,6 +463,25 @@ def test_workload_convT_bneval_avgpool_sampled(tc):
     idx = np.concatenate([idx, [0, flat.size - 1]])
     ref = orc.convT_bneval_avgpool_at(x, w, b, rm, rv, idx, g, be, wl.eps, **wl.kwargs())
     check(flat[idx], ref, wl.name + " eval")
+
+
+@pytest.mark.parametrize("name", ["dwconv_k3", "dwconv_k3_ndhwc", "conv_k3_ndhwc"])
+def test_workload_grouped_and_channels_last_sampled(tc, name):
+    """The depthwise conv (direct kernel) in both layouts and the dense
+    channels-last conv (engine between layout transposes) at full size,
+    sampled outputs against the oracle."""
+    wl, x, w, b = _wl(name)
+    kw = dict(stride=wl.stride, padding=wl.padding, dilation=wl.dilation, groups=wl.groups)
+    if wl.op == "conv3d_ndhwc":
+        y = tc.conv3d_fwd_ndhwc(_dev(np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))), _dev(w),
+                                _dev(b), **kw).cpu().numpy()
+        y = y.transpose(0, 4, 1, 2, 3)  # compare in NCDHW order
+    else:
+        y = tc.conv3d_fwd(_dev(x), _dev(w), _dev(b), **kw).cpu().numpy()
+    flat = np.ascontiguousarray(y).ravel()
+    idx = inputs.sample_indices(606 + wl.index, flat.size, 20000)
+    idx = np.concatenate([idx, [0, flat.size - 1]])
+    check(flat[idx], orc.conv3d_at(x, w, b, idx, **kw), name)
 
 
 def test_workload_conv_maxpool_lse_relu_sampled(tc):

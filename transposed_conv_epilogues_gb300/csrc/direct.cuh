@@ -34,6 +34,16 @@ inline bool direct_eligible(int cin_g, int cout_g, int s2, int d2, int k2) {
          k2 <= kDirectMaxK2;
 }
 
+// Shared-memory tiled form (NCDHW, one input channel per group, stride and
+// dilation 1 along axis 0): a CTA of 128 threads computes a kTileY x 64
+// output tile over a chunk of output planes, for every output channel of a
+// group, each thread a 4 x 4 block (y, x); a ring of k0 + 1 input planes
+// (W1 rows x W2p columns) must fit kTiledSmemFloats.
+constexpr int kTileY = 32;
+constexpr int kTiledSmemFloats = 11 * 1024;
+// slab extents of the tiled form for a conv, or false when it does not apply
+bool direct_tiled_geometry(const DirectParams& p, int* W1, int* W2p);
+
 cudaError_t direct_conv_launch(const DirectParams& p, bool ndhwc, int sm_count, cudaStream_t st);
 
 // Layout transposes of an [N][A][B] float array to [N][B][A] (A, B >= 1):

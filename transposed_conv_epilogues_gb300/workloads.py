@@ -37,8 +37,10 @@ from . import inputs
 class Workload:
     index: int
     name: str
-    op: str  # "conv3d" | "conv_transpose3d" | "convT_bn_avgpool" | "convT_bneval_avgpool"
-    #          | "conv_maxpool_lse_relu"
+    op: str  # "conv3d" | "conv3d_ndhwc" | "conv_transpose3d" | "convT_bn_avgpool"
+    #          | "convT_bneval_avgpool" | "conv_maxpool_lse_relu"
+    # x_shape / w_shape are NCDHW / PyTorch layouts; a "conv3d_ndhwc" workload
+    # feeds x and reads y channels-last
     x_shape: tuple
     w_shape: tuple
     bias: bool
@@ -114,7 +116,10 @@ WORKLOADS = [
 # 128), which makes the GEMM K 3456, and the transposed-conv + BN + pool
 # pipeline of "Kimi-K2.6 l2_p72" with BatchNorm in evaluation mode (running
 # statistics, as that page's first fused kernel reads them) at the same shape.
-# Seeds follow the same rule (i = 6, 7, 8).
+# Seeds follow the same rule (i = 6, 7, 8).  Then grouped and channels-last
+# convs (the direct kernel and the layout route, i = 9, 10, 11): a depthwise
+# k3 conv on [8,64,32,64,64] in NCDHW and in NDHWC, and a dense k3 conv
+# 32 -> 64 on [4,32,32,64,64] in NDHWC (fan_in: Cin/G * 27).
 EXTRA_WORKLOADS = [
     Workload(6, "conv331_p1", "conv3d", (16, 3, 256, 256, 10), (64, 3, 3, 3, 1), True,
              fan_in=3 * 9, desc="Conv3d (3,3,1) 3->64 at the page's original shape"),
@@ -125,6 +130,13 @@ EXTRA_WORKLOADS = [
     Workload(8, "convT_bneval_avgpool", "convT_bneval_avgpool", (64, 3, 32, 32, 32),
              (3, 16, 3, 3, 3), True, stride=(2, 2, 2), padding=(1, 1, 1), fan_in=16 * 27,
              desc="ConvTranspose3d 3->16 k3 s2 p1 + BN(running stats) + AvgPool3d(2) x2"),
+    Workload(9, "dwconv_k3", "conv3d", (8, 64, 32, 64, 64), (64, 1, 3, 3, 3), True,
+             padding=(1, 1, 1), groups=64, fan_in=27, desc="depthwise Conv3d k3 p1, 64 channels"),
+    Workload(10, "dwconv_k3_ndhwc", "conv3d_ndhwc", (8, 64, 32, 64, 64), (64, 1, 3, 3, 3), True,
+             padding=(1, 1, 1), groups=64, fan_in=27,
+             desc="depthwise Conv3d k3 p1, 64 channels, channels-last"),
+    Workload(11, "conv_k3_ndhwc", "conv3d_ndhwc", (4, 32, 32, 64, 64), (64, 32, 3, 3, 3), True,
+             padding=(1, 1, 1), fan_in=32 * 27, desc="Conv3d 32->64 k3 p1, channels-last"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
@@ -185,6 +197,8 @@ def y_shape(wl: Workload):
         return (N, 1) + tuple(o // 2 for o in O)
     if wl.op in ("convT_bn_avgpool", "convT_bneval_avgpool"):
         return (N, wl.cout) + tuple(o // 2 // 2 for o in O)
+    if wl.op == "conv3d_ndhwc":
+        return (N,) + O + (wl.cout,)
     return (N, wl.cout) + O
 
 
