@@ -274,7 +274,7 @@ def test_direct_grouped_conv(tc, case):
     check(y, orc.conv3d(x, w, b, s, p, d, G), f"direct {case}")
 
 
-NDHWC_CASES = DIRECT_CASES[:3] + [
+NDHWC_CASES = DIRECT_CASES[:3] + DIRECT_CASES[5:7] + [
     # not for the direct kernel: through the engine with layout transposes
     ((2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1, 1, 1),
     ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1),           # (k,k,1): merged form

@@ -341,6 +341,87 @@ bool direct_tiled_geometry(const DirectParams& p, int* W1, int* W2p) {
   return true;
 }
 
+// Channels-last form for 3 x 3 (y, x) filters with stride and dilation 1
+// along y: a thread owns one output channel and a 4 x 4 (y, x) block at one
+// (n, o0); items are ordered with the output channel fastest, so the lanes
+// of a warp read and write consecutive channels.  Each input row segment
+// (the 4 + 2 columns the block needs, stride C apart) feeds every output row
+// that reads it.
+template <int S2>
+__global__ void __launch_bounds__(256, 2) direct_ndhwc_k3_kernel(const __grid_constant__ DirectParams p,
+                                                              int nyb) {
+  constexpr int R = kDirectRun, RY = 4;
+  constexpr int NS = (R - 1) * S2 + 3;  // segment columns
+  const long long items = (long long)p.N * p.O[0] * nyb * p.nrun2 * p.Cout;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (long long)gridDim.x * blockDim.x) {
+    long long q = it;
+    const int oc = (int)(q % p.Cout);
+    q /= p.Cout;
+    const int r2 = (int)(q % p.nrun2);
+    q /= p.nrun2;
+    const int yb = (int)(q % nyb);
+    q /= nyb;
+    const int o0 = (int)(q % p.O[0]);
+    const int n = (int)(q / p.O[0]);
+    const int ic0 = (oc / p.cout_g) * p.cin_g;
+    const int o2s = r2 * R, o1s = yb * RY;
+    const int x2s = o2s * S2 - p.p[2], y1s = o1s - p.p[1];
+    const float bv = p.bias ? __ldg(p.bias + oc) : 0.f;
+    float acc[RY][R];
+#pragma unroll
+    for (int a = 0; a < RY; ++a)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[a][r] = bv;
+    const int kv = p.k[0] * 9;
+    for (int ci = 0; ci < p.cin_g; ++ci) {
+      const int ic = ic0 + ci;
+      for (int k0 = 0; k0 < p.k[0]; ++k0) {
+        const int z = o0 * p.s[0] - p.p[0] + k0 * p.d[0];
+        if ((unsigned)z >= (unsigned)p.S[0]) continue;
+        const float* wk = p.w + ((long long)oc * p.cin_g + ci) * kv + k0 * 9;
+        float wr[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) wr[i] = __ldg(wk + i);
+        const float* zp = p.x + ((long long)n * p.S[0] + z) * p.S[1] * p.S[2] * p.C + ic;
+        float seg[RY + 2][NS];
+#pragma unroll
+        for (int r = 0; r < RY + 2; ++r) {
+          const int yi = y1s + r;
+          const bool rok = (unsigned)yi < (unsigned)p.S[1];
+          const float* rowp = zp + (long long)yi * p.S[2] * p.C;
+#pragma unroll
+          for (int j = 0; j < NS; ++j) {
+            const int xi = x2s + j;
+            seg[r][j] = (rok && (unsigned)xi < (unsigned)p.S[2]) ? __ldg(rowp + (long long)xi * p.C)
+                                                                 : 0.f;
+          }
+        }
+#pragma unroll
+        for (int k1 = 0; k1 < 3; ++k1)
+#pragma unroll
+          for (int k2 = 0; k2 < 3; ++k2) {
+            const float wv = wr[k1 * 3 + k2];
+#pragma unroll
+            for (int a = 0; a < RY; ++a)
+#pragma unroll
+              for (int rx = 0; rx < R; ++rx)
+                acc[a][rx] = fmaf(wv, seg[a + k1][rx * S2 + k2], acc[a][rx]);
+          }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < RY; ++a) {
+      const int yo1 = o1s + a;
+      if (yo1 >= p.O[1]) break;
+      float* yrow = p.y + (((long long)n * p.O[0] + o0) * p.O[1] + yo1) * p.O[2] * p.Cout + oc;
+#pragma unroll
+      for (int rx = 0; rx < R; ++rx)
+        if (o2s + rx < p.O[2]) yrow[(long long)(o2s + rx) * p.Cout] = acc[a][rx];
+    }
+  }
+}
+
 template <bool NDHWC>
 static cudaError_t launch_layout(const DirectParams& p, unsigned blocks, cudaStream_t st) {
   const int s2 = p.s[2], d2 = p.d[2];
@@ -381,6 +462,16 @@ cudaError_t direct_conv_launch(const DirectParams& p, bool ndhwc, int sm_count, 
       }
       return cudaGetLastError();
     }
+  }
+  if (ndhwc && p.k[1] == 3 && p.k[2] == 3 && p.s[1] == 1 && p.d[1] == 1 && p.d[2] == 1) {
+    const int nyb = (p.O[1] + 3) / 4;
+    const long long items = (long long)p.N * p.O[0] * nyb * p.nrun2 * p.Cout;
+    long long blocks = (items + 255) / 256;
+    if (blocks > 8LL * sm_count) blocks = 8LL * sm_count;
+    if (blocks < 1) blocks = 1;
+    if (p.s[2] == 1) direct_ndhwc_k3_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(p, nyb);
+    else direct_ndhwc_k3_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(p, nyb);
+    return cudaGetLastError();
   }
   // persistent grid: 8 CTAs of 256 threads per SM, fewer for small problems
   long long blocks = (p.items + 255) / 256;
