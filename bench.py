@@ -51,6 +51,18 @@ def peaks():
         return 6800.0, 1900.0 * TF32_OVER_BF16 / 3.0, "fallback"
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise max of a list of floats over the ranks of the process
+    group (identity on one rank): each rank's time reduced to the job's."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -299,14 +311,11 @@ def run_ours(args):
     per = {}
     step_ms = 0.0
     total_flops = 0.0
-    for wl in wls:
+    # mean event time per workload, then the max over ranks
+    mean_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in ev[wl.name]) / len(ev[wl.name])
+                              for wl in wls], world, dev)
+    for wl, ms in zip(wls, mean_ms):
         ts = [a.elapsed_time(b) for a, b in ev[wl.name]]
-        ms = sum(ts) / len(ts)
-        # max over ranks
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
         fl = 2.0 * W.valid_macs(wl)
         by = W.algorithmic_bytes(wl)
         t_tc = fl / (tf_peak * 1e12)
@@ -370,11 +379,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks([statistics.mean(e2e_ms)], world, dev)[0]
 
     line = {
         "metric": "effective TFLOP/s (2 x valid MACs / device time), fp32-accurate (1e-4 vs "
