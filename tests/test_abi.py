@@ -187,6 +187,16 @@ def test_direct_and_ndhwc_plans(lib):
     assert tc.workspace_bytes(5, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
 
 
+def test_ndhwc_transpose_route_limits(lib):
+    """The channels-last route through the engine transposes with batch in
+    the grid's y dimension: a batch above 65535 is rejected on the host."""
+    with pytest.raises(tc.Tc3dError) as e:
+        tc.workspace_bytes(5, (70000, 5, 4, 4, 4), (7, 5, 3, 3, 3), 1, 1)
+    assert e.value.status == tc.TC3D_ERR_UNSUPPORTED
+    # the direct kernel (few channels per group) has no such limit
+    assert tc.workspace_bytes(5, (70000, 8, 4, 4, 4), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
+
+
 def test_ndhwc_argument_errors(lib):
     fn = lib.tc3d_conv3d_fwd_ndhwc
     P = ctypes.c_void_p

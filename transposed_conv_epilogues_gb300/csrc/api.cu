@@ -373,6 +373,12 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
     cp->ws_total = 256;  // nothing is staged
   } else if (cp->ndhwc) {
     // channels-last through the engine: x and y transposed to NCDHW copies
+    // (the transpose grid: batch in y, 32 x 32 tiles in x)
+    const int64_t sv = (int64_t)pb.S[0] * pb.S[1] * pb.S[2];
+    const int64_t ov = cp->pl.O[0] * cp->pl.O[1] * cp->pl.O[2];
+    auto tiles = [](int64_t a, int64_t b) { return ((a + 31) / 32) * ((b + 31) / 32); };
+    if (pb.N > 65535 || tiles(sv, pb.Cin) > INT32_MAX || tiles(pb.Cout, ov) > INT32_MAX)
+      return TC3D_ERR_UNSUPPORTED;
     const int64_t xs = (int64_t)pb.N * pb.Cin * pb.S[0] * pb.S[1] * pb.S[2] * 4;
     cp->ws_xt_off = (cp->ws_total + 255) / 256 * 256;
     cp->ws_yt_off = (cp->ws_xt_off + xs + 255) / 256 * 256;

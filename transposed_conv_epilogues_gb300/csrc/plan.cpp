@@ -18,6 +18,7 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 
 #include "../../include/tc3d.h"
@@ -665,6 +666,10 @@ int make_pool_plan(const Plan& bn, PoolPlan* out) {
     pp.box_Tn[b] = (int)std::max<int64_t>(
         1, std::min<int64_t>({(int64_t)(pb.N + 7) / 8,
                               kGramSlabFloats / (planes * pp.box_W1[b] * W2p)}));
+    // the kernel decodes unit indices in 32 bits
+    const int64_t units = ceil_div(pb.N, pp.box_Tn[b]) * ext[a0] *
+                          ceil_div(ext[a1], pp.box_T1[b]) * ceil_div(ext[a2], T2);
+    if (units > INT32_MAX) return pp.status;
   }
 
   // pooled conv: window z = 4q + j reads input 2q + e, e = (j + p - d k)/2
