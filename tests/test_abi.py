@@ -187,6 +187,44 @@ def test_direct_and_ndhwc_plans(lib):
     assert tc.workspace_bytes(5, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
 
 
+def test_direct_forms(lib):
+    """Which direct kernel a conv takes: 0 the general one, 1 the NCDHW
+    shared-memory tiled one, 2 the channels-last register-blocked 3 x 3 one,
+    3 the channels-last streaming one (one input channel per group, a
+    multiplier dividing 32, k0 <= 3 at stride 1, a 3 x 3 (y, x) plane), 4 the
+    NCDHW streaming one (one input channel per group, a 3 x 3 x 3 filter,
+    stride 1 along z and y)."""
+    def form(op, xs, ws, s, p, d, G):
+        pl = tc.plan_describe(op, xs, ws, s, p, d, 0, G)
+        assert pl["direct"] == 1
+        return pl["direct_form"]
+    dw = ((2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 8)
+    assert form(0, *dw) == 4 and form(5, *dw) == 3
+    assert form(0, (1, 3, 7, 37, 136), (6, 1, 3, 3, 3), (1, 1, 2), (1, 1, 2), 1, 3) == 4
+    # NCDHW, k0 = 1 or 2, or a 5-row filter: the tiled kernel
+    assert form(0, (1, 3, 7, 35, 133), (6, 1, 1, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3) == 1
+    assert form(0, (2, 4, 9, 40, 70), (4, 1, 2, 3, 3), 1, 1, 1, 4) == 1
+    assert form(0, (2, 2, 6, 33, 66), (2, 1, 3, 5, 2), 1, (1, 2, 0), (1, 1, 2), 2) == 1
+    # k0 = 2 at stride 2 along x: its ring of 3 planes is over the tiled
+    # kernel's shared-memory budget -> the general kernel
+    assert form(0, (1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3) == 0
+    # stride 2 along x, a channel multiplier of 2, k0 = 2 / 1
+    assert form(5, (1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3) == 3
+    assert form(5, (2, 36, 6, 7, 9), (36, 1, 1, 3, 3), 1, (0, 1, 0), 1, 36) == 3
+    assert form(5, (1, 6, 11, 5, 6), (96, 1, 3, 3, 3), 1, 1, 1, 6) == 3      # multiplier 16
+    # not streaming: two input channels per group, stride 2 along z, k0 = 4,
+    # a multiplier of 3 -> the register-blocked 3 x 3 kernel
+    assert form(5, (2, 8, 6, 9, 11), (8, 2, 3, 3, 3), 1, 1, 1, 4) == 2
+    assert form(5, (1, 6, 9, 8, 10), (6, 1, 3, 3, 3), (2, 1, 1), 1, 1, 6) == 2
+    assert form(5, (1, 4, 9, 8, 10), (4, 1, 4, 3, 3), 1, 1, 1, 4) == 2
+    assert form(5, (1, 4, 9, 8, 10), (12, 1, 3, 3, 3), 1, 1, 1, 4) == 2
+    # a 5-tap x extent or dilation 2 along x -> the general kernel
+    assert form(5, (1, 6, 7, 9, 17), (12, 1, 3, 3, 5), (1, 2, 2), (1, 0, 2), 1, 6) == 0
+    assert form(5, (2, 4, 8, 6, 11), (4, 2, 2, 3, 3), 1, (0, 1, 2), (1, 1, 2), 2) == 0
+    assert form(0, (1, 9, 5, 6, 23), (9, 3, 1, 3, 7), (2, 1, 2), (0, 1, 3), (1, 2, 2), 3) == 0
+    assert tc.plan_describe(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)["direct_form"] == -1
+
+
 def test_ndhwc_transpose_route_limits(lib):
     """The channels-last route through the engine transposes with batch in
     the grid's y dimension: a batch above 65535 is rejected on the host."""

@@ -256,12 +256,21 @@ DIRECT_CASES = [
     ((2, 4, 8, 6, 11), (4, 2, 2, 3, 3), 1, (0, 1, 2), (1, 1, 2), 2),    # dilation 2 on x
     ((1, 9, 5, 6, 23), (9, 3, 1, 3, 7), (2, 1, 2), (0, 1, 3), (1, 2, 2), 3),  # 7 taps, s2 d2
     ((3, 4, 4, 5, 6), (8, 1, 3, 1, 2), 1, 1, 1, 4),                    # ragged, k2 = 2
-    # the shared-memory tiled form (one input channel per group): a 3x3 filter
-    # plane unrolled, stride 2 along x, a channel multiplier of 2, several
-    # y/x tiles and output-plane chunks
+    # the NCDHW streaming form (3 x 3 x 3), 4-byte copies: several y / x
+    # tiles and output-plane chunks
     ((2, 4, 9, 40, 70), (4, 1, 3, 3, 3), 1, 1, 1, 4),
-    ((1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3),
+    # the shared-memory tiled form (one input channel per group): a 3x3 filter
+    # plane unrolled with k0 = 1 and stride 2 along x (a channel multiplier
+    # of 2) and with k0 = 2; a 5 x 2 plane at dilation 2 along x
+    ((1, 3, 7, 35, 133), (6, 1, 1, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3),
+    ((2, 4, 9, 40, 70), (4, 1, 2, 3, 3), 1, 1, 1, 4),
     ((2, 2, 6, 33, 66), (2, 1, 3, 5, 2), 1, (1, 2, 0), (1, 1, 2), 2),
+    # the NCDHW streaming form with 16-byte copies (rows a multiple of 4
+    # floats), the window starting 2, 0 and 1 columns into its first piece;
+    # stride 2 along x with a channel multiplier of 2; several x and y tiles
+    ((1, 3, 7, 37, 136), (6, 1, 3, 3, 3), (1, 1, 2), (1, 1, 2), 1, 3),
+    ((1, 4, 6, 34, 68), (4, 1, 3, 3, 3), 1, (0, 1, 0), 1, 4),
+    ((2, 2, 5, 9, 72), (2, 1, 3, 3, 3), 1, (2, 1, 3), 1, 2),
 ]
 
 
@@ -274,11 +283,25 @@ def test_direct_grouped_conv(tc, case):
     check(y, orc.conv3d(x, w, b, s, p, d, G), f"direct {case}")
 
 
-NDHWC_CASES = DIRECT_CASES[:3] + DIRECT_CASES[5:7] + [
+NDHWC_CASES = DIRECT_CASES[:3] + DIRECT_CASES[5:6] + [
+    ((1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3),
     # not for the direct kernel: through the engine with layout transposes
     ((2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1, 1, 1),
     ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1),           # (k,k,1): merged form
     ((1, 8, 6, 7, 9), (12, 4, 3, 2, 3), (1, 2, 1), 1, 1, 2),
+    # the streaming form: ragged 32-channel blocks with a multiplier of 2,
+    # pad 2 along z and stride 2 along x; k0 = 1; a multiplier of 16 and a
+    # channel count that is not a multiple of 4 (4-byte copies); several
+    # output-plane chunks of 9 planes (9, 9, 7)
+    ((1, 40, 5, 9, 18), (80, 1, 3, 3, 3), (1, 1, 2), (2, 1, 1), 1, 40),
+    ((2, 36, 6, 7, 9), (36, 1, 1, 3, 3), 1, (0, 1, 0), 1, 36),
+    ((1, 6, 11, 5, 6), (96, 1, 3, 3, 3), 1, 1, 1, 6),
+    ((2, 6, 8, 21, 19), (6, 1, 3, 3, 3), 1, 1, 1, 6),
+    ((2, 64, 25, 40, 64), (64, 1, 3, 3, 3), 1, 1, 1, 64),
+    # the register-blocked 3 x 3 kernel: two input channels per group, and
+    # stride 2 along z
+    ((2, 8, 6, 9, 11), (8, 2, 3, 3, 3), 1, 1, 1, 4),
+    ((1, 6, 9, 8, 10), (6, 1, 3, 3, 3), (2, 1, 1), 1, 1, 6),
 ]
 
 
@@ -290,6 +313,45 @@ def test_conv3d_ndhwc(tc, case):
     y = tc.conv3d_fwd_ndhwc(_dev(x_cl), _dev(w), _dev(b), s, p, d, G).cpu().numpy()
     ref = orc.conv3d(x, w, b, s, p, d, G).transpose(0, 2, 3, 4, 1)
     check(y, ref, f"ndhwc {case}")
+
+
+def test_conv3d_ndhwc_stream_chunks(tc):
+    """The streaming form splits the (2, 64, 25, 40, 64) depthwise conv into
+    output-plane chunks of 9, 9 and 7 planes on a 152-SM GB300; each chunk
+    walks its planes plus a 2-plane halo."""
+    xs, ws = (2, 64, 25, 40, 64), (64, 1, 3, 3, 3)
+    assert tc.plan_describe(5, xs, ws, 1, 1, 1, 0, 64)["direct_form"] == 3
+    x, w, b = make(xs, ws, 64, True, seed=74)
+    x_cl = np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))
+    y = tc.conv3d_fwd_ndhwc(_dev(x_cl), _dev(w), _dev(b), 1, 1, 1, 64).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, 1, 1, 1, 64).transpose(0, 2, 3, 4, 1), "ndhwc stream chunks")
+
+
+def test_direct_stream_misaligned(tc):
+    """NCDHW x 4 bytes past a 16-byte boundary: the streaming form copies
+    with 4-byte pieces."""
+    xs, ws = (2, 4, 6, 9, 64), (4, 1, 3, 3, 3)
+    x, w, b = make(xs, ws, 4, True, seed=76)
+    buf = torch.zeros(x.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(x.ravel()).cuda()
+    xv = buf[1:].view(xs)
+    assert xv.data_ptr() % 16 != 0
+    y = tc.conv3d_fwd(xv, _dev(w), _dev(b), 1, 1, 1, 4).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, 1, 1, 1, 4), "direct stream misaligned")
+
+
+def test_conv3d_ndhwc_stream_misaligned(tc):
+    """x 4 bytes past a 16-byte boundary: the streaming form copies with
+    4-byte pieces."""
+    xs, ws = (2, 32, 7, 9, 20), (32, 1, 3, 3, 3)
+    x, w, b = make(xs, ws, 32, True, seed=75)
+    x_cl = np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))
+    buf = torch.zeros(x_cl.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(x_cl.ravel()).cuda()
+    xv = buf[1:].view(x_cl.shape)
+    assert xv.data_ptr() % 16 != 0
+    y = tc.conv3d_fwd_ndhwc(xv, _dev(w), _dev(b), 1, 1, 1, 32).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, 1, 1, 1, 32).transpose(0, 2, 3, 4, 1), "ndhwc stream misaligned")
 
 
 # --------------------------------------------------------------------------

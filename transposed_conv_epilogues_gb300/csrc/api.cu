@@ -38,6 +38,7 @@ struct DeviceState {
   int* err = nullptr;  // device address of the error word
   bool smem_set[4] = {false, false, false, false};  // per kernel id
   bool gram_smem_set = false;
+  bool direct_smem_set = false;
   // auxiliary stream for the bias slab fill, which runs beside the engine
   // (fork / join through two events; calls that use it are serialised by
   // g_fork_mu while they enqueue)
@@ -387,18 +388,12 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
   return TC3D_OK;
 }
 
-// The direct conv kernel (grouped convs with few channels per group; NCDHW
-// or channels-last)
-int run_direct(const CallPlan& cp, const float* x, const float* w, const float* bias, float* y,
-               DeviceState* d, cudaStream_t st) {
+// The direct kernel's parameters for a planned call (data pointers null)
+DirectParams direct_params(const CallPlan& cp) {
   const Plan& pl = cp.pl;
   const Problem& pb = cp.upb;
   DirectParams dp;
   std::memset(&dp, 0, sizeof(dp));
-  dp.x = x;
-  dp.w = w;
-  dp.bias = bias;
-  dp.y = y;
   dp.N = pb.N;
   dp.C = pb.Cin;
   dp.Cout = pb.Cout;
@@ -414,6 +409,25 @@ int run_direct(const CallPlan& cp, const float* x, const float* w, const float* 
   }
   dp.nrun2 = (dp.O[2] + kDirectRun - 1) / kDirectRun;
   dp.items = (long long)pb.N * pb.Cout * dp.O[0] * dp.O[1] * dp.nrun2;
+  return dp;
+}
+
+// The direct conv kernel (grouped convs with few channels per group; NCDHW
+// or channels-last)
+int run_direct(const CallPlan& cp, const float* x, const float* w, const float* bias, float* y,
+               DeviceState* d, cudaStream_t st) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!d->direct_smem_set) {
+      if (direct_set_smem() != cudaSuccess) return TC3D_ERR_CUDA;
+      d->direct_smem_set = true;
+    }
+  }
+  DirectParams dp = direct_params(cp);
+  dp.x = x;
+  dp.w = w;
+  dp.bias = bias;
+  dp.y = y;
   return direct_conv_launch(dp, cp.ndhwc, d->sm_count, st) == cudaSuccess ? TC3D_OK
                                                                          : TC3D_ERR_CUDA;
 }
@@ -859,6 +873,8 @@ int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout,
     if (pl.status == TC3D_OK && (op == OP_CONV || op == OP_CONV_NDHWC)) {
       s.pop_back();
       append(s, ", \"direct\": %lld", cp.direct ? 1 : 0);
+      append(s, ", \"direct_form\": %lld",
+             cp.direct ? (long long)direct_form(direct_params(cp), cp.ndhwc) : -1LL);
       append(s, ", \"ndhwc\": %lld", cp.ndhwc ? 1 : 0);
       s += "}";
     }

@@ -44,6 +44,31 @@ constexpr int kTiledSmemFloats = 11 * 1024;
 // slab extents of the tiled form for a conv, or false when it does not apply
 bool direct_tiled_geometry(const DirectParams& p, int* W1, int* W2p);
 
+// Channels-last streaming form: one input channel per group and a channel
+// multiplier (cout_g) that divides 32; k0 <= 3 with stride and dilation 1
+// along axis 0; a 3 x 3 (y, x) filter plane with stride and dilation 1 along
+// y and dilation 1 along x.
+inline bool ndhwc_stream_eligible(const DirectParams& p) {
+  return p.cin_g == 1 && (32 % p.cout_g) == 0 && p.k[0] >= 1 && p.k[0] <= 3 && p.s[0] == 1 &&
+         p.d[0] == 1 &&
+         p.k[1] == 3 && p.k[2] == 3 && p.s[1] == 1 && p.d[1] == 1 && p.d[2] == 1 &&
+         (p.s[2] == 1 || p.s[2] == 2);
+}
+
+// The direct kernel a conv takes (the layout flag: channels-last)
+enum DirectForm {
+  kDirectGeneral = 0,
+  kDirectTiled = 1,
+  kDirectNdhwcK3 = 2,
+  kDirectNdhwcStream = 3,
+  kDirectTiledStream = 4
+};
+int direct_form(const DirectParams& p, bool ndhwc);
+
+// Opts the streaming form's kernels into their shared-memory size (once per
+// device, before the first direct_conv_launch).
+cudaError_t direct_set_smem();
+
 cudaError_t direct_conv_launch(const DirectParams& p, bool ndhwc, int sm_count, cudaStream_t st);
 
 // Layout transposes of an [N][A][B] float array to [N][B][A] (A, B >= 1):
