@@ -223,6 +223,10 @@ def test_direct_forms(lib):
     assert form(5, (2, 4, 8, 6, 11), (4, 2, 2, 3, 3), 1, (0, 1, 2), (1, 1, 2), 2) == 0
     assert form(0, (1, 9, 5, 6, 23), (9, 3, 1, 3, 7), (2, 1, 2), (0, 1, 3), (1, 2, 2), 3) == 0
     assert tc.plan_describe(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)["direct_form"] == -1
+    # the NCDHW streaming and tiled grids put (n, channel) in grid z: above
+    # 65535 pairs -> the general kernel (persistent, no such limit)
+    assert form(0, (1023, 64, 3, 4, 4), (64, 1, 3, 3, 3), 1, 1, 1, 64) == 4
+    assert form(0, (1024, 64, 3, 4, 4), (64, 1, 3, 3, 3), 1, 1, 1, 64) == 0
 
 
 def test_ndhwc_transpose_route_limits(lib):
