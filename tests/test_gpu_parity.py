@@ -158,6 +158,14 @@ BN_CASES = [
     ((3, 2, 6, 5, 9), (2, 3, 2, 4, 3), 2, (0, 1, 1), 1, (1, 0, 0), 1, False),
     ((2, 3, 9, 5, 6), (3, 4, 3, 3, 3), (1, 2, 2), 1, 1, 0, 1, True),  # unfused: stride 1 axis
     ((2, 3, 6, 6, 6), (3, 4, 3, 3, 3), 2, 1, 2, 0, 1, True),          # unfused: dilation 2
+    # batch statistics in lag form (at most 3 channels, one or two consecutive
+    # offsets per axis, axis-2 rows a multiple of 4 floats) + the pooled conv
+    # on CUDA cores; the workload's form is the first BN case above
+    ((2, 2, 9, 7, 12), (2, 4, 3, 3, 3), 2, 0, 1, 0, 1, True),         # offsets {-1, 0}
+    ((1, 3, 5, 6, 36), (3, 3, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # two column blocks
+    ((2, 1, 9, 10, 8), (1, 4, 2, 3, 1), 2, (0, 1, 0), 1, (1, 1, 1), 1, True),  # one offset on x
+    ((3, 2, 6, 17, 4), (2, 3, 3, 2, 3), 2, (1, 0, 1), 1, 0, 1, False),  # ragged row block
+    ((5, 3, 12, 40, 16), (3, 24, 3, 3, 3), 2, 1, 1, 0, 1, True),      # 24 channels, 5 row blocks
 ]
 
 
@@ -391,6 +399,36 @@ def test_deterministic_repeat(tc):
     c1 = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), 1, 1)
     c2 = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), 1, 1)
     assert torch.equal(c1, c2)
+
+
+def test_fill_stream_does_not_couple_callers(tc):
+    """A transposed conv forks its bias slab fill onto an auxiliary stream of
+    its caller's stream.  Work another caller queued on another stream must
+    not hold it up: stream B sleeps (a bounded spin kernel) before its own
+    transposed conv; the call on stream A, queued after it, still completes
+    while B sleeps."""
+    x, w, b = make((2, 6, 5, 7, 8), (6, 10, 3, 3, 3), 10)   # k3 s2 p1 d2: a bias slab
+    xd, wd, bd = _dev(x), _dev(w), _dev(b)
+    kw = dict(stride=2, padding=1, dilation=2)
+    ref = tc.conv_transpose3d_fwd(xd, wd, bd, **kw)
+    assert tc.plan_describe(tc.OP_CONV_TRANSPOSE3D, x.shape, w.shape, 2, 1, 2)["fill_slab"] == 1
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    ya, yb = torch.empty_like(ref), torch.empty_like(ref)
+    with torch.cuda.stream(sb):
+        torch.cuda._sleep(2_000_000_000)  # about a second at 2 GHz
+        tc.conv_transpose3d_fwd(xd, wd, bd, **kw, out=yb)
+        done_b = torch.cuda.Event()
+        done_b.record(sb)
+    with torch.cuda.stream(sa):
+        tc.conv_transpose3d_fwd(xd, wd, bd, **kw, out=ya)
+        done_a = torch.cuda.Event()
+        done_a.record(sa)
+    done_a.synchronize()
+    b_pending = not done_b.query()
+    torch.cuda.synchronize()
+    assert b_pending, "stream B finished first: the check could not tell"
+    assert torch.equal(ya, ref) and torch.equal(yb, ref)
 
 
 def test_cuda_graph_capture_replays(tc):

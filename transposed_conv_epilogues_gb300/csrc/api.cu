@@ -39,16 +39,45 @@ struct DeviceState {
   bool smem_set[4] = {false, false, false, false};  // per kernel id
   bool gram_smem_set = false;
   bool direct_smem_set = false;
-  // auxiliary stream for the bias slab fill, which runs beside the engine
-  // (fork / join through two events; calls that use it are serialised by
-  // g_fork_mu while they enqueue)
-  cudaStream_t aux = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  bool lag_smem_set = false;
+  // auxiliary streams for the bias slab fill, which runs beside the engine:
+  // one per caller stream (fork / join through two events of its own), so a
+  // fill never waits behind work another caller queued; calls enqueue under
+  // g_fork_mu
+  struct Aux {
+    cudaStream_t caller = nullptr;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+  };
+  static constexpr int kMaxAux = 32;
+  Aux aux[kMaxAux];
+  int n_aux = 0;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 std::mutex g_fork_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// The auxiliary stream and events of caller stream st (created on its first
+// use; nullptr once kMaxAux caller streams have one: the fill then runs on
+// st itself).  Call with g_fork_mu held.
+DeviceState::Aux* aux_for(DeviceState* d, cudaStream_t st) {
+  for (int i = 0; i < d->n_aux; ++i)
+    if (d->aux[i].caller == st) return &d->aux[i];
+  if (d->n_aux == DeviceState::kMaxAux) return nullptr;
+  DeviceState::Aux a;
+  a.caller = st;
+  if (cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();  // leave no error behind for the next launch check
+    if (a.aux) cudaStreamDestroy(a.aux);
+    if (a.fork) cudaEventDestroy(a.fork);
+    return nullptr;
+  }
+  d->aux[d->n_aux] = a;
+  return &d->aux[d->n_aux++];
+}
 
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -65,10 +94,6 @@ int device_state(DeviceState** out) {
     } else if (major != 10 || minor != 3) {
       d.status = TC3D_ERR_DEVICE;  // the kernels are built for sm_103a only
     } else if (error_flag_address(&d.err) != cudaSuccess) {
-      d.status = TC3D_ERR_CUDA;
-    } else if (cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking) != cudaSuccess ||
-               cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-               cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming) != cudaSuccess) {
       d.status = TC3D_ERR_CUDA;
     }
     if (!g_encode && d.status == TC3D_OK) {
@@ -247,6 +272,54 @@ void encode_xmap(const Plan& pl, const float* x, EngineParams* ep) {
   if (r == CUDA_SUCCESS) ep->use_tma = 1;
 }
 
+// Tensor map of the lag kernel: x as (S2, S1, S0, C, N), box 40 x 3 x 4 x C
+// x 1 (one warp's window rows of 4 consecutive planes).  False (the Gram kernel then takes the statistics) when x or its rows
+// break TMA's 16-byte rules.
+bool encode_lag_map(const Problem& pb, const float* x, LagParams* lp) {
+  std::memset(lp, 0, sizeof(*lp));
+  if (!g_encode || !aligned(x, 16) || (pb.S[2] % 4) != 0) return false;
+  cuuint64_t dims[5] = {(cuuint64_t)pb.S[2], (cuuint64_t)pb.S[1], (cuuint64_t)pb.S[0],
+                        (cuuint64_t)pb.Cin, (cuuint64_t)pb.N};
+  cuuint64_t strides[4];
+  strides[0] = (cuuint64_t)pb.S[2] * 4;
+  strides[1] = strides[0] * pb.S[1];
+  strides[2] = strides[1] * pb.S[0];
+  strides[3] = strides[2] * pb.Cin;
+  for (int i = 0; i < 4; ++i)
+    if (strides[i] >= (1ull << 40)) return false;
+  cuuint32_t box[5] = {(cuuint32_t)kLagBoxCols, (cuuint32_t)kLagBoxRows, (cuuint32_t)kLagChunk,
+                       (cuuint32_t)pb.Cin, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return g_encode(&lp->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float*>(x), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the pooled-conv kernel: x as (S2, S1, S0, C, N), box 36 x 9 x
+// 3 x C x 1.  False (the engine then runs the pooled conv) when x or its
+// rows break TMA's 16-byte rules.
+bool encode_pooled_map(const Problem& pb, const float* x, PooledParams* pq) {
+  std::memset(pq, 0, sizeof(*pq));
+  if (!g_encode || !aligned(x, 16) || (pb.S[2] % 4) != 0) return false;
+  cuuint64_t dims[5] = {(cuuint64_t)pb.S[2], (cuuint64_t)pb.S[1], (cuuint64_t)pb.S[0],
+                        (cuuint64_t)pb.Cin, (cuuint64_t)pb.N};
+  cuuint64_t strides[4];
+  strides[0] = (cuuint64_t)pb.S[2] * 4;
+  strides[1] = strides[0] * pb.S[1];
+  strides[2] = strides[1] * pb.S[0];
+  strides[3] = strides[2] * pb.Cin;
+  for (int i = 0; i < 4; ++i)
+    if (strides[i] >= (1ull << 40)) return false;
+  cuuint32_t box[5] = {(cuuint32_t)kPooledBoxCols, (cuuint32_t)kPooledBoxRows, 3,
+                       (cuuint32_t)pb.Cin, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return g_encode(&pq->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float*>(x), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cudaStream_t st) {
   PackParams pp;
   std::memset(&pp, 0, sizeof(pp));
@@ -364,11 +437,11 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
   if (pb.op == OP_CONV && (pb.groups > 1 || cp->ndhwc))
     cp->direct = direct_eligible(cp->pl.cin_g, cp->pl.cout_g, pb.stride[2], pb.dil[2], pb.k[2]);
   // the algebraic path: always for running statistics; for batch statistics
-  // only where the fused engine epilogue cannot run (its Gram statistics
-  // measured slower than that epilogue on the 64 x 3 x 32^3 workload, and
-  // much faster than the full-output fallback)
+  // where its statistics run in lag form, or where the fused engine epilogue
+  // cannot run (the patch-Gram kernel measured slower than that epilogue on
+  // the 64 x 3 x 32^3 workload, and much faster than the full-output fallback)
   cp->pool_ok = is_bn_op(op) && make_pool_plan(cp->pl, &cp->pp) == TC3D_OK;
-  cp->pool = cp->pool_ok && (op == OP_CONVT_BN_EVAL || !cp->pl.fused);
+  cp->pool = cp->pool_ok && (op == OP_CONVT_BN_EVAL || !cp->pl.fused || cp->pp.lag);
   cp->ws_total = cp->pool ? cp->pp.ws_total : cp->pl.ws_total;
   if (cp->direct) {
     cp->ws_total = 256;  // nothing is staged
@@ -444,7 +517,42 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   float* w2 = reinterpret_cast<float*>(wsb + pp.ws_w2_off);
   float* b2 = reinterpret_cast<float*>(wsb + pp.ws_b2_off);
   double* gsum = nullptr;
-  if (op == OP_CONVT_BN_POOL) {
+  const float* lrs = nullptr;
+  LagParams lp;
+  if (op == OP_CONVT_BN_POOL && pp.lag && encode_lag_map(pb, x, &lp)) {
+    // batch statistics in lag form: region sums, reduced over the grid
+    lp.part = reinterpret_cast<float*>(wsb + pp.ws_lpart_off);
+    lp.rs = reinterpret_cast<float*>(wsb + pp.ws_lrs_off);
+    lp.err = d->err;
+    lp.timeout_cycles = timeout_cycles(g_timeout_ns.load());
+    lp.N = pb.N;
+    for (int a = 0; a < 3; ++a) {
+      lp.L[a] = pb.S[a];
+      lp.nseg[a] = pp.lag_nseg[a];
+      lp.bulk[a] = pp.lag_bulk[a];
+      for (int i = 0; i <= kLagMaxSeg; ++i) lp.seg[a][i] = pp.lag_seg[a][i];
+    }
+    for (int a = 0; a < 3; ++a) {
+      lp.nrange[a] = pp.lag_nrange[a];
+      for (int k = 0; k < 4; ++k)
+        for (int e = 0; e < 2; ++e) lp.range[a][k][e] = pp.lag_range[a][k][e];
+    }
+    lp.nbox = pp.lag_nbox;
+    lp.nb1 = pp.lag_nb1;
+    lp.nb2 = pp.lag_nb2;
+    for (int i = 0; i < kLagMaxSeg; ++i) lp.nc[i] = pp.lag_nc[i];
+    for (int i = 0; i <= kLagMaxSeg; ++i) lp.cta0[i] = pp.lag_cta0[i];
+    lp.grid = pp.lag_grid;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (!d->lag_smem_set) {
+        if (lag_set_smem() != cudaSuccess) return TC3D_ERR_CUDA;
+        d->lag_smem_set = true;
+      }
+    }
+    if (lag_launch(lp, pb.Cin, st) != cudaSuccess) return TC3D_ERR_CUDA;
+    lrs = lp.rs;
+  } else if (op == OP_CONVT_BN_POOL) {
     GramParams gp;
     std::memset(&gp, 0, sizeof(gp));
     gp.x = x;
@@ -522,6 +630,30 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   fp.rmean = bn.rmean;
   fp.rvar = bn.rvar;
   fp.gcls = gsum;
+  fp.lrs = lrs;
+  for (int a = 0; a < 3; ++a) {
+    fp.lag_nseg[a] = pp.lag_nseg[a];
+    fp.lag_nrange[a] = pp.lag_nrange[a];
+    for (int k = 0; k < 4; ++k)
+      for (int e = 0; e < 2; ++e) fp.lag_range[a][k][e] = pp.lag_range[a][k][e];
+    for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < kMaxAxisTaps; ++i) fp.lag_ridx[a][r][i] = pp.lag_ridx[a][r][i];
+  }
+  // the pooled conv: on CUDA cores where its kernel takes the problem (few
+  // channels, at most 3 taps per axis, TMA-loadable x), else through the
+  // engine; the finalize writes the summed weights in the layout it reads
+  PooledParams pq;
+  bool pooled = false;
+  {
+    int Ke[3], P[3];
+    for (int a = 0; a < 3; ++a) {
+      Ke[a] = pp.Ke[a];
+      P[a] = (int)pl.P[a];
+    }
+    pooled = pooled_ok(pb.Cin, pb.Cout, Ke, P, pb.N) && encode_pooled_map(pb, x, &pq);
+  }
+  fp.pooled_layout = pooled ? 1 : 0;
+  fp.w2_stride = pooled_coutp(pb.Cout);
   fp.w2 = w2;
   fp.b2 = b2;
   fp.eps = bn.eps;
@@ -544,10 +676,63 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
       }
     }
   }
+  // summed taps: bit k of wkmask[a][e] iff 0 <= 2 (e_min + e) - p + d k <= 3
+  for (int a = 0; a < 3; ++a)
+    for (int e = 0; e < kMaxAxisTaps; ++e) {
+      unsigned m = 0;
+      if (e < pp.Ke[a])
+        for (int k = 0; k < pb.k[a]; ++k) {
+          const int j = 2 * (pp.e_min[a] + e) - pb.pad[a] + pb.dil[a] * k;
+          if (j >= 0 && j <= 3) m |= 1u << k;
+        }
+      fp.wkmask[a][e] = m;
+    }
   fp.ncls = pp.ncls;
+  // the class entries: (ci, taps t0, t1, t2) in patch order of the class
+  fp.ent_off[0] = 0;
+  for (int c = 0; c < pp.ncls; ++c) {
+    const int r0 = pp.cls_r[c][0], r1 = pp.cls_r[c][1], r2 = pp.cls_r[c][2];
+    const int n0 = pp.ntap[0][r0], n1 = pp.ntap[1][r1], n2 = pp.ntap[2][r2];
+    int row = fp.ent_off[c];
+    for (int ci = 0; ci < pb.Cin; ++ci)
+      for (int t0 = 0; t0 < n0; ++t0)
+        for (int t1 = 0; t1 < n1; ++t1)
+          for (int t2 = 0; t2 < n2; ++t2, ++row) {
+            const int v0 = pp.tap_u[0][r0][t0], v1 = pp.tap_u[1][r1][t1], v2 = pp.tap_u[2][r2][t2];
+            fp.ent_d[row] = ci * fp.V + (v0 * pp.nU[1] + v1) * pp.nU[2] + v2;
+            fp.ent_w[row] = ((ci * pb.k[0] + pp.tap_k[0][r0][t0]) * pb.k[1] + pp.tap_k[1][r1][t1]) *
+                                pb.k[2] +
+                            pp.tap_k[2][r2][t2];
+            fp.ent_cv[row] = ci | v0 << 4 | v1 << 8 | v2 << 12;
+            fp.ent_box[row] = pp.lag ? (pp.lag_ridx[0][r0][v0] * pp.lag_nrange[1] +
+                                        pp.lag_ridx[1][r1][v1]) *
+                                               pp.lag_nrange[2] +
+                                           pp.lag_ridx[2][r2][v2]
+                                     : 0;
+          }
+    fp.ent_off[c + 1] = row;
+  }
   for (int c = 0; c < 8; ++c)
     for (int a = 0; a < 3; ++a) fp.cls_r[c][a] = pp.cls_r[c][a];
-  if (pool_finalize_launch(fp, st) != cudaSuccess) return TC3D_ERR_CUDA;
+  if (pool_finalize_launch(fp, lrs != nullptr, st) != cudaSuccess) return TC3D_ERR_CUDA;
+  if (pooled) {
+    pq.w2 = w2;
+    pq.b2 = b2;
+    pq.y = y;
+    pq.err = d->err;
+    pq.timeout_cycles = timeout_cycles(g_timeout_ns.load());
+    pq.N = pb.N;
+    pq.Cin = pb.Cin;
+    pq.Cout = pb.Cout;
+    pq.coutp = pooled_coutp(pb.Cout);
+    for (int a = 0; a < 3; ++a) {
+      pq.P[a] = (int)pl.P[a];
+      pq.pad[a] = -pp.e_min[a];
+    }
+    pq.nq1b = (pq.P[1] + kPooledRows - 1) / kPooledRows;
+    pq.nq2b = (pq.P[2] + kPooledQ2 - 1) / kPooledQ2;
+    return pooled_launch(pq, d->sm_count, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
+  }
   int rc = launch_pack(pp.cplan, w2, wpack, d->sm_count, st);
   if (rc) return rc;
   return launch_engine(pp.cplan, pp.cplan.epi, x, wpack, b2, y, nullptr, d, st);
@@ -604,14 +789,19 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
     // the engine on the auxiliary stream: fork after the work queued so far
     // on st, join before anything queued on st later.
     std::lock_guard<std::mutex> lk(g_fork_mu);
-    if (cudaEventRecord(d->ev_fork, st) != cudaSuccess) return TC3D_ERR_CUDA;
+    DeviceState::Aux* a = aux_for(d, st);
+    if (!a) {
+      rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
+      return rc ? rc : launch_fill(pl, bias, y, d, st);
+    }
+    if (cudaEventRecord(a->fork, st) != cudaSuccess) return TC3D_ERR_CUDA;
     rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
     if (rc) return rc;
-    if (cudaStreamWaitEvent(d->aux, d->ev_fork, 0) != cudaSuccess) return TC3D_ERR_CUDA;
-    rc = launch_fill(pl, bias, y, d, d->aux);
+    if (cudaStreamWaitEvent(a->aux, a->fork, 0) != cudaSuccess) return TC3D_ERR_CUDA;
+    rc = launch_fill(pl, bias, y, d, a->aux);
     if (rc) return rc;
-    if (cudaEventRecord(d->ev_join, d->aux) != cudaSuccess ||
-        cudaStreamWaitEvent(st, d->ev_join, 0) != cudaSuccess)
+    if (cudaEventRecord(a->join, a->aux) != cudaSuccess ||
+        cudaStreamWaitEvent(st, a->join, 0) != cudaSuccess)
       return TC3D_ERR_CUDA;
     return TC3D_OK;
   }
@@ -925,7 +1115,42 @@ int tc3d_plan_describe(int op, int N, int Cin, int S0, int S1, int S2, int Cout,
                    pp.box_hi[i][2]);
           s += b;
         }
-        s += "], \"pool_cls\": [";
+        append(s, "], \"lag\": %lld", pp.lag);
+        if (pp.lag) {
+          append(s, ", \"lag_grid\": %lld", pp.lag_grid);
+          append(s, ", \"lag_nb\": [%lld", pp.lag_nb1);
+          append(s, ", %lld]", pp.lag_nb2);
+          s += ", \"lag_seg\": [";
+          for (int a = 0; a < 3; ++a) {
+            s += a ? ", [" : "[";
+            for (int i = 0; i <= pp.lag_nseg[a]; ++i) append(s, i ? ", %lld" : "%lld", pp.lag_seg[a][i]);
+            s += "]";
+          }
+          append(s, "], \"lag_bulk\": [%lld", pp.lag_bulk[0]);
+          append(s, ", %lld", pp.lag_bulk[1]);
+          append(s, ", %lld]", pp.lag_bulk[2]);
+          s += ", \"lag_nc\": [";
+          for (int i = 0; i < pp.lag_nseg[0]; ++i) append(s, i ? ", %lld" : "%lld", pp.lag_nc[i]);
+          s += "], \"lag_cta0\": [";
+          for (int i = 0; i <= pp.lag_nseg[0]; ++i) append(s, i ? ", %lld" : "%lld", pp.lag_cta0[i]);
+          // per axis, class value r and offset index: [segment lo, hi)
+          s += "], \"lag_srange\": [";
+          for (int a = 0; a < 3; ++a) {
+            s += a ? ", [" : "[";
+            for (int r = 0; r < 2; ++r) {
+              s += r ? ", [" : "[";
+              for (int i = 0; i < pp.nU[a]; ++i) {
+                snprintf(b, sizeof(b), "%s[%d, %d]", i ? ", " : "", pp.lag_srange[a][r][i][0],
+                         pp.lag_srange[a][r][i][1]);
+                s += b;
+              }
+              s += "]";
+            }
+            s += "]";
+          }
+          s += "]";
+        }
+        s += ", \"pool_cls\": [";
         for (int c = 0; c < pp.ncls; ++c) {
           snprintf(b, sizeof(b), "%s[[%d, %d, %d], [", c ? ", " : "", pp.cls_r[c][0],
                    pp.cls_r[c][1], pp.cls_r[c][2]);

@@ -29,11 +29,17 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 // be looked up once per device (with that device current) and passed on.
 int noalloc_scratch(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TC3D_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // the failure is reported here, not by the next launch check
+    return TC3D_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, tc3d_noalloc_scratch) != cudaSuccess || !p) return TC3D_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, tc3d_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return TC3D_ERR_CUDA;
+    }
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];

@@ -534,6 +534,131 @@ int make_plan(const Problem& pb, Plan* out) {
   return st;
 }
 
+// Lag form of the batch statistics (see lag_slot in plan.h): segments,
+// region count, the per-class segment ranges and the work split.  Leaves
+// pp.lag = 0 where it does not apply: more than 3 channels, an axis whose
+// offsets are neither one value nor two consecutive ones, rows along axis 2
+// that TMA cannot load (extent not a multiple of 4), more than one segment
+// wider than one position, or more CTAs than kLagMaxCtas.
+static void plan_lag(const Plan& bn, PoolPlan& pp) {
+  const Problem& pb = bn.pb;
+  pp.lag = 0;
+  if (pb.Cin > kLagMaxCin || pb.S[2] % 4 != 0) return;
+  for (int a = 0; a < 3; ++a) {
+    if (pp.nU[a] > 2) return;
+    if (pp.nU[a] == 2 && pp.U[a][1] != pp.U[a][0] + 1) return;
+  }
+  auto clampi = [](int64_t v, int64_t lo, int64_t hi) {
+    return (int)std::min<int64_t>(std::max<int64_t>(v, lo), hi);
+  };
+  for (int a = 0; a < 3; ++a) {
+    const int L = pb.S[a];
+    // breakpoints: the ends of the z ranges [u, M_r + u) of every class
+    // value r with taps along this axis and every offset u, clipped to x
+    int bp[2 + 4 * kMaxAxisTaps], nbp = 0;
+    bp[nbp++] = 0;
+    bp[nbp++] = L;
+    for (int r = 0; r < 2; ++r) {
+      if (!pp.ntap[a][r]) continue;
+      const int64_t Mr = ceil_div(bn.O[a] - r, 2);
+      for (int i = 0; i < pp.nU[a]; ++i) {
+        bp[nbp++] = clampi(pp.U[a][i], 0, L);
+        bp[nbp++] = clampi(Mr + pp.U[a][i], 0, L);
+      }
+    }
+    std::sort(bp, bp + nbp);
+    nbp = (int)(std::unique(bp, bp + nbp) - bp);
+    if (nbp - 1 > kLagMaxSeg) return;
+    pp.lag_nseg[a] = nbp - 1;
+    for (int s = 0; s < nbp; ++s) pp.lag_seg[a][s] = bp[s];
+    // one wide segment; every other one a single position
+    int bulk = 0;
+    for (int s = 1; s < nbp - 1; ++s)
+      if (bp[s + 1] - bp[s] > bp[bulk + 1] - bp[bulk]) bulk = s;
+    for (int s = 0; s < nbp - 1; ++s)
+      if (s != bulk && bp[s + 1] - bp[s] != 1) return;
+    pp.lag_bulk[a] = bulk;
+    for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < kMaxAxisTaps; ++i) pp.lag_srange[a][r][i][0] = pp.lag_srange[a][r][i][1] = 0;
+    for (int r = 0; r < 2; ++r) {
+      if (!pp.ntap[a][r]) continue;
+      const int64_t Mr = ceil_div(bn.O[a] - r, 2);
+      for (int i = 0; i < pp.nU[a]; ++i) {
+        const int lo = clampi(pp.U[a][i], 0, L), hi = clampi(Mr + pp.U[a][i], 0, L);
+        if (lo >= hi) continue;
+        const int slo = (int)(std::find(bp, bp + nbp, lo) - bp);
+        const int shi = (int)(std::find(bp, bp + nbp, hi) - bp);
+        pp.lag_srange[a][r][i][0] = slo;
+        pp.lag_srange[a][r][i][1] = shi;
+      }
+    }
+    pp.lag_nrange[a] = 0;
+    for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < kMaxAxisTaps; ++i) {
+        pp.lag_ridx[a][r][i] = 0;
+        if (!pp.ntap[a][r] || i >= pp.nU[a]) continue;
+        const int lo = pp.lag_srange[a][r][i][0], hi = pp.lag_srange[a][r][i][1];
+        int k = 0;
+        while (k < pp.lag_nrange[a] && !(pp.lag_range[a][k][0] == lo && pp.lag_range[a][k][1] == hi))
+          ++k;
+        if (k == pp.lag_nrange[a]) {
+          if (k == 4) return;
+          pp.lag_range[a][k][0] = lo;
+          pp.lag_range[a][k][1] = hi;
+          ++pp.lag_nrange[a];
+        }
+        pp.lag_ridx[a][r][i] = k;
+      }
+  }
+  pp.lag_nreg = pp.lag_nseg[0] * pp.lag_nseg[1] * pp.lag_nseg[2];
+  pp.lag_nbox = pp.lag_nrange[0] * pp.lag_nrange[1] * pp.lag_nrange[2];
+  // work split: the jobs of axis-0 segment s (one per block of 8 rows and 32
+  // columns) cost about N (2 len(s) + 1) each (steps, plus the planes every
+  // run of consecutive planes loads first); CTAs in proportion, at least
+  // one per job, then spare CTAs to the segment whose CTAs carry most
+  pp.lag_nb1 = (int)ceil_div(pb.S[1], kLagRows);
+  pp.lag_nb2 = (int)ceil_div(pb.S[2], kLagCols);
+  const int64_t jobs_per_seg = (int64_t)pp.lag_nb1 * pp.lag_nb2;
+  if (jobs_per_seg * pp.lag_nseg[0] > kLagMaxCtas) return;
+  double cost[kLagMaxSeg], total = 0.0;
+  for (int s = 0; s < pp.lag_nseg[0]; ++s) {
+    const int len = pp.lag_seg[0][s + 1] - pp.lag_seg[0][s];
+    cost[s] = (double)pb.N * (2.0 * len + 1.0);
+    total += cost[s] * (double)jobs_per_seg;
+  }
+  int64_t grid = 0;
+  for (int s = 0; s < pp.lag_nseg[0]; ++s) {
+    const int len = pp.lag_seg[0][s + 1] - pp.lag_seg[0][s];
+    const int64_t cap = (int64_t)pb.N * len;
+    const int64_t share = (int64_t)((double)kLagGridTarget * cost[s] / total);
+    pp.lag_nc[s] = (int)std::max<int64_t>(1, std::min<int64_t>(cap, share));
+    grid += jobs_per_seg * pp.lag_nc[s];
+  }
+  for (;;) {
+    int best = -1;
+    double worst = 0.0;
+    for (int s = 0; s < pp.lag_nseg[0]; ++s) {
+      const int len = pp.lag_seg[0][s + 1] - pp.lag_seg[0][s];
+      if (pp.lag_nc[s] >= (int64_t)pb.N * len) continue;
+      const double per = cost[s] / pp.lag_nc[s];
+      if (per > worst) {
+        worst = per;
+        best = s;
+      }
+    }
+    if (best < 0 || grid + jobs_per_seg > std::max<int64_t>(kLagGridTarget, jobs_per_seg * pp.lag_nseg[0]))
+      break;
+    ++pp.lag_nc[best];
+    grid += jobs_per_seg;
+  }
+  if (grid > kLagMaxCtas) return;
+  pp.lag_cta0[0] = 0;
+  for (int s = 0; s < pp.lag_nseg[0]; ++s)
+    pp.lag_cta0[s + 1] = pp.lag_cta0[s] + (int)(jobs_per_seg * pp.lag_nc[s]);
+  pp.lag_grid = (int)grid;
+  pp.lag = 1;
+}
+
 int make_pool_plan(const Plan& bn, PoolPlan* out) {
   PoolPlan& pp = *out;
   std::memset(&pp, 0, sizeof(pp));
@@ -712,11 +837,17 @@ int make_pool_plan(const Plan& bn, PoolPlan* out) {
   pp.conv = c;
   if (make_plan(c, &pp.cplan) != TC3D_OK) return pp.status;
 
+  if (pb.op == OP_CONVT_BN_POOL) plan_lag(bn, pp);
+
   // workspace: the pooled conv's packed weights first, then this path's own
   int64_t off = pp.cplan.ws_total;
   pp.ws_wpack_off = pp.cplan.ws_wpack_off;
   pp.ws_w2_off = off;
-  pp.ws_w2_bytes = (int64_t)pb.Cout * pb.Cin * pp.Ke[0] * pp.Ke[1] * pp.Ke[2] * 4;
+  // summed weights: [Cout][Cin][Ke] for the engine, or [Cin][3][3][3][Cout
+  // padded to 16] for the pooled-conv kernel
+  pp.ws_w2_bytes = std::max<int64_t>((int64_t)pb.Cout * pb.Cin * pp.Ke[0] * pp.Ke[1] * pp.Ke[2],
+                                     (int64_t)pb.Cin * 27 * ((pb.Cout + 15) / 16 * 16)) *
+                   4;
   off = round_up(off + pp.ws_w2_bytes, 256);
   pp.ws_b2_off = off;
   off = round_up(off + (int64_t)pb.Cout * 4, 256);
@@ -726,6 +857,13 @@ int make_pool_plan(const Plan& bn, PoolPlan* out) {
     off = round_up(off + pp.ws_gpart_bytes, 256);
     pp.ws_gsum_off = off;
     off = round_up(off + (int64_t)kGramMaxBoxes * kGramEntries * 8, 256);
+    if (pp.lag) {
+      pp.ws_lpart_off = off;
+      pp.ws_lpart_bytes = (int64_t)pp.lag_grid * pp.lag_nbox * kLagSlots * 4;
+      off = round_up(off + pp.ws_lpart_bytes, 256);
+      pp.ws_lrs_off = off;
+      off = round_up(off + (int64_t)pp.lag_nbox * kLagSlots * 4, 256);
+    }
   }
   pp.ws_total = off;
   pp.status = TC3D_OK;

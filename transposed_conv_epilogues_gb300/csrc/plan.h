@@ -7,6 +7,13 @@
 #include <cstddef>
 #include <cstdint>
 
+// functions shared by the host planner and the kernels
+#if defined(__CUDACC__)
+#define TC3D_HD __host__ __device__
+#else
+#define TC3D_HD
+#endif
+
 namespace tc3d {
 
 enum OpKind : int {
@@ -169,6 +176,43 @@ constexpr int kGramMaxCtas = 1024;                              // partial slots
 constexpr int kGramMaxBoxes = 8;
 constexpr int kGramSlabFloats = 12288;                          // one x slab buffer (48 KB)
 
+// Lag form of the batch statistics.  When x has at most 3 channels and every
+// axis has one offset or two consecutive ones, an entry of G_r is
+//   sum over the rows m of class r of x[c, m + u] x[c', m + u']
+//     = sum over z in [u, M_r + u) (per axis) of x[c, z] x[c', z + delta],
+// delta = u' - u in {-1, 0, 1}^3 (x zero outside its extent), and an entry
+// of s_r is the same kind of sum of x[c, z].  The ends of those z ranges,
+// over all classes and offsets, cut each axis into a few segments: one wide
+// one and positions of their own at the ends.  The lag kernel sums every
+// product x[c, z] x[c', z + delta] (and every x[c, z]) over every region (a
+// product of three segments); an entry of G_r or s_r is the sum of the
+// regions its range covers.  Per input position that is 126 products for 3
+// channels, against the D (D + 1) / 2 = 300 of the 24-entry patch Gram.
+constexpr int kLagMaxCin = 3;
+constexpr int kLagSlots = 128;    // per region: Cin first-order sums, then the products
+constexpr int kLagMaxSeg = 5;     // segments per axis
+constexpr int kLagRows = 8;       // axis-1 rows of a CTA (one per warp)
+constexpr int kLagCols = 32;      // axis-2 columns of a CTA (one per lane)
+constexpr int kLagChunk = 4;      // planes per tensor copy of a warp's window rows
+constexpr int kLagBoxCols = kLagCols + 8;  // box columns 32 b2 - 4 .. 32 b2 + 35
+constexpr int kLagBoxRows = 3;    // a warp's row and its two neighbours
+constexpr int kLagGridTarget = 152;  // CTAs the work is shared among (one per SM)
+constexpr int kLagMaxCtas = 1024;
+
+// Slot of the product x[c, z] x[c2, z + delta] among a region's sums, with
+// delta = (j / 9 - 1, j / 3 % 3 - 1, j % 3 - 1): channel pairs c <= c2, and for
+// c == c2 only the lags delta >= 0 in lexicographic order (j >= 13; the others
+// are the same products seen from the other factor).  Slots 0 .. cin-1 hold
+// the sums of x[c, z].  Returns -1 for a pair that has no slot.
+TC3D_HD constexpr int lag_slot(int cin, int c, int c2, int j) {
+  if (c > c2 || (c == c2 && j < 13)) return -1;
+  int s = cin;
+  for (int cc = 0; cc < c; ++cc) s += 14 + 27 * (cin - 1 - cc);
+  return c2 == c ? s + j - 13 : s + 14 + 27 * (c2 - c - 1) + j;
+}
+TC3D_HD constexpr int lag_nslots(int cin) { return cin + cin * 14 + 27 * cin * (cin - 1) / 2; }
+static_assert(lag_nslots(kLagMaxCin) <= kLagSlots, "lag slots of 3 channels fit a region row");
+
 struct PoolPlan {
   int status;     // 0: the algebraic path applies
   int D;          // patch entries Cin * nU0 * nU1 * nU2 (<= kGramMaxD)
@@ -199,6 +243,34 @@ struct PoolPlan {
   int64_t ws_b2_off;                   // folded bias [Cout]
   int64_t ws_gpart_off, ws_gpart_bytes;// per-CTA Gram partials [kGramMaxCtas][kGramEntries] f32
   int64_t ws_gsum_off;                 // per-class combined Gram [8][kGramEntries] f64
+
+  // lag form of the batch statistics (lag = 1: taken instead of the Gram
+  // kernel; see lag_slot)
+  int lag;
+  int lag_nseg[3];
+  int lag_seg[3][kLagMaxSeg + 1];      // segment s of axis a: [lag_seg[a][s], lag_seg[a][s + 1])
+  int lag_bulk[3];                     // the wide segment; every other one is one position
+  // per axis, class value r and offset index i: the segments [lo, hi) of
+  // the z range [U_i, M_r + U_i) clipped to x
+  int lag_srange[3][2][kMaxAxisTaps][2];
+  // the distinct ranges among them per axis (at most 4), and the range of
+  // each (class value, offset index); a class entry is then the sum over one
+  // box of ranges
+  int lag_nrange[3];
+  int lag_range[3][4][2];
+  int lag_ridx[3][2][kMaxAxisTaps];
+  int lag_nreg;                        // regions, nseg0 * nseg1 * nseg2
+  // work: a job is (segment s0 of axis 0, block of 8 rows, block of 32
+  // columns); the jobs of segment s0 take lag_nc[s0] CTAs each, which share
+  // its N * len(s0) (sample, plane) steps
+  int lag_nb1, lag_nb2;
+  int lag_nc[kLagMaxSeg];
+  int lag_cta0[kLagMaxSeg + 1];        // first CTA of each axis-0 segment
+  int lag_grid;
+  int lag_nbox;                          // boxes, nrange0 * nrange1 * nrange2
+  int64_t ws_lpart_off, ws_lpart_bytes;  // per-CTA box sums [grid][nbox][kLagSlots] f32
+  int64_t ws_lrs_off;                    // box sums over the grid [nbox][kLagSlots] f32
+
   int64_t ws_total;
 };
 

@@ -2,7 +2,11 @@
 // reduction, and the per-channel finalize (see PoolPlan in plan.h).
 #include "pool.cuh"
 
+#include <algorithm>
+#include <climits>
 #include <cstring>
+
+#include "ptx.cuh"
 
 namespace tc3d {
 
@@ -373,62 +377,93 @@ __device__ __forceinline__ void block_sum2_pool(double& a, double& b) {
   b = sb[0];
 }
 
-// entry i of class c's patch: (ci, tap t0, t1, t2) -> patch index d and weight
-__device__ __forceinline__ void class_entry(const PoolFinParams& p, int c, int co, int i, int& d,
-                                            float& wv) {
-  const int r0 = p.cls_r[c][0], r1 = p.cls_r[c][1], r2 = p.cls_r[c][2];
-  const int n0 = p.ntap[0][r0], n1 = p.ntap[1][r1], n2 = p.ntap[2][r2];
-  const int t2 = i % n2, t1 = (i / n2) % n1, t0 = (i / (n1 * n2)) % n0, ci = i / (n0 * n1 * n2);
-  d = ci * p.V + (p.tap_u[0][r0][t0] * p.nU[1] + p.tap_u[1][r1][t1]) * p.nU[2] +
-      p.tap_u[2][r2][t2];
-  const int k0 = p.tap_k[0][r0][t0], k1 = p.tap_k[1][r1][t1], k2 = p.tap_k[2][r2][t2];
-  wv = __ldg(p.w + (((long long)ci * p.Cout + co) * p.k[0] + k0) * p.k[1] * p.k[2] +
-             (long long)k1 * p.k[2] + k2);
-}
-
 __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constant__ PoolFinParams p) {
   const int co = blockIdx.x;
+  extern __shared__ float fin_smem[];  // this channel's weights [Cin][k0][k1][k2]
   __shared__ float s_scale;
-  __shared__ int sd[8][kGramMaxD];
-  __shared__ float sw[8][kGramMaxD];
-  __shared__ int sne[8], soff[9];
   double s1 = 0.0, s2 = 0.0;
-  if (p.gcls) {
+  const bool batch = p.gcls != nullptr || p.lrs != nullptr;
+  const int nr1 = p.lag_nrange[1], nr2 = p.lag_nrange[2];
+  // this channel's weights [Cin][k0][k1][k2]; in lag form then the box sums
+  // [box][slot] (a box is one segment range per axis: the z range of a class
+  // entry's first factor)
+  float* wsh = fin_smem;
+  const int kvol = p.k[0] * p.k[1] * p.k[2];
+  float* bs = fin_smem + ((p.Cin * kvol + 3) & ~3);
+  for (int e = threadIdx.x; e < p.Cin * kvol; e += 256) {
+    const int ci = e / kvol, kk = e - ci * kvol;
+    wsh[e] = __ldg(p.w + ((long long)ci * p.Cout + co) * kvol + kk);
+  }
+  // (launched dependent only after the lag reduction, which writes no
+  // weights; a dependent is signalled only after this wait, so no later
+  // kernel of the call runs ahead of work queued before the call)
+  grid_dependency_wait();  // the statistics of the kernels before
+  grid_launch_dependents();
+  if (p.lrs) {
+    const int nb = p.lag_nrange[0] * nr1 * nr2 * kLagSlots;
+    for (int e = threadIdx.x; e < nb; e += 256) bs[e] = __ldg(p.lrs + e);
+  }
+  __syncthreads();
+  if (batch) {
     // class sums of the bias-free transposed conv: w_r . s_r and w_r^T G_r w_r
-    // (G_r, s_r: the class's combined Gram); first every class's patch
-    // entries (index, weight), then all (class, i, j) pairs in one loop
-    if (threadIdx.x < 8) {
-      const int c = threadIdx.x;
-      sne[c] = c < p.ncls ? p.Cin * p.ntap[0][p.cls_r[c][0]] * p.ntap[1][p.cls_r[c][1]] *
-                                p.ntap[2][p.cls_r[c][2]]
-                          : 0;
+    // (G_r, s_r: the class's combined Gram).  Thread t takes row t of the
+    // entries of all classes (entry i of class c) and its pairs (i, j).  The
+    // entry tables are read from shared memory: indexing kernel parameters
+    // with values that differ across a warp would serialise the reads.
+    __shared__ int e_d[8 * kGramMaxD], e_w[8 * kGramMaxD], e_cv[8 * kGramMaxD],
+        e_box[8 * kGramMaxD], e_off[9];
+    const int nrows = p.ent_off[p.ncls];
+    for (int r = threadIdx.x; r < nrows; r += 256) {
+      e_d[r] = p.ent_d[r];
+      e_w[r] = p.ent_w[r];
+      e_cv[r] = p.ent_cv[r];
+      e_box[r] = p.ent_box[r];
     }
+    if (threadIdx.x < 9) e_off[threadIdx.x] = p.ent_off[threadIdx.x];
     __syncthreads();
-    if (threadIdx.x == 0) {
-      soff[0] = 0;
-      for (int c = 0; c < 8; ++c) soff[c + 1] = soff[c] + sne[c] * sne[c];
-    }
-    for (int q = threadIdx.x; q < 8 * kGramMaxD; q += 256) {
-      const int c = q / kGramMaxD, i = q % kGramMaxD;
-      if (i < sne[c]) class_entry(p, c, co, i, sd[c][i], sw[c][i]);
-    }
-    __syncthreads();
-    for (int q = threadIdx.x; q < soff[8]; q += 256) {
+    float f1 = 0.f, f2 = 0.f;
+    for (int row = threadIdx.x; row < nrows; row += 256) {
       int c = 0;
-      while (q >= soff[c + 1]) ++c;
-      const int ne = sne[c], i = (q - soff[c]) / ne, j = (q - soff[c]) % ne;
-      const int di = sd[c][i], dj = sd[c][j];
-      const int lo = (di >> 3) <= (dj >> 3) ? di : dj, hi = lo == di ? dj : di;
-      const double* G = p.gcls + (size_t)c * kGramEntries;
-      s2 += (double)sw[c][i] * (double)sw[c][j] * G[lo * kGramMaxD + hi];
-      if (j == 0) s1 += (double)sw[c][i] * G[kGramMaxD * kGramMaxD + di];
+      while (row >= e_off[c + 1]) ++c;
+      const int r0 = e_off[c], ne = e_off[c + 1] - r0;
+      const int di = e_d[row];
+      const float wi = wsh[e_w[row]];
+      if (p.lrs) {
+        const int cvi = e_cv[row];
+        f1 = fmaf(wi, bs[e_box[row] * kLagSlots + (cvi & 15)], f1);
+        float g = 0.f;
+        for (int j = 0; j < ne; ++j) {
+          const int dj = e_d[r0 + j];
+          // the factor earlier in patch order (channel-major, offsets in
+          // lexicographic order) at lag v_later - v_earlier; offsets are
+          // consecutive, so index differences are offset differences
+          const int first = di <= dj ? row : r0 + j, second = di <= dj ? r0 + j : row;
+          const int ca = e_cv[first], cb = e_cv[second];
+          const int jl = 9 * (((cb >> 4) & 15) - ((ca >> 4) & 15) + 1) +
+                         3 * (((cb >> 8) & 15) - ((ca >> 8) & 15) + 1) +
+                         (((cb >> 12) & 15) - ((ca >> 12) & 15) + 1);
+          g = fmaf(wsh[e_w[r0 + j]],
+                   bs[e_box[first] * kLagSlots + lag_slot(p.Cin, ca & 15, cb & 15, jl)], g);
+        }
+        f2 = fmaf(wi, g, f2);
+      } else {
+        const double* G = p.gcls + (size_t)c * kGramEntries;
+        s1 += (double)wi * G[kGramMaxD * kGramMaxD + di];
+        for (int j = 0; j < ne; ++j) {
+          const int dj = e_d[r0 + j];
+          const int lo = (di >> 3) <= (dj >> 3) ? di : dj, hi = lo == di ? dj : di;
+          s2 += (double)wi * (double)wsh[e_w[r0 + j]] * G[lo * kGramMaxD + hi];
+        }
+      }
     }
+    s1 += (double)f1;
+    s2 += (double)f2;
   }
   block_sum2_pool(s1, s2);
   if (threadIdx.x == 0) {
     const double g = p.gamma ? (double)p.gamma[co] : 1.0, be = p.beta ? (double)p.beta[co] : 0.0;
     double scale, shift;
-    if (p.gcls) {
+    if (batch) {
       // y = (pooled mean of t0 - mean of t0) * scale + beta  (the bias cancels)
       const double mean = s1 / p.count;
       double var = s2 / p.count - mean * mean;
@@ -444,28 +479,198 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
     p.b2[co] = (float)shift;
   }
   __syncthreads();
-  // summed weights: W'[e] = sum of W[k] over taps k with 2(e_min + e) - p + d k in [0, 3]
-  const int kv = p.Ke[0] * p.Ke[1] * p.Ke[2];
+  // summed weights: W'[e] = sum of W[k] over taps k with 2(e_min + e) - p + d k
+  // in [0, 3]; in the pooled-conv kernel's layout every axis has 3 taps (zero
+  // past Ke) and channels are innermost
+  const int K0 = p.pooled_layout ? 3 : p.Ke[0], K1 = p.pooled_layout ? 3 : p.Ke[1],
+            K2 = p.pooled_layout ? 3 : p.Ke[2];
+  const int kv = K0 * K1 * K2;
+  __shared__ unsigned wkm[3 * kMaxAxisTaps];
+  if (threadIdx.x < 3 * kMaxAxisTaps)
+    wkm[threadIdx.x] = p.wkmask[threadIdx.x / kMaxAxisTaps][threadIdx.x % kMaxAxisTaps];
+  __syncthreads();
   for (int q = threadIdx.x; q < p.Cin * kv; q += 256) {
     const int ci = q / kv, e = q % kv;
-    const int ee[3] = {e / (p.Ke[1] * p.Ke[2]), (e / p.Ke[2]) % p.Ke[1], e % p.Ke[2]};
+    const int ee[3] = {e / (K1 * K2), (e / K2) % K1, e % K2};
     float acc = 0.f;
-    for (int k0 = 0; k0 < p.k[0]; ++k0) {
-      const int j0 = 2 * (p.e_min[0] + ee[0]) - p.pad[0] + p.dil[0] * k0;
-      if (j0 < 0 || j0 > 3) continue;
-      for (int k1 = 0; k1 < p.k[1]; ++k1) {
-        const int j1 = 2 * (p.e_min[1] + ee[1]) - p.pad[1] + p.dil[1] * k1;
-        if (j1 < 0 || j1 > 3) continue;
-        for (int k2 = 0; k2 < p.k[2]; ++k2) {
-          const int j2 = 2 * (p.e_min[2] + ee[2]) - p.pad[2] + p.dil[2] * k2;
-          if (j2 < 0 || j2 > 3) continue;
-          acc += __ldg(p.w + (((long long)ci * p.Cout + co) * p.k[0] + k0) * p.k[1] * p.k[2] +
-                       (long long)k1 * p.k[2] + k2);
+    if (ee[0] < p.Ke[0] && ee[1] < p.Ke[1] && ee[2] < p.Ke[2]) {
+      // taps k of each axis with 2 (e_min + e) - p + d k in [0, 3]
+      const unsigned m0 = wkm[ee[0]], m1 = wkm[kMaxAxisTaps + ee[1]], m2 = wkm[2 * kMaxAxisTaps + ee[2]];
+      for (unsigned a = m0; a; a &= a - 1)
+        for (unsigned b = m1; b; b &= b - 1)
+          for (unsigned c = m2; c; c &= c - 1)
+            acc += wsh[ci * kvol + ((__ffs(a) - 1) * p.k[1] + (__ffs(b) - 1)) * p.k[2] + (__ffs(c) - 1)];
+    }
+    if (p.pooled_layout)
+      p.w2[(long long)q * p.w2_stride + co] = acc * s_scale;
+    else
+      p.w2[((long long)co * p.Cin + ci) * kv + e] = acc * s_scale;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pooled convolution on CUDA cores: y[n, co, q] = b2[co] + sum over ci and
+// e of w2[ci, e, co] x[n, ci, 2 q + e - pad] (stride 2, 3 taps per axis with
+// zero weights past Ke, at most 4 input channels).  An item is (sample n,
+// q0, 4 rows of q1, 16 of q2) for all channels, one warp per 16 channels.
+// CTAs are persistent: the weights come in once by a bulk copy, the items'
+// input boxes (36 columns x 9 rows x 3 planes x Cin, zero outside x; the x
+// start rounded down to 16 bytes, so each row starts `shift` columns in) by
+// TMA into two buffers, the next item's box landing while the current one is
+// used.  Lane (g, q2) computes the 4 rows of its q2 for 8 channels: per (ci,
+// e0, e2) it reads the 9 inputs of its column (lanes read consecutive even
+// columns: distinct banks) and, per e1, 8 weights (two 16-byte broadcasts),
+// 32 multiply-adds each.
+// ---------------------------------------------------------------------------
+constexpr int kPooledKe = 3;
+constexpr int kPooledBoxFloats = kPooledBoxCols * kPooledBoxRows * kPooledKe;  // per channel
+
+size_t pooled_smem_bytes(int Cin, int coutp) {
+  const size_t box = ((size_t)Cin * kPooledBoxFloats * 4 + 127) / 128 * 128;
+  const size_t wb = (size_t)Cin * 27 * coutp * 4;
+  return 128 + 2 * box + wb + 64;
+}
+
+__device__ __forceinline__ void pooled_issue(const PooledParams& p, uint32_t dst, uint32_t bar,
+                                             int item, uint32_t box_bytes) {
+  const int per = p.nq1b * p.nq2b;
+  const int s = item / per, r = item - s * per;
+  const int n = s / p.P[0], q0 = s - n * p.P[0];
+  const int q1b = r / p.nq2b, q2b = r - q1b * p.nq2b;
+  mbar_arrive_expect_tx(bar, box_bytes);
+  tma_load_5d(dst, &p.xmap, (2 * q2b * kPooledQ2 - p.pad[2]) & ~3, 2 * q1b * kPooledRows - p.pad[1],
+              2 * q0 - p.pad[0], 0, n, bar);
+}
+
+__global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant__ PooledParams p) {
+  extern __shared__ __align__(128) uint8_t pooled_raw[];
+  uint8_t* base = pooled_raw + ((128u - (smem_u32(pooled_raw) & 127u)) & 127u);
+  const uint32_t box_bytes = (uint32_t)(p.Cin * kPooledBoxFloats * 4);
+  const uint32_t box_stride = (box_bytes + 127u) / 128u * 128u;
+  const float* xsb = reinterpret_cast<const float*>(base);
+  const float* ws = reinterpret_cast<const float*>(base + 2 * box_stride);
+  const uint32_t wbytes = (uint32_t)(p.Cin * 27 * p.coutp * 4);
+  const uint32_t bar0 = smem_u32(base + 2 * box_stride + wbytes);  // boxes: bar0, bar0 + 8; weights: + 16
+  const int items = p.nq1b * p.nq2b * p.N * p.P[0];
+  if (threadIdx.x == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    mbar_init(bar0 + 16, 1);
+    fence_barrier_init();
+    for (int t = 0; t < 2; ++t) {
+      const int it = (int)blockIdx.x + t * (int)gridDim.x;
+      if (it < items) pooled_issue(p, smem_u32(base) + t * box_stride, bar0 + 8u * t, it, box_bytes);
+    }
+    grid_dependency_wait();  // the folded weights and bias of the finalize
+    mbar_arrive_expect_tx(bar0 + 16, wbytes);
+    bulk_g2s(smem_u32(ws), p.w2, wbytes, bar0 + 16);
+  }
+  grid_dependency_wait();
+  __syncthreads();
+  // every thread takes the same branch on a wait's outcome (the loop holds a
+  // CTA barrier)
+  bool ok = __syncthreads_and(mbar_wait(bar0 + 16, 0, p.timeout_cycles, nullptr));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q2l = lane & 15, g = lane >> 4;
+  const int co0 = 16 * warp + 8 * g;
+  const long long pv = (long long)p.P[0] * p.P[1] * p.P[2];
+  const int per = p.nq1b * p.nq2b;
+  int t = 0;
+  for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++t) {
+    const int buf = t & 1;
+    ok = __syncthreads_and(mbar_wait(bar0 + 8u * buf, (uint32_t)((t >> 1) & 1), p.timeout_cycles,
+                                     nullptr));
+    if (!ok) break;
+    const int s = item / per, r = item - s * per;
+    const int n = s / p.P[0], q0 = s - n * p.P[0];
+    const int q1b = r / p.nq2b, q2b = r - q1b * p.nq2b;
+    const int q1a = q1b * kPooledRows, q2a = q2b * kPooledQ2;
+    const int xc = 2 * q2a - p.pad[2];
+    const int shift = xc - (xc & ~3);
+    const float* xs = xsb + buf * (box_stride / 4);
+    float acc[kPooledRows][8];
+#pragma unroll
+    for (int i = 0; i < kPooledRows; ++i)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
+    for (int ci = 0; ci < p.Cin; ++ci) {
+#pragma unroll
+      for (int e0 = 0; e0 < kPooledKe; ++e0)
+#pragma unroll
+        for (int e2 = 0; e2 < kPooledKe; ++e2) {
+          const float* col =
+              xs + ((ci * kPooledKe + e0) * kPooledBoxRows) * kPooledBoxCols + shift + 2 * q2l + e2;
+          float v[kPooledBoxRows];
+#pragma unroll
+          for (int j = 0; j < kPooledBoxRows; ++j) v[j] = col[j * kPooledBoxCols];
+#pragma unroll
+          for (int e1 = 0; e1 < kPooledKe; ++e1) {
+            const float* wr =
+                ws + (((ci * kPooledKe + e0) * kPooledKe + e1) * kPooledKe + e2) * p.coutp + co0;
+            const float4 wa = *reinterpret_cast<const float4*>(wr);
+            const float4 wb = *reinterpret_cast<const float4*>(wr + 4);
+            const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < kPooledRows; ++i) {
+              const float xv = v[2 * i + e1];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) acc[i][c] = fmaf(xv, w8[c], acc[i][c]);
+            }
+          }
         }
+    }
+    // this item's box is read: the one two items on may land in it
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int nx = item + 2 * (int)gridDim.x;
+      if (nx < items) pooled_issue(p, smem_u32(base) + buf * box_stride, bar0 + 8u * buf, nx, box_bytes);
+    }
+    const int q2 = q2a + q2l;
+    if (q2 < p.P[2]) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int co = co0 + c;
+        if (co >= p.Cout) break;
+        const float bb = p.b2 ? __ldg(p.b2 + co) : 0.f;
+        float* yo = p.y + ((long long)n * p.Cout + co) * pv + (long long)q0 * p.P[1] * p.P[2] + q2;
+#pragma unroll
+        for (int i = 0; i < kPooledRows; ++i)
+          if (q1a + i < p.P[1]) yo[(long long)(q1a + i) * p.P[2]] = acc[i][c] + bb;
       }
     }
-    p.w2[((long long)co * p.Cin + ci) * kv + e] = acc * s_scale;
   }
+  if (!ok) {
+    // a wait ran out: flag it; the boxes still in flight land before the CTA leaves
+    if (threadIdx.x == 0) {
+      atomicExch(p.err, 1);
+      for (int k = 0; k < 2; ++k) mbar_wait(bar0 + 8u * k, (uint32_t)((t >> 1) & 1), p.timeout_cycles, nullptr);
+    }
+  }
+}
+
+bool pooled_ok(int Cin, int Cout, const int Ke[3], const int P[3], int N) {
+  if (Cin < 1 || Cin > kPooledMaxCin || Cout < 1 || Cout > kPooledMaxCout) return false;
+  for (int a = 0; a < 3; ++a)
+    if (Ke[a] < 1 || Ke[a] > kPooledKe || P[a] < 1) return false;
+  const long long nq1b = (P[1] + kPooledRows - 1) / kPooledRows;
+  const long long nq2b = (P[2] + kPooledQ2 - 1) / kPooledQ2;
+  return nq1b * nq2b * N * P[0] <= INT32_MAX &&
+         pooled_smem_bytes(Cin, pooled_coutp(Cout)) <= 100 * 1024;
+}
+
+cudaError_t pooled_launch(const PooledParams& p, int sm_count, cudaStream_t st) {
+  const long long items = (long long)p.nq1b * p.nq2b * p.N * p.P[0];
+  const size_t smem = pooled_smem_bytes(p.Cin, p.coutp);
+  // persistent CTAs: as many as fit on the SMs at once (shared memory bound)
+  const long long per_sm = std::max<long long>(1, std::min<long long>(16, (227 * 1024) / (long long)(smem + 1024)));
+  const unsigned grid = (unsigned)std::min<long long>(items, per_sm * sm_count);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(pooled_conv_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_dependent(pooled_conv_kernel, dim3(grid), dim3(32 * (p.coutp / 16)), smem, st, p);
 }
 
 constexpr size_t kGramSmem = 2 * kGramSlabFloats * sizeof(float);
@@ -496,9 +701,19 @@ cudaError_t gram_reduce_launch(const float* part, const int* box_cta0_host, int 
   return cudaGetLastError();
 }
 
-cudaError_t pool_finalize_launch(const PoolFinParams& p, cudaStream_t st) {
-  pool_finalize_kernel<<<p.Cout, 256, 0, st>>>(p);
-  return cudaGetLastError();
+cudaError_t pool_finalize_launch(const PoolFinParams& p, bool dependent, cudaStream_t st) {
+  size_t smem = (((size_t)p.Cin * p.k[0] * p.k[1] * p.k[2] + 3) & ~(size_t)3) * 4;
+  if (p.lrs) smem += (size_t)p.lag_nrange[0] * p.lag_nrange[1] * p.lag_nrange[2] * kLagSlots * 4;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(pool_finalize_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  if (!dependent) {
+    pool_finalize_kernel<<<p.Cout, 256, smem, st>>>(p);
+    return cudaGetLastError();
+  }
+  return launch_dependent(pool_finalize_kernel, dim3(p.Cout), dim3(256), smem, st, p);
 }
 
 }  // namespace tc3d

@@ -3,6 +3,7 @@
 // the per-channel finalize that folds the BatchNorm affine map and the 1/64
 // of the 4x4x4 pool into the pooled convolution's weights and bias.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -10,6 +11,25 @@
 #include "plan.h"
 
 namespace tc3d {
+
+// Launch a kernel that may start before the previous kernel of the stream
+// ends (programmatic dependent launch); the kernel waits for it with
+// grid_dependency_wait before reading what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Gram CTA: 32q threads per 8x8 Gram block, q = max(1, 8 / blocks), so
 // 256 threads for up to 8 blocks and 320 for the 10 blocks of a 32-entry patch
@@ -39,6 +59,53 @@ struct GramParams {
   int box_cta0[kGramMaxBoxes + 1];  // CTAs [box_cta0[b], box_cta0[b+1]) take box b
 };
 
+// Lag kernel (lag.cu): region sums of x[c, z] and x[c, z] x[c', z + delta]
+// per CTA, then summed over the grid.  Tables as in PoolPlan (lag_*).
+struct LagParams {
+  CUtensorMap xmap;  // x [N, C, L0, L1, L2] as (L2, L1, L0, C, N); box (40, 3, 4, C, 1)
+  float* part;       // [grid][nbox][kLagSlots]
+  float* rs;         // [nbox][kLagSlots]: box sums over the grid
+  int* err;
+  unsigned long long timeout_cycles;
+  int N, L[3];
+  int nseg[3], seg[3][kLagMaxSeg + 1], bulk[3];
+  int nrange[3], range[3][4][2], nbox;  // boxes: a segment range per axis
+  int nb1, nb2;
+  int nc[kLagMaxSeg], cta0[kLagMaxSeg + 1];
+  int grid;
+};
+size_t lag_smem_bytes();
+cudaError_t lag_set_smem();
+// the lag kernel (cin channels, 1..3) and the reduction of its partials
+cudaError_t lag_launch(const LagParams& p, int cin, cudaStream_t st);
+
+// Pooled convolution on CUDA cores (pool.cu): stride 2, at most 3 taps per
+// axis, Cin <= 4, Cout <= 64; y = conv(x, w2) + b2 over P0 x P1 x P2 outputs,
+// input position 2 q + e - pad.  A CTA takes (n, q0, 4 rows of q1, 16 of q2)
+// with one warp per 16 channels; its input box and the weights come in by TMA.
+constexpr int kPooledMaxCin = 4;
+constexpr int kPooledMaxCout = 64;
+constexpr int kPooledRows = 4;     // q1 outputs per CTA (per thread)
+constexpr int kPooledQ2 = 16;      // q2 outputs per CTA (one per lane pair)
+constexpr int kPooledBoxCols = 36; // columns of the input box (33 used + alignment shift)
+constexpr int kPooledBoxRows = 2 * kPooledRows + 1;
+struct PooledParams {
+  CUtensorMap xmap;  // x as (L2, L1, L0, Cin, N); box (36, 9, 3, Cin, 1)
+  const float* w2;   // [ci][e0][e1][e2][coutp], 3 taps per axis (zero past Ke)
+  const float* b2;   // [Cout] or nullptr
+  float* y;          // [N][Cout][P0][P1][P2]
+  int* err;
+  unsigned long long timeout_cycles;
+  int N, Cin, Cout, coutp, P[3], pad[3];
+  int nq1b, nq2b;    // q1 blocks of 4, q2 blocks of 16
+};
+// the kernel takes the problem (sizes, taps, channels); x's tensor map is
+// encoded by the caller
+bool pooled_ok(int Cin, int Cout, const int Ke[3], const int P[3], int N);
+inline int pooled_coutp(int Cout) { return (Cout + 15) / 16 * 16; }
+size_t pooled_smem_bytes(int Cin, int coutp);
+cudaError_t pooled_launch(const PooledParams& p, int sm_count, cudaStream_t st);
+
 struct PoolFinParams {
   const float* w;  // transposed-conv weights [Cin][Cout][k0][k1][k2]
   const float* bias;
@@ -47,7 +114,19 @@ struct PoolFinParams {
   const float* rmean;   // evaluation mode only
   const float* rvar;
   const double* gcls;   // batch statistics: per class combined Gram [ncls][kGramEntries];
-                        // nullptr in evaluation mode
+                        // nullptr in evaluation mode and in lag form
+  const float* lrs;     // batch statistics in lag form: box sums [nbox][kLagSlots]
+  int lag_nseg[3];
+  int lag_nrange[3], lag_range[3][4][2], lag_ridx[3][2][kMaxAxisTaps];
+  unsigned wkmask[3][kMaxAxisTaps];  // per axis and summed tap e: bit k set iff W[k] adds in
+  // per class c and entry i of its patch (rows off[c] .. off[c + 1] - 1 of
+  // all classes): the patch index d, the index of its weight in a channel's
+  // [Cin][k0][k1][k2] block, and in lag form its channel and offset indices
+  // (ci | v0 << 4 | v1 << 8 | v2 << 12) and its box as a first factor
+  int ent_off[9];
+  int ent_d[8 * kGramMaxD], ent_w[8 * kGramMaxD], ent_cv[8 * kGramMaxD], ent_box[8 * kGramMaxD];
+  int pooled_layout;    // 1: w2 as [ci][e0][e1][e2][w2_stride] with 3 taps per axis
+  int w2_stride;        //    (zero past Ke), the pooled-conv kernel's layout
   float* w2;            // [Cout][Cin][Ke0][Ke1][Ke2]
   float* b2;            // [Cout]
   float eps;
@@ -69,6 +148,8 @@ cudaError_t gram_launch(const GramParams& p, unsigned ctas, cudaStream_t st);
 cudaError_t gram_reduce_launch(const float* part, const int* box_cta0_host, int nbox,
                                const int (*cls_coef)[kGramMaxBoxes], int ncls, double* gcls,
                                cudaStream_t st);
-cudaError_t pool_finalize_launch(const PoolFinParams& p, cudaStream_t st);
+// dependent: launched after the lag reduction with programmatic dependent
+// launch (the first kernel of a call is launched normally)
+cudaError_t pool_finalize_launch(const PoolFinParams& p, bool dependent, cudaStream_t st);
 
 }  // namespace tc3d

@@ -131,6 +131,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel of the
+// stream ends; it waits here (a no-op for an ordinary launch) before touching
+// anything that kernel writes.  A kernel signals, once its remaining work no
+// longer delays what comes next, that its dependent may be launched.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ---------------------------------------------------------------------------
 // whole warp; writes the TMEM base address to *dst_smem
