@@ -149,10 +149,20 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def source_hash():
+# the sources each captured kernel is built from (a capture stays valid while
+# they are unchanged)
+KERNEL_SOURCES = {
+    "engine": ["engine.cu", "engine.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
+    "lag": ["lag.cu", "pool.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
+    "pooled": ["pool.cu", "pool.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
+    "direct": ["direct.cu", "direct.cuh", "plan.h", "plan.cpp"],
+}
+
+
+def source_hash(kind="engine"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transposed_conv_epilogues_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -160,7 +170,7 @@ def source_hash():
 
 def recorded_traffic(kernel_workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current sources; else None."""
+    the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic_by_workload.txt")
     try:
         with open(path) as f:
@@ -168,7 +178,7 @@ def recorded_traffic(kernel_workload):
     except Exception:
         return None
     e = t.get(kernel_workload)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(e.get("sources", "engine")):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -309,11 +319,13 @@ def run_ours(args):
             pl = tc.plan_describe(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
                                   wl.dilation, wl.output_padding, wl.groups)
             if pl.get("pool_path"):
-                # [lag kernel + reduction | Gram + reduction] + finalize + pooled conv
-                # (the direct kernel, or weight pack + engine)
+                # batch statistics: lag kernel + reduction + per-channel finalize,
+                # or Gram + reduction + finalize; running statistics: finalize; then the
+                # pooled conv (the direct kernel, or weight pack + engine)
                 pooled = 1 if max(pl["pool_Ke"]) <= 3 and wl.x_shape[1] <= 4 else 2
-                stats = 2 if wl.op == "convT_bn_avgpool" else 0
-                return stats + 1 + pooled
+                if wl.op == "convT_bneval_avgpool":
+                    return 1 + pooled
+                return 3 + pooled
             return 4 if wl.op == "convT_bn_avgpool" else 3
         return {"conv_transpose3d": 3, "conv_maxpool_lse_relu": 2}[wl.op]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

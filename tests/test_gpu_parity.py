@@ -535,15 +535,18 @@ def test_workload_convT_s2p1d2_sampled(tc):
     check(flat[idx], orc.conv_transpose3d_at(x, w, None, idx, **wl.kwargs()), wl.name)
 
 
-def test_workload_convT_bn_avgpool_sampled(tc):
+def test_workload_convT_bn_avgpool_full(tc):
+    """The transposed-conv + BN + pool workload at full size, every one of its
+    3,456,000 outputs against the oracle (whose statistics pass streams the
+    whole transposed conv anyway)."""
     wl, x, w, b = _wl("convT_bn_avgpool")
     y = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), None, None, wl.eps,
                             **wl.kwargs()).cpu().numpy()
     assert y.shape == (64, 16, 15, 15, 15)
     flat = y.ravel()
-    idx = inputs.sample_indices(404, flat.size, 3000)
+    idx = np.arange(flat.size, dtype=np.int64)
     ref = orc.convT_bn_avgpool_at(x, w, b, idx, None, None, wl.eps, **wl.kwargs())
-    check(flat[idx], ref, wl.name)
+    check(flat, ref, wl.name)
     # BatchNorm with gamma 1, beta 0: each channel of the pooled output has
     # mean ~ 0 (pooling averages whole windows of the normalised tensor)
     assert np.all(np.abs(y.mean(axis=(0, 2, 3, 4))) < 0.05)
@@ -589,8 +592,13 @@ def test_workload_conv_maxpool_lse_relu_sampled(tc):
     y = tc.conv_maxpool_lse_relu(_dev(x), _dev(w), _dev(b), **wl.kwargs()).cpu().numpy()
     assert y.shape == (4, 1, 16, 64, 64)
     flat = y.ravel()
+    # random points, plus whole blocks: every pooled output of sample 0 in
+    # depth planes 0 and 15, and of sample 3 in plane 8 (entire engine tiles,
+    # among them the first and the last tiles of the persistent schedule)
+    P = y.shape[2:]
+    blocks = [np.arange(P[1] * P[2]) + ((n * P[0] + d) * P[1] * P[2]) for n, d in ((0, 0), (0, 15), (3, 8))]
     idx = inputs.sample_indices(505, flat.size, 1500)
-    idx = np.concatenate([idx, [0, flat.size - 1]])
+    idx = np.concatenate([idx, [0, flat.size - 1]] + blocks).astype(np.int64)
     check(flat[idx], orc.conv_maxpool_lse_relu_at(x, w, b, idx, **wl.kwargs()), wl.name)
     # logsumexp over 64 channels >= their max, so ReLU rarely clips here
     assert np.all(flat >= 0.0)

@@ -656,8 +656,12 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   fp.w2_stride = pooled_coutp(pb.Cout);
   fp.w2 = w2;
   fp.b2 = b2;
+  // lag form with the pooled conv: the pooled conv applies the scale, so the
+  // summed weights need not wait for the statistics
+  fp.s2 = lrs && pooled ? b2 + pb.Cout : nullptr;
   fp.eps = bn.eps;
   fp.count = (double)pb.N * (double)pl.O[0] * (double)pl.O[1] * (double)pl.O[2];
+  fp.inv_count = 1.0 / fp.count;
   fp.Cin = pb.Cin;
   fp.Cout = pb.Cout;
   fp.V = pp.D / pb.Cin;
@@ -714,10 +718,17 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   }
   for (int c = 0; c < 8; ++c)
     for (int a = 0; a < 3; ++a) fp.cls_r[c][a] = pp.cls_r[c][a];
-  if (pool_finalize_launch(fp, lrs != nullptr, st) != cudaSuccess) return TC3D_ERR_CUDA;
+  if (lrs) {
+    // the lag kernel's box sums, reduced; then the finalize, a CTA per channel
+    if (lag_finalize_launch(fp, lp.part, lp.grid, lp.nbox * kLagSlots, st) != cudaSuccess)
+      return TC3D_ERR_CUDA;
+  } else if (pool_finalize_launch(fp, false, st) != cudaSuccess) {
+    return TC3D_ERR_CUDA;
+  }
   if (pooled) {
     pq.w2 = w2;
     pq.b2 = b2;
+    pq.s2 = fp.s2;
     pq.y = y;
     pq.err = d->err;
     pq.timeout_cycles = timeout_cycles(g_timeout_ns.load());

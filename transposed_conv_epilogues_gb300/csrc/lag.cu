@@ -397,6 +397,12 @@ __global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_
     abort_flag = 0;
     prefetch_tensormap(&p.xmap);
   }
+  // The finalize kernels that follow may be launched now: this kernel is
+  // launched normally (all work queued before it has finished), and what
+  // they do before their own wait reads only the call's inputs and writes
+  // only buffers no kernel of the call before them touches.  Small enough
+  // to share an SM with this kernel, they stage their tables meanwhile.
+  grid_launch_dependents();
   if (threadIdx.x < kLagRows) segw[threadIdx.x] = seg_of(p, 1, kLagRows * b1 + threadIdx.x);
   if (threadIdx.x < 32) segl[threadIdx.x] = seg_of(p, 2, kLagCols * b2 + threadIdx.x);
   __syncthreads();
@@ -456,8 +462,6 @@ __global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_
       if (z0 < zb && lw.ok) lw.template step<1>(win, acc, false, false);
     }
   }
-  // the reduction kernel that follows may be launched now
-  grid_launch_dependents();
   // on a time-out, the chunks still in flight land before the warp leaves
   if (lane == 0 && !lw.ok) {
     for (int q = lw.qc; q < lw.qi; ++q)
@@ -503,48 +507,58 @@ __global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_
   }
   __syncthreads();
   // this CTA's share of every box sum (the boxes whose axis-0 range holds
-  // its segment s0): the sum of its regions inside the box
-  float* dst = p.part + (size_t)blockIdx.x * p.nbox * kLagSlots;
-  const int nr1 = p.nrange[1], nr2 = p.nrange[2];
-  __shared__ int rng[3][4][2];  // (shared: indexing the parameter with per-thread values serialises)
-  if (threadIdx.x < 24) rng[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2] =
-      p.range[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2];
-  __syncthreads();
-  for (int e = threadIdx.x; e < p.nbox * kLagSlots; e += kLagThreads) {
-    const int bx = e / kLagSlots, k = e - bx * kLagSlots;
-    const int c2 = bx % nr2, c1 = (bx / nr2) % nr1, c0 = bx / (nr1 * nr2);
-    float v = 0.f;
-    if (k < NS && s0 >= rng[0][c0][0] && s0 < rng[0][c0][1])
-      for (int s1 = rng[1][c1][0]; s1 < rng[1][c1][1]; ++s1)
-        for (int s2 = rng[2][c2][0]; s2 < rng[2][c2][1]; ++s2) {
-          const int r12 = s1 * p.nseg[2] + s2;
-          v += outa[r12 * kLagSlots + k] + outa[(kLagMaxReg2 + r12) * kLagSlots + k];
+  // its segment s0): the sum of its regions inside the box.  Per slot k:
+  // R[s1][s2] = both halves; T[s1][b2] = sum of R over range b2 of axis 2;
+  // box (b0, b1, b2) = [s0 in range b0] * sum of T over range b1 of axis 1.
+  {
+    const int ns1 = p.nseg[1], ns2 = p.nseg[2];
+    const int nr0 = p.nrange[0], nr1 = p.nrange[1], nr2 = p.nrange[2];
+    __shared__ int rng[3][4][2];
+    if (threadIdx.x < 24)
+      rng[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2] =
+          p.range[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2];
+    __syncthreads();
+    float* dst = p.part + (size_t)blockIdx.x * p.nbox * kLagSlots;
+    const int k = threadIdx.x & 127;
+    if (threadIdx.x < 128) {
+      float T[kLagMaxSeg][4];
+#pragma unroll
+      for (int s1 = 0; s1 < kLagMaxSeg; ++s1)
+#pragma unroll
+        for (int b2 = 0; b2 < 4; ++b2) T[s1][b2] = 0.f;
+      if (k < NS) {
+#pragma unroll
+        for (int s1 = 0; s1 < kLagMaxSeg; ++s1) {
+          if (s1 >= ns1) break;
+#pragma unroll
+          for (int s2 = 0; s2 < kLagMaxSeg; ++s2) {
+            if (s2 >= ns2) break;
+            const int r12 = s1 * ns2 + s2;
+            const float v = outa[r12 * kLagSlots + k] + outa[(kLagMaxReg2 + r12) * kLagSlots + k];
+#pragma unroll
+            for (int b2 = 0; b2 < 4; ++b2)
+              if (b2 < nr2 && s2 >= rng[2][b2][0] && s2 < rng[2][b2][1]) T[s1][b2] += v;
+          }
         }
-    dst[e] = v;
+      }
+      for (int b0 = 0; b0 < nr0; ++b0) {
+        const bool in0 = k < NS && s0 >= rng[0][b0][0] && s0 < rng[0][b0][1];
+        for (int b1 = 0; b1 < nr1; ++b1) {
+#pragma unroll
+          for (int b2 = 0; b2 < 4; ++b2) {
+            if (b2 >= nr2) break;
+            float v = 0.f;
+            if (in0) {
+#pragma unroll
+              for (int s1 = 0; s1 < kLagMaxSeg; ++s1)
+                if (s1 >= rng[1][b1][0] && s1 < rng[1][b1][1]) v += T[s1][b2];
+            }
+            dst[((b0 * nr1 + b1) * nr2 + b2) * kLagSlots + k] = v;
+          }
+        }
+      }
+    }
   }
-}
-
-// rs[e] = sum over the grid's CTAs of part[cta][e], e < nent (box sums):
-// thread
-// (entry, slice g) adds the CTAs g, g + 8, ... in fp32, and the 8 slice sums
-// are added in a fixed pairwise order (the partial sums are box sums of one
-// CTA each; the total stays within a few units of the fp32 rounding)
-__global__ void __launch_bounds__(256) lag_reduce_kernel(const float* __restrict__ part,
-                                                         float* __restrict__ rs, int ctas,
-                                                         int nent) {
-  __shared__ float sh[8][32];
-  grid_dependency_wait();  // the partial sums of the lag kernel
-  grid_launch_dependents();
-  const int el = threadIdx.x & 31, g = threadIdx.x >> 5;
-  const int e = blockIdx.x * 32 + el;
-  float s = 0.f;
-  if (e < nent)
-    for (int i = g; i < ctas; i += 8) s += part[(size_t)i * nent + e];
-  sh[g][el] = s;
-  __syncthreads();
-  if (g == 0 && e < nent)
-    rs[e] = ((sh[0][el] + sh[1][el]) + (sh[2][el] + sh[3][el])) +
-            ((sh[4][el] + sh[5][el]) + (sh[6][el] + sh[7][el]));
 }
 
 }  // namespace
@@ -572,11 +586,7 @@ cudaError_t lag_launch(const LagParams& p, int cin, cudaStream_t st) {
     case 3: lag_stats_kernel<3><<<p.grid, kLagThreads, kLagSmem, st>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int nent = p.nbox * kLagSlots;
-  return launch_dependent(lag_reduce_kernel, dim3((nent + 31) / 32), dim3(256), 0, st,
-                          (const float*)p.part, p.rs, p.grid, nent);
+  return cudaGetLastError();
 }
 
 }  // namespace tc3d

@@ -612,6 +612,18 @@ static void plan_lag(const Plan& bn, PoolPlan& pp) {
   }
   pp.lag_nreg = pp.lag_nseg[0] * pp.lag_nseg[1] * pp.lag_nseg[2];
   pp.lag_nbox = pp.lag_nrange[0] * pp.lag_nrange[1] * pp.lag_nrange[2];
+  // the finalize stages a channel's weights and its gather list in shared
+  // memory, the reduction its entry flags (at most 192 KB each)
+  int rows = 0, pairs = 0;
+  for (int c = 0; c < pp.ncls; ++c) {
+    const int ne = pb.Cin * pp.ntap[0][pp.cls_r[c][0]] * pp.ntap[1][pp.cls_r[c][1]] *
+                   pp.ntap[2][pp.cls_r[c][2]];
+    rows += ne;
+    pairs += ne * (ne + 1) / 2;
+  }
+  if (lag_channel_smem_floats(pb.Cin, pb.k[0] * pb.k[1] * pb.k[2], rows, pairs) * 4 > 192 * 1024 ||
+      lag_reduce_smem_ints(pp.lag_nbox * kLagSlots) * 4 > 192 * 1024)
+    return;
   // work split: the jobs of axis-0 segment s (one per block of 8 rows and 32
   // columns) cost about N (2 len(s) + 1) each (steps, plus the planes every
   // run of consecutive planes loads first); CTAs in proportion, at least
@@ -849,8 +861,8 @@ int make_pool_plan(const Plan& bn, PoolPlan* out) {
                                      (int64_t)pb.Cin * 27 * ((pb.Cout + 15) / 16 * 16)) *
                    4;
   off = round_up(off + pp.ws_w2_bytes, 256);
-  pp.ws_b2_off = off;
-  off = round_up(off + (int64_t)pb.Cout * 4, 256);
+  pp.ws_b2_off = off;  // b2 [Cout], then (lag form) the pooled conv's scale [Cout]
+  off = round_up(off + (int64_t)pb.Cout * 8, 256);
   if (pb.op == OP_CONVT_BN_POOL) {
     pp.ws_gpart_off = off;
     pp.ws_gpart_bytes = (int64_t)kGramMaxCtas * kGramEntries * 4;

@@ -210,6 +210,13 @@ TC3D_HD constexpr int lag_slot(int cin, int c, int c2, int j) {
   for (int cc = 0; cc < c; ++cc) s += 14 + 27 * (cin - 1 - cc);
   return c2 == c ? s + j - 13 : s + 14 + 27 * (c2 - c - 1) + j;
 }
+// dynamic shared memory (4-byte words) of the lag finalize: the reduction's
+// entry flags and list; a channel's weights, and the gather list (the pairs
+// i <= j of every class, then the rows) with its coefficients
+TC3D_HD constexpr int64_t lag_reduce_smem_ints(int nent) { return 2 * (int64_t)nent; }
+TC3D_HD constexpr int64_t lag_channel_smem_floats(int Cin, int kvol, int rows, int pairs) {
+  return (int64_t)Cin * kvol + 2 * ((int64_t)pairs + rows);
+}
 TC3D_HD constexpr int lag_nslots(int cin) { return cin + cin * 14 + 27 * cin * (cin - 1) / 2; }
 static_assert(lag_nslots(kLagMaxCin) <= kLagSlots, "lag slots of 3 channels fit a region row");
 
@@ -240,7 +247,7 @@ struct PoolPlan {
   Plan cplan;                          // its engine plan
   int64_t ws_wpack_off;                // = cplan.ws_wpack_off
   int64_t ws_w2_off, ws_w2_bytes;      // summed, scaled weights [Cout][Cin][Ke0][Ke1][Ke2]
-  int64_t ws_b2_off;                   // folded bias [Cout]
+  int64_t ws_b2_off;                   // folded bias [Cout], then the pooled conv's scale [Cout]
   int64_t ws_gpart_off, ws_gpart_bytes;// per-CTA Gram partials [kGramMaxCtas][kGramEntries] f32
   int64_t ws_gsum_off;                 // per-class combined Gram [8][kGramEntries] f64
 

@@ -361,6 +361,20 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // Finalize: one CTA per output channel.
 // ---------------------------------------------------------------------------
+// Copies n ints of a table held in the kernel parameters into shared memory.
+// Every lane of a warp reads the same element (one broadcast from the
+// constant bank); reads whose index differs across a warp would be
+// serialised, one constant-cache access per distinct address.
+__device__ __forceinline__ void stage_param_ints(int* dst, const int* src, int n) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const bool lead = (threadIdx.x & 31) == 0;
+#pragma unroll 4
+  for (int r = warp; r < n; r += nw) {
+    const int v = src[r];
+    if (lead) dst[r] = v;
+  }
+}
+
 __device__ __forceinline__ void block_sum2_pool(double& a, double& b) {
   __shared__ double sa[256], sb[256];
   sa[threadIdx.x] = a;
@@ -413,13 +427,11 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
     __shared__ int e_d[8 * kGramMaxD], e_w[8 * kGramMaxD], e_cv[8 * kGramMaxD],
         e_box[8 * kGramMaxD], e_off[9];
     const int nrows = p.ent_off[p.ncls];
-    for (int r = threadIdx.x; r < nrows; r += 256) {
-      e_d[r] = p.ent_d[r];
-      e_w[r] = p.ent_w[r];
-      e_cv[r] = p.ent_cv[r];
-      e_box[r] = p.ent_box[r];
-    }
-    if (threadIdx.x < 9) e_off[threadIdx.x] = p.ent_off[threadIdx.x];
+    stage_param_ints(e_d, p.ent_d, nrows);
+    stage_param_ints(e_w, p.ent_w, nrows);
+    stage_param_ints(e_cv, p.ent_cv, nrows);
+    stage_param_ints(e_box, p.ent_box, nrows);
+    stage_param_ints(e_off, p.ent_off, 9);
     __syncthreads();
     float f1 = 0.f, f2 = 0.f;
     for (int row = threadIdx.x; row < nrows; row += 256) {
@@ -461,22 +473,24 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
   }
   block_sum2_pool(s1, s2);
   if (threadIdx.x == 0) {
-    const double g = p.gamma ? (double)p.gamma[co] : 1.0, be = p.beta ? (double)p.beta[co] : 0.0;
-    double scale, shift;
+    // the square root in float (fp64 square roots and divisions are slow on
+    // this part); mean and variance in double
+    const float g = p.gamma ? p.gamma[co] : 1.f, be = p.beta ? p.beta[co] : 0.f;
+    float scale, shift;
     if (batch) {
       // y = (pooled mean of t0 - mean of t0) * scale + beta  (the bias cancels)
-      const double mean = s1 / p.count;
-      double var = s2 / p.count - mean * mean;
+      const double mean = s1 * p.inv_count;
+      double var = s2 * p.inv_count - mean * mean;
       if (var < 0.0) var = 0.0;
-      scale = g / sqrt(var + (double)p.eps);
-      shift = be - mean * scale;
+      scale = g * rsqrtf((float)var + p.eps);
+      shift = be - (float)mean * scale;
     } else {
-      const double bv = p.bias ? (double)p.bias[co] : 0.0;
-      scale = g / sqrt((double)p.rvar[co] + (double)p.eps);
-      shift = be + (bv - (double)p.rmean[co]) * scale;
+      const float bv = p.bias ? p.bias[co] : 0.f;
+      scale = g * rsqrtf(p.rvar[co] + p.eps);
+      shift = be + (bv - p.rmean[co]) * scale;
     }
-    s_scale = (float)(scale / 64.0);
-    p.b2[co] = (float)shift;
+    s_scale = scale * (1.0f / 64.0f);
+    p.b2[co] = shift;
   }
   __syncthreads();
   // summed weights: W'[e] = sum of W[k] over taps k with 2(e_min + e) - p + d k
@@ -486,8 +500,8 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
             K2 = p.pooled_layout ? 3 : p.Ke[2];
   const int kv = K0 * K1 * K2;
   __shared__ unsigned wkm[3 * kMaxAxisTaps];
-  if (threadIdx.x < 3 * kMaxAxisTaps)
-    wkm[threadIdx.x] = p.wkmask[threadIdx.x / kMaxAxisTaps][threadIdx.x % kMaxAxisTaps];
+  stage_param_ints(reinterpret_cast<int*>(wkm), reinterpret_cast<const int*>(&p.wkmask[0][0]),
+                   3 * kMaxAxisTaps);
   __syncthreads();
   for (int q = threadIdx.x; q < p.Cin * kv; q += 256) {
     const int ci = q / kv, e = q % kv;
@@ -506,6 +520,309 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
     else
       p.w2[((long long)co * p.Cin + ci) * kv + e] = acc * s_scale;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Lag form, batch statistics: the reduction of the lag kernel's per-CTA box
+// sums and the finalize of each channel.
+//   Per class c with entries i, j (rows r0 + i of the entry tables), the
+//   statistics need G_c[i, j] for i <= j (G_c is symmetric: the box sum of
+//   the factor earlier in patch order at lag v_later - v_earlier) and s_c[i],
+//   the first-order sums: the "gather list", ntri pairs then the rows.
+//   w^T G w = sum over i <= j of (i == j ? 1 : 2) w_i w_j G_ij, so a channel's
+//   statistics are two dot products of the gathered values with per-channel
+//   coefficients.
+// Both kernels are small (128 threads, at most 32 registers) so that they
+// share the SMs with the lag kernel, launched while it runs: everything that
+// does not need the box sums (the tables from the kernel parameters, the
+// gather list, the coefficients, the summed weights) is done then.  After
+// their waits, on the call's critical path, each reaches L2 once with all of
+// its loads in flight.
+// ---------------------------------------------------------------------------
+constexpr int kLfThreads = 128;
+constexpr int kLfMaxRows = 8 * kGramMaxD;
+constexpr int kLrEnt = 8;              // reduction: entries per step of a CTA
+constexpr int kLrGroups = kLfThreads / kLrEnt;
+constexpr int kLrBatch = 10;           // reduction loads in flight per thread
+constexpr int kLcBatch = 8;            // channel: gather loads in flight per thread
+
+// the entry tables in shared memory and the per-class offsets (pairs i <= j)
+struct LagTabs {
+  int e_d[kLfMaxRows], e_w[kLfMaxRows], e_cv[kLfMaxRows], e_box[kLfMaxRows];
+  int e_off[9], toff[9];
+};
+
+__device__ void lag_stage_tabs(const PoolFinParams& p, LagTabs& t) {
+  const int nrows = p.ent_off[p.ncls];
+  stage_param_ints(t.e_d, p.ent_d, nrows);
+  stage_param_ints(t.e_w, p.ent_w, nrows);
+  stage_param_ints(t.e_cv, p.ent_cv, nrows);
+  stage_param_ints(t.e_box, p.ent_box, nrows);
+  stage_param_ints(t.e_off, p.ent_off, 9);
+  if (threadIdx.x == 0) {
+    t.toff[0] = 0;
+    for (int c = 0; c < p.ncls; ++c) {
+      const int ne = p.ent_off[c + 1] - p.ent_off[c];
+      t.toff[c + 1] = t.toff[c] + ne * (ne + 1) / 2;
+    }
+  }
+}
+
+// item q of the gather list: its index into the box sums, and its class
+// rows (i, j; i == j == -1 - row for a first-order sum)
+__device__ __forceinline__ int lag_gather_item(const PoolFinParams& p, const LagTabs& t, int ntri,
+                                               int q, int& ri, int& rj) {
+  if (q >= ntri) {
+    const int row = q - ntri;
+    ri = rj = -1 - row;
+    return t.e_box[row] * kLagSlots + (t.e_cv[row] & 15);
+  }
+  int c = 0;
+  while (q >= t.toff[c + 1]) ++c;
+  const int r0 = t.e_off[c], ne = t.e_off[c + 1] - r0;
+  int l = q - t.toff[c], i = 0;
+  while (l >= ne - i) {  // row i of the upper triangle holds ne - i pairs
+    l -= ne - i;
+    ++i;
+  }
+  const int j = i + l;
+  ri = r0 + i;
+  rj = r0 + j;
+  const int first = t.e_d[ri] <= t.e_d[rj] ? ri : rj, second = first == ri ? rj : ri;
+  const int ca = t.e_cv[first], cb = t.e_cv[second];
+  const int jl = 9 * (((cb >> 4) & 15) - ((ca >> 4) & 15) + 1) +
+                 3 * (((cb >> 8) & 15) - ((ca >> 8) & 15) + 1) +
+                 (((cb >> 12) & 15) - ((ca >> 12) & 15) + 1);
+  return t.e_box[first] * kLagSlots + lag_slot(p.Cin, ca & 15, cb & 15, jl);
+}
+
+// summed weights (ci, e) of channel co, times sc; wc: the channel's weights
+// [Cin][k0][k1][k2]
+__device__ __forceinline__ void lag_fold_channel(const PoolFinParams& p, const float* wc,
+                                                 const unsigned* wkm, int co, float sc) {
+  const int kvol = p.k[0] * p.k[1] * p.k[2];
+  const int K0 = p.pooled_layout ? 3 : p.Ke[0], K1 = p.pooled_layout ? 3 : p.Ke[1],
+            K2 = p.pooled_layout ? 3 : p.Ke[2];
+  const int kv = K0 * K1 * K2;
+  for (int q = threadIdx.x; q < p.Cin * kv; q += kLfThreads) {
+    const int ci = q / kv, e = q - ci * kv;
+    const int ee[3] = {e / (K1 * K2), (e / K2) % K1, e % K2};
+    float acc = 0.f;
+    if (ee[0] < p.Ke[0] && ee[1] < p.Ke[1] && ee[2] < p.Ke[2]) {
+      // taps k of each axis with 2 (e_min + e) - p + d k in [0, 3]
+      const unsigned m0 = wkm[ee[0]], m1 = wkm[kMaxAxisTaps + ee[1]], m2 = wkm[2 * kMaxAxisTaps + ee[2]];
+      const float* w = wc + ci * kvol;
+      for (unsigned a = m0; a; a &= a - 1)
+        for (unsigned b = m1; b; b &= b - 1)
+          for (unsigned cc = m2; cc; cc &= cc - 1)
+            acc += w[((__ffs(a) - 1) * p.k[1] + (__ffs(b) - 1)) * p.k[2] + (__ffs(cc) - 1)];
+    }
+    if (p.pooled_layout)
+      p.w2[(long long)q * p.w2_stride + co] = acc * sc;
+    else
+      p.w2[((long long)co * p.Cin + ci) * kv + e] = acc * sc;
+  }
+}
+
+// Reduction: rs[e] = sum over the lag kernel's CTAs of part[cta][e] for the
+// entries e the gather list reads.  Before the wait every CTA builds the
+// list of those entries (flags, then a block scan), in ascending order; after
+// it, a CTA takes 8 entries per step, thread (g, k) adding the CTAs g, g + 16,
+// ... of entry k in fp32 and the 16 slice sums added in a fixed pairwise
+// order (the partial sums are box sums of one CTA each; the total stays
+// within a few units of the fp32 rounding).
+__global__ void __launch_bounds__(kLfThreads, 16) lag_reduce_kernel(const __grid_constant__ PoolFinParams p,
+                                                                   const float* __restrict__ part,
+                                                                   int ctas, int nent) {
+  extern __shared__ int lr_smem[];  // [nent] flags, then the list of needed entries
+  __shared__ LagTabs t;
+  __shared__ int wsum[kLfThreads / 32], nneed;
+  __shared__ float sh[kLrGroups][kLrEnt];
+  int* flag = lr_smem;
+  int* list = lr_smem + nent;
+  // the kernels of the call before this one do not write p.lrs, and the
+  // following one reads it only after its own wait
+  grid_launch_dependents();
+  lag_stage_tabs(p, t);
+  for (int e = threadIdx.x; e < nent; e += kLfThreads) flag[e] = 0;
+  __syncthreads();
+  const int nrows = t.e_off[p.ncls], ntri = t.toff[p.ncls];
+  for (int q = threadIdx.x; q < ntri + nrows; q += kLfThreads) {
+    int ri, rj;
+    flag[lag_gather_item(p, t, ntri, q, ri, rj)] = 1;
+  }
+  __syncthreads();
+  // block scan of the flags over contiguous chunks of the entries
+  const int per = (nent + kLfThreads - 1) / kLfThreads;
+  const int e0 = threadIdx.x * per, e1 = min(nent, e0 + per);
+  int cnt = 0;
+  for (int e = e0; e < e1; ++e) cnt += flag[e];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int base = incl - cnt;
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  if (threadIdx.x == kLfThreads - 1) nneed = base + cnt;
+  for (int e = e0; e < e1; ++e)
+    if (flag[e]) list[base++] = e;
+  __syncthreads();
+
+  grid_dependency_wait();  // the lag kernel's partial sums
+  const int k = threadIdx.x % kLrEnt, g = threadIdx.x / kLrEnt;
+  for (int s0 = blockIdx.x * kLrEnt; s0 < nneed; s0 += gridDim.x * kLrEnt) {
+    const int s = s0 + k;
+    const int e = s < nneed ? list[s] : 0;
+    float v = 0.f;
+    if (s < nneed) {
+      for (int i0 = g; i0 < ctas; i0 += kLrGroups * kLrBatch) {
+        float r[kLrBatch];
+#pragma unroll
+        for (int u = 0; u < kLrBatch; ++u) {
+          const int i = i0 + kLrGroups * u;
+          r[u] = i < ctas ? part[(size_t)i * nent + e] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kLrBatch; ++u) v += r[u];
+      }
+    }
+    sh[g][k] = v;
+    __syncthreads();
+    if (g == 0 && s < nneed) {
+      float a[kLrGroups];
+#pragma unroll
+      for (int u = 0; u < kLrGroups; ++u) a[u] = sh[u][k];
+#pragma unroll
+      for (int w = kLrGroups / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int u = 0; u < w; ++u) a[u] += a[u + w];
+      const_cast<float*>(p.lrs)[e] = a[0];
+    }
+    __syncthreads();
+  }
+}
+
+// Finalize of channel co = blockIdx.x: before the wait, the gather list and
+// the channel's coefficients (and, with the pooled layout, its unscaled
+// summed weights: the pooled conv applies scale / 64 in its epilogue);
+// after it, the gather and the two dot products, mean and biased variance,
+// the BatchNorm affine; for the engine's layout also the summed weights with
+// scale / 64 folded in.
+__global__ void __launch_bounds__(kLfThreads, 16) lag_channel_kernel(const __grid_constant__ PoolFinParams p) {
+  extern __shared__ float lc_smem[];
+  __shared__ LagTabs t;
+  __shared__ unsigned wkm[3 * kMaxAxisTaps];
+  __shared__ float red[2][kLfThreads / 32];
+  __shared__ float s_sc;
+  const int co = blockIdx.x;
+  const int kvol = p.k[0] * p.k[1] * p.k[2];
+  const int wpc = p.Cin * kvol;  // weights of the channel
+  float* wc = lc_smem;           // [Cin][kvol]
+  // the pooled conv reads w2, s2 and b2 only after its wait on this kernel
+  grid_launch_dependents();
+  for (int e = threadIdx.x; e < wpc; e += kLfThreads) {
+    const int ci = e / kvol, kk = e - ci * kvol;
+    wc[e] = __ldg(p.w + ((long long)ci * p.Cout + co) * kvol + kk);
+  }
+  lag_stage_tabs(p, t);
+  stage_param_ints(reinterpret_cast<int*>(wkm), reinterpret_cast<const int*>(&p.wkmask[0][0]),
+                   3 * kMaxAxisTaps);
+  __syncthreads();
+  const int nrows = t.e_off[p.ncls], ntri = t.toff[p.ncls], ngat = ntri + nrows;
+  int* gidx = reinterpret_cast<int*>(wc + wpc);      // [ngat]
+  float* coef = reinterpret_cast<float*>(gidx + ngat);  // [ngat]
+  for (int q = threadIdx.x; q < ngat; q += kLfThreads) {
+    int ri, rj;
+    gidx[q] = lag_gather_item(p, t, ntri, q, ri, rj);
+    if (ri < 0)
+      coef[q] = wc[t.e_w[-1 - ri]];
+    else
+      coef[q] = wc[t.e_w[ri]] * wc[t.e_w[rj]] * (ri == rj ? 1.f : 2.f);
+  }
+  const bool unscaled = p.s2 != nullptr;
+  if (unscaled) lag_fold_channel(p, wc, wkm, co, 1.f);
+  __syncthreads();
+
+  grid_dependency_wait();  // the box sums
+  float f1 = 0.f, f2 = 0.f;
+  for (int q0 = threadIdx.x; q0 < ngat; q0 += kLfThreads * kLcBatch) {
+    float v[kLcBatch];
+#pragma unroll
+    for (int u = 0; u < kLcBatch; ++u) {
+      const int q = q0 + kLfThreads * u;
+      v[u] = q < ngat ? __ldcg(p.lrs + gidx[q]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kLcBatch; ++u) {
+      const int q = q0 + kLfThreads * u;
+      if (q < ntri)
+        f2 = fmaf(coef[q], v[u], f2);
+      else if (q < ngat)
+        f1 = fmaf(coef[q], v[u], f1);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    f1 += __shfl_xor_sync(0xffffffffu, f1, o);
+    f2 += __shfl_xor_sync(0xffffffffu, f2, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = f1;
+    red[1][threadIdx.x >> 5] = f2;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float t1 = (red[0][0] + red[0][1]) + (red[0][2] + red[0][3]);
+    const float t2 = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+    // y = (pooled mean of t0 - mean of t0) * scale + beta (the bias
+    // cancels); the square root in float
+    const double mean = (double)t1 * p.inv_count;
+    double var = (double)t2 * p.inv_count - mean * mean;
+    if (var < 0.0) var = 0.0;
+    const float scale = (p.gamma ? p.gamma[co] : 1.f) * rsqrtf((float)var + p.eps);
+    s_sc = scale * (1.0f / 64.0f);
+    if (unscaled) p.s2[co] = scale * (1.0f / 64.0f);
+    p.b2[co] = (p.beta ? p.beta[co] : 0.f) - (float)mean * scale;
+  }
+  if (!unscaled) {
+    __syncthreads();
+    lag_fold_channel(p, wc, wkm, co, s_sc);
+  }
+}
+
+cudaError_t lag_finalize_launch(const PoolFinParams& p, const float* part, int ctas, int nent,
+                                cudaStream_t st) {
+  const int nrows = p.ent_off[p.ncls];
+  int ntri = 0;
+  for (int c = 0; c < p.ncls; ++c) {
+    const int ne = p.ent_off[c + 1] - p.ent_off[c];
+    ntri += ne * (ne + 1) / 2;
+  }
+  const size_t smem_r = (size_t)lag_reduce_smem_ints(nent) * 4;
+  const size_t smem_c =
+      (size_t)lag_channel_smem_floats(p.Cin, p.k[0] * p.k[1] * p.k[2], nrows, ntri) * 4;
+  if (smem_r > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(lag_reduce_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+    if (e != cudaSuccess) return e;
+  }
+  if (smem_c > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(lag_channel_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
+    if (e != cudaSuccess) return e;
+  }
+  // reduction CTAs: a step of 8 entries each for at most every gathered value
+  // (the needed entries are at most that many)
+  const int steps = (ntri + nrows + kLrEnt - 1) / kLrEnt;
+  const cudaError_t e = launch_dependent(lag_reduce_kernel, dim3(std::min(steps, 96)),
+                                         dim3(kLfThreads), smem_r, st, p, part, ctas, nent);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(lag_channel_kernel, dim3(p.Cout), dim3(kLfThreads), smem_c, st, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -633,10 +950,11 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
         const int co = co0 + c;
         if (co >= p.Cout) break;
         const float bb = p.b2 ? __ldg(p.b2 + co) : 0.f;
+        const float sc = p.s2 ? __ldg(p.s2 + co) : 1.f;
         float* yo = p.y + ((long long)n * p.Cout + co) * pv + (long long)q0 * p.P[1] * p.P[2] + q2;
 #pragma unroll
         for (int i = 0; i < kPooledRows; ++i)
-          if (q1a + i < p.P[1]) yo[(long long)(q1a + i) * p.P[2]] = acc[i][c] + bb;
+          if (q1a + i < p.P[1]) yo[(long long)(q1a + i) * p.P[2]] = fmaf(acc[i][c], sc, bb);
       }
     }
   }

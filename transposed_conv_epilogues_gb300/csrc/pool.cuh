@@ -76,7 +76,7 @@ struct LagParams {
 };
 size_t lag_smem_bytes();
 cudaError_t lag_set_smem();
-// the lag kernel (cin channels, 1..3) and the reduction of its partials
+// the lag kernel (cin channels, 1..3)
 cudaError_t lag_launch(const LagParams& p, int cin, cudaStream_t st);
 
 // Pooled convolution on CUDA cores (pool.cu): stride 2, at most 3 taps per
@@ -93,6 +93,7 @@ struct PooledParams {
   CUtensorMap xmap;  // x as (L2, L1, L0, Cin, N); box (36, 9, 3, Cin, 1)
   const float* w2;   // [ci][e0][e1][e2][coutp], 3 taps per axis (zero past Ke)
   const float* b2;   // [Cout] or nullptr
+  const float* s2;   // [Cout] scale of the sums (y = s2 * acc + b2), or nullptr (1)
   float* y;          // [N][Cout][P0][P1][P2]
   int* err;
   unsigned long long timeout_cycles;
@@ -129,8 +130,11 @@ struct PoolFinParams {
   int w2_stride;        //    (zero past Ke), the pooled-conv kernel's layout
   float* w2;            // [Cout][Cin][Ke0][Ke1][Ke2]
   float* b2;            // [Cout]
+  float* s2;            // lag form with the pooled layout: [Cout] scale / 64, which the
+                        // pooled conv applies (w2 then holds unscaled sums); else nullptr
   float eps;
   double count;         // outputs per channel, N * O0 * O1 * O2
+  double inv_count;     // 1 / count
   int Cin, Cout, k[3], pad[3], dil[3];
   int V, nU[3];
   int ntap[3][2], tap_k[3][2][kMaxAxisTaps], tap_u[3][2][kMaxAxisTaps];
@@ -148,6 +152,12 @@ cudaError_t gram_launch(const GramParams& p, unsigned ctas, cudaStream_t st);
 cudaError_t gram_reduce_launch(const float* part, const int* box_cta0_host, int nbox,
                                const int (*cls_coef)[kGramMaxBoxes], int ncls, double* gcls,
                                cudaStream_t st);
+// Lag form, after the lag kernel (dependent launches): the reduction of its
+// per-CTA box sums part[ctas][nent] into p.lrs (the entries the statistics
+// read), then the finalize of every channel, a CTA each: statistics, b2 and
+// s2 (or, without s2, the weights w2 with the scale folded in)
+cudaError_t lag_finalize_launch(const PoolFinParams& p, const float* part, int ctas, int nent,
+                                cudaStream_t st);
 // dependent: launched after the lag reduction with programmatic dependent
 // launch (the first kernel of a call is launched normally)
 cudaError_t pool_finalize_launch(const PoolFinParams& p, bool dependent, cudaStream_t st);
