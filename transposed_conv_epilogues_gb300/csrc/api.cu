@@ -631,14 +631,6 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   fp.rvar = bn.rvar;
   fp.gcls = gsum;
   fp.lrs = lrs;
-  for (int a = 0; a < 3; ++a) {
-    fp.lag_nseg[a] = pp.lag_nseg[a];
-    fp.lag_nrange[a] = pp.lag_nrange[a];
-    for (int k = 0; k < 4; ++k)
-      for (int e = 0; e < 2; ++e) fp.lag_range[a][k][e] = pp.lag_range[a][k][e];
-    for (int r = 0; r < 2; ++r)
-      for (int i = 0; i < kMaxAxisTaps; ++i) fp.lag_ridx[a][r][i] = pp.lag_ridx[a][r][i];
-  }
   // the pooled conv: on CUDA cores where its kernel takes the problem (few
   // channels, at most 3 taps per axis, TMA-loadable x), else through the
   // engine; the finalize writes the summed weights in the layout it reads
@@ -659,6 +651,7 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
   // lag form with the pooled conv: the pooled conv applies the scale, so the
   // summed weights need not wait for the statistics
   fp.s2 = lrs && pooled ? b2 + pb.Cout : nullptr;
+  fp.pool_ctr = pooled ? reinterpret_cast<unsigned*>(b2 + 2 * pb.Cout) : nullptr;
   fp.eps = bn.eps;
   fp.count = (double)pb.N * (double)pl.O[0] * (double)pl.O[1] * (double)pl.O[2];
   fp.inv_count = 1.0 / fp.count;
@@ -722,13 +715,14 @@ int run_pool(int op, const CallPlan& cp, const float* x, const float* w, const f
     // the lag kernel's box sums, reduced; then the finalize, a CTA per channel
     if (lag_finalize_launch(fp, lp.part, lp.grid, lp.nbox * kLagSlots, st) != cudaSuccess)
       return TC3D_ERR_CUDA;
-  } else if (pool_finalize_launch(fp, false, st) != cudaSuccess) {
+  } else if (pool_finalize_launch(fp, st) != cudaSuccess) {
     return TC3D_ERR_CUDA;
   }
   if (pooled) {
     pq.w2 = w2;
     pq.b2 = b2;
     pq.s2 = fp.s2;
+    pq.ctr = fp.pool_ctr;
     pq.y = y;
     pq.err = d->err;
     pq.timeout_cycles = timeout_cycles(g_timeout_ns.load());

@@ -861,8 +861,10 @@ int make_pool_plan(const Plan& bn, PoolPlan* out) {
                                      (int64_t)pb.Cin * 27 * ((pb.Cout + 15) / 16 * 16)) *
                    4;
   off = round_up(off + pp.ws_w2_bytes, 256);
-  pp.ws_b2_off = off;  // b2 [Cout], then (lag form) the pooled conv's scale [Cout]
-  off = round_up(off + (int64_t)pb.Cout * 8, 256);
+  // b2 [Cout], then (lag form) the pooled conv's scale [Cout], then the
+  // pooled conv's item counter
+  pp.ws_b2_off = off;
+  off = round_up(off + (int64_t)pb.Cout * 8 + 16, 256);
   if (pb.op == OP_CONVT_BN_POOL) {
     pp.ws_gpart_off = off;
     pp.ws_gpart_bytes = (int64_t)kGramMaxCtas * kGramEntries * 4;

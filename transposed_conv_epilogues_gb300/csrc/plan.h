@@ -247,7 +247,8 @@ struct PoolPlan {
   Plan cplan;                          // its engine plan
   int64_t ws_wpack_off;                // = cplan.ws_wpack_off
   int64_t ws_w2_off, ws_w2_bytes;      // summed, scaled weights [Cout][Cin][Ke0][Ke1][Ke2]
-  int64_t ws_b2_off;                   // folded bias [Cout], then the pooled conv's scale [Cout]
+  int64_t ws_b2_off;                   // folded bias [Cout], the pooled conv's scale [Cout]
+                                       // and its item counter
   int64_t ws_gpart_off, ws_gpart_bytes;// per-CTA Gram partials [kGramMaxCtas][kGramEntries] f32
   int64_t ws_gsum_off;                 // per-class combined Gram [8][kGramEntries] f64
 

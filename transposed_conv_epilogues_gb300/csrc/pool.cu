@@ -396,27 +396,19 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
   extern __shared__ float fin_smem[];  // this channel's weights [Cin][k0][k1][k2]
   __shared__ float s_scale;
   double s1 = 0.0, s2 = 0.0;
-  const bool batch = p.gcls != nullptr || p.lrs != nullptr;
-  const int nr1 = p.lag_nrange[1], nr2 = p.lag_nrange[2];
-  // this channel's weights [Cin][k0][k1][k2]; in lag form then the box sums
-  // [box][slot] (a box is one segment range per axis: the z range of a class
-  // entry's first factor)
+  const bool batch = p.gcls != nullptr;
   float* wsh = fin_smem;
   const int kvol = p.k[0] * p.k[1] * p.k[2];
-  float* bs = fin_smem + ((p.Cin * kvol + 3) & ~3);
   for (int e = threadIdx.x; e < p.Cin * kvol; e += 256) {
     const int ci = e / kvol, kk = e - ci * kvol;
     wsh[e] = __ldg(p.w + ((long long)ci * p.Cout + co) * kvol + kk);
   }
-  // (launched dependent only after the lag reduction, which writes no
-  // weights; a dependent is signalled only after this wait, so no later
-  // kernel of the call runs ahead of work queued before the call)
+  // (a dependent is signalled only after this wait, so no later kernel of
+  // the call runs ahead of work queued before the call)
   grid_dependency_wait();  // the statistics of the kernels before
   grid_launch_dependents();
-  if (p.lrs) {
-    const int nb = p.lag_nrange[0] * nr1 * nr2 * kLagSlots;
-    for (int e = threadIdx.x; e < nb; e += 256) bs[e] = __ldg(p.lrs + e);
-  }
+  // the pooled conv reads its counter only after its wait on this kernel
+  if (co == 0 && threadIdx.x == 0 && p.pool_ctr) *p.pool_ctr = 0u;
   __syncthreads();
   if (batch) {
     // class sums of the bias-free transposed conv: w_r . s_r and w_r^T G_r w_r
@@ -424,52 +416,26 @@ __global__ void __launch_bounds__(256) pool_finalize_kernel(const __grid_constan
     // entries of all classes (entry i of class c) and its pairs (i, j).  The
     // entry tables are read from shared memory: indexing kernel parameters
     // with values that differ across a warp would serialise the reads.
-    __shared__ int e_d[8 * kGramMaxD], e_w[8 * kGramMaxD], e_cv[8 * kGramMaxD],
-        e_box[8 * kGramMaxD], e_off[9];
+    __shared__ int e_d[8 * kGramMaxD], e_w[8 * kGramMaxD], e_off[9];
     const int nrows = p.ent_off[p.ncls];
     stage_param_ints(e_d, p.ent_d, nrows);
     stage_param_ints(e_w, p.ent_w, nrows);
-    stage_param_ints(e_cv, p.ent_cv, nrows);
-    stage_param_ints(e_box, p.ent_box, nrows);
     stage_param_ints(e_off, p.ent_off, 9);
     __syncthreads();
-    float f1 = 0.f, f2 = 0.f;
     for (int row = threadIdx.x; row < nrows; row += 256) {
       int c = 0;
       while (row >= e_off[c + 1]) ++c;
       const int r0 = e_off[c], ne = e_off[c + 1] - r0;
       const int di = e_d[row];
       const float wi = wsh[e_w[row]];
-      if (p.lrs) {
-        const int cvi = e_cv[row];
-        f1 = fmaf(wi, bs[e_box[row] * kLagSlots + (cvi & 15)], f1);
-        float g = 0.f;
-        for (int j = 0; j < ne; ++j) {
-          const int dj = e_d[r0 + j];
-          // the factor earlier in patch order (channel-major, offsets in
-          // lexicographic order) at lag v_later - v_earlier; offsets are
-          // consecutive, so index differences are offset differences
-          const int first = di <= dj ? row : r0 + j, second = di <= dj ? r0 + j : row;
-          const int ca = e_cv[first], cb = e_cv[second];
-          const int jl = 9 * (((cb >> 4) & 15) - ((ca >> 4) & 15) + 1) +
-                         3 * (((cb >> 8) & 15) - ((ca >> 8) & 15) + 1) +
-                         (((cb >> 12) & 15) - ((ca >> 12) & 15) + 1);
-          g = fmaf(wsh[e_w[r0 + j]],
-                   bs[e_box[first] * kLagSlots + lag_slot(p.Cin, ca & 15, cb & 15, jl)], g);
-        }
-        f2 = fmaf(wi, g, f2);
-      } else {
-        const double* G = p.gcls + (size_t)c * kGramEntries;
-        s1 += (double)wi * G[kGramMaxD * kGramMaxD + di];
-        for (int j = 0; j < ne; ++j) {
-          const int dj = e_d[r0 + j];
-          const int lo = (di >> 3) <= (dj >> 3) ? di : dj, hi = lo == di ? dj : di;
-          s2 += (double)wi * (double)wsh[e_w[r0 + j]] * G[lo * kGramMaxD + hi];
-        }
+      const double* G = p.gcls + (size_t)c * kGramEntries;
+      s1 += (double)wi * G[kGramMaxD * kGramMaxD + di];
+      for (int j = 0; j < ne; ++j) {
+        const int dj = e_d[r0 + j];
+        const int lo = (di >> 3) <= (dj >> 3) ? di : dj, hi = lo == di ? dj : di;
+        s2 += (double)wi * (double)wsh[e_w[r0 + j]] * G[lo * kGramMaxD + hi];
       }
     }
-    s1 += (double)f1;
-    s2 += (double)f2;
   }
   block_sum2_pool(s1, s2);
   if (threadIdx.x == 0) {
@@ -723,8 +689,10 @@ __global__ void __launch_bounds__(kLfThreads, 16) lag_channel_kernel(const __gri
   const int kvol = p.k[0] * p.k[1] * p.k[2];
   const int wpc = p.Cin * kvol;  // weights of the channel
   float* wc = lc_smem;           // [Cin][kvol]
-  // the pooled conv reads w2, s2 and b2 only after its wait on this kernel
+  // the pooled conv reads w2, s2, b2 and its counter only after its wait on
+  // this kernel
   grid_launch_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.pool_ctr) *p.pool_ctr = 0u;
   for (int e = threadIdx.x; e < wpc; e += kLfThreads) {
     const int ci = e / kvol, kk = e - ci * kvol;
     wc[e] = __ldg(p.w + ((long long)ci * p.Cout + co) * kvol + kk);
@@ -826,18 +794,22 @@ cudaError_t lag_finalize_launch(const PoolFinParams& p, const float* part, int c
 }
 
 // ---------------------------------------------------------------------------
-// Pooled convolution on CUDA cores: y[n, co, q] = b2[co] + sum over ci and
-// e of w2[ci, e, co] x[n, ci, 2 q + e - pad] (stride 2, 3 taps per axis with
-// zero weights past Ke, at most 4 input channels).  An item is (sample n,
-// q0, 4 rows of q1, 16 of q2) for all channels, one warp per 16 channels.
-// CTAs are persistent: the weights come in once by a bulk copy, the items'
-// input boxes (36 columns x 9 rows x 3 planes x Cin, zero outside x; the x
-// start rounded down to 16 bytes, so each row starts `shift` columns in) by
-// TMA into two buffers, the next item's box landing while the current one is
-// used.  Lane (g, q2) computes the 4 rows of its q2 for 8 channels: per (ci,
-// e0, e2) it reads the 9 inputs of its column (lanes read consecutive even
-// columns: distinct banks) and, per e1, 8 weights (two 16-byte broadcasts),
-// 32 multiply-adds each.
+// Pooled convolution on CUDA cores: y[n, co, q] = s2[co] (sum over ci and e
+// of w2[ci, e, co] x[n, ci, 2 q + e - pad]) + b2[co] (stride 2, 3 taps per
+// axis with zero weights past Ke, at most 4 input channels).  An item is
+// (sample n, q0, 4 rows of q1, 16 of q2) for all channels, one warp per 16
+// channels.  CTAs are persistent: the weights come in once by a bulk copy,
+// the items' input boxes (36 columns x 9 rows x 3 planes x Cin, zero outside
+// x; the x start rounded down to 16 bytes, so each row starts `shift`
+// columns in) by TMA into two buffers, the next item's box landing while the
+// current one is used.  A CTA's first two items are blockIdx.x and
+// blockIdx.x + gridDim.x; the later ones come from a counter (zeroed by the
+// finalize before this kernel), so CTAs that finish early take more.
+// Lane (g, q2) computes the 4 rows of its q2 for 8 channels: per (ci, e0,
+// e2) it reads the 9 inputs of its column (lanes read consecutive even
+// columns: distinct banks; both halves of the warp read the same ones) and,
+// per e1, 8 weights (two 16-byte broadcasts), 32 multiply-adds as 16 packed
+// f32x2 ones (channel pairs).
 // ---------------------------------------------------------------------------
 constexpr int kPooledKe = 3;
 constexpr int kPooledBoxFloats = kPooledBoxCols * kPooledBoxRows * kPooledKe;  // per channel
@@ -861,6 +833,8 @@ __device__ __forceinline__ void pooled_issue(const PooledParams& p, uint32_t dst
 
 __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant__ PooledParams p) {
   extern __shared__ __align__(128) uint8_t pooled_raw[];
+  __shared__ int s_item[2];  // the item of each box buffer (>= items: none)
+  __shared__ float s_sc[kPooledMaxCout], s_bb[kPooledMaxCout];
   uint8_t* base = pooled_raw + ((128u - (smem_u32(pooled_raw) & 127u)) & 127u);
   const uint32_t box_bytes = (uint32_t)(p.Cin * kPooledBoxFloats * 4);
   const uint32_t box_stride = (box_bytes + 127u) / 128u * 128u;
@@ -876,13 +850,18 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
     fence_barrier_init();
     for (int t = 0; t < 2; ++t) {
       const int it = (int)blockIdx.x + t * (int)gridDim.x;
+      s_item[t] = it;
       if (it < items) pooled_issue(p, smem_u32(base) + t * box_stride, bar0 + 8u * t, it, box_bytes);
     }
-    grid_dependency_wait();  // the folded weights and bias of the finalize
+    grid_dependency_wait();  // the summed weights, scales and bias of the finalize
     mbar_arrive_expect_tx(bar0 + 16, wbytes);
     bulk_g2s(smem_u32(ws), p.w2, wbytes, bar0 + 16);
   }
   grid_dependency_wait();
+  for (int c = threadIdx.x; c < p.Cout; c += blockDim.x) {
+    s_sc[c] = p.s2 ? p.s2[c] : 1.f;
+    s_bb[c] = p.b2 ? p.b2[c] : 0.f;
+  }
   __syncthreads();
   // every thread takes the same branch on a wait's outcome (the loop holds a
   // CTA barrier)
@@ -893,12 +872,14 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
   const int co0 = 16 * warp + 8 * g;
   const long long pv = (long long)p.P[0] * p.P[1] * p.P[2];
   const int per = p.nq1b * p.nq2b;
-  int t = 0;
-  for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++t) {
+  uint32_t ph = 0;  // bit k: phase of box buffer k
+  for (int t = 0; ok; ++t) {
     const int buf = t & 1;
-    ok = __syncthreads_and(mbar_wait(bar0 + 8u * buf, (uint32_t)((t >> 1) & 1), p.timeout_cycles,
-                                     nullptr));
+    const int item = s_item[buf];
+    if (item >= items) break;
+    ok = __syncthreads_and(mbar_wait(bar0 + 8u * buf, (ph >> buf) & 1u, p.timeout_cycles, nullptr));
     if (!ok) break;
+    ph ^= 1u << buf;
     const int s = item / per, r = item - s * per;
     const int n = s / p.P[0], q0 = s - n * p.P[0];
     const int q1b = r / p.nq2b, q2b = r - q1b * p.nq2b;
@@ -906,11 +887,12 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
     const int xc = 2 * q2a - p.pad[2];
     const int shift = xc - (xc & ~3);
     const float* xs = xsb + buf * (box_stride / 4);
-    float acc[kPooledRows][8];
+    // channel pairs (2 h, 2 h + 1) in one packed f32x2 accumulator
+    float2 acc[kPooledRows][4];
 #pragma unroll
     for (int i = 0; i < kPooledRows; ++i)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
+      for (int h = 0; h < 4; ++h) acc[i][h] = make_float2(0.f, 0.f);
     for (int ci = 0; ci < p.Cin; ++ci) {
 #pragma unroll
       for (int e0 = 0; e0 < kPooledKe; ++e0)
@@ -927,20 +909,22 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
                 ws + (((ci * kPooledKe + e0) * kPooledKe + e1) * kPooledKe + e2) * p.coutp + co0;
             const float4 wa = *reinterpret_cast<const float4*>(wr);
             const float4 wb = *reinterpret_cast<const float4*>(wr + 4);
-            const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            const float2 w4[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
+                                  make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
 #pragma unroll
             for (int i = 0; i < kPooledRows; ++i) {
-              const float xv = v[2 * i + e1];
+              const float2 xv = make_float2(v[2 * i + e1], v[2 * i + e1]);
 #pragma unroll
-              for (int c = 0; c < 8; ++c) acc[i][c] = fmaf(xv, w8[c], acc[i][c]);
+              for (int h = 0; h < 4; ++h) acc[i][h] = __ffma2_rn(xv, w4[h], acc[i][h]);
             }
           }
         }
     }
-    // this item's box is read: the one two items on may land in it
+    // this item's box is read: the CTA's next item may land in it
     __syncthreads();
     if (threadIdx.x == 0) {
-      const int nx = item + 2 * (int)gridDim.x;
+      const int nx = p.ctr ? 2 * (int)gridDim.x + (int)atomicAdd(p.ctr, 1u) : item + 2 * (int)gridDim.x;
+      s_item[buf] = nx;
       if (nx < items) pooled_issue(p, smem_u32(base) + buf * box_stride, bar0 + 8u * buf, nx, box_bytes);
     }
     const int q2 = q2a + q2l;
@@ -949,21 +933,22 @@ __global__ void __launch_bounds__(128) pooled_conv_kernel(const __grid_constant_
       for (int c = 0; c < 8; ++c) {
         const int co = co0 + c;
         if (co >= p.Cout) break;
-        const float bb = p.b2 ? __ldg(p.b2 + co) : 0.f;
-        const float sc = p.s2 ? __ldg(p.s2 + co) : 1.f;
+        const float bb = s_bb[co], sc = s_sc[co];
         float* yo = p.y + ((long long)n * p.Cout + co) * pv + (long long)q0 * p.P[1] * p.P[2] + q2;
 #pragma unroll
         for (int i = 0; i < kPooledRows; ++i)
-          if (q1a + i < p.P[1]) yo[(long long)(q1a + i) * p.P[2]] = fmaf(acc[i][c], sc, bb);
+          if (q1a + i < p.P[1])
+            yo[(long long)(q1a + i) * p.P[2]] = fmaf(c & 1 ? acc[i][c >> 1].y : acc[i][c >> 1].x, sc, bb);
       }
     }
   }
-  if (!ok) {
-    // a wait ran out: flag it; the boxes still in flight land before the CTA leaves
-    if (threadIdx.x == 0) {
-      atomicExch(p.err, 1);
-      for (int k = 0; k < 2; ++k) mbar_wait(bar0 + 8u * k, (uint32_t)((t >> 1) & 1), p.timeout_cycles, nullptr);
-    }
+  if (!ok && threadIdx.x == 0) {
+    // a wait ran out: flag it; the boxes still in flight land before the CTA
+    // leaves (buffer k holds one iff its item is valid: a box is issued for
+    // every valid item and not yet waited for)
+    atomicExch(p.err, 1);
+    for (int k = 0; k < 2; ++k)
+      if (s_item[k] < items) mbar_wait(bar0 + 8u * k, (ph >> k) & 1u, p.timeout_cycles, nullptr);
   }
 }
 
@@ -973,22 +958,29 @@ bool pooled_ok(int Cin, int Cout, const int Ke[3], const int P[3], int N) {
     if (Ke[a] < 1 || Ke[a] > kPooledKe || P[a] < 1) return false;
   const long long nq1b = (P[1] + kPooledRows - 1) / kPooledRows;
   const long long nq2b = (P[2] + kPooledQ2 - 1) / kPooledQ2;
-  return nq1b * nq2b * N * P[0] <= INT32_MAX &&
+  // (item numbers, the counter's included, stay far below 2^31)
+  return nq1b * nq2b * N * P[0] <= INT32_MAX / 2 &&
          pooled_smem_bytes(Cin, pooled_coutp(Cout)) <= 100 * 1024;
 }
 
 cudaError_t pooled_launch(const PooledParams& p, int sm_count, cudaStream_t st) {
   const long long items = (long long)p.nq1b * p.nq2b * p.N * p.P[0];
   const size_t smem = pooled_smem_bytes(p.Cin, p.coutp);
-  // persistent CTAs: as many as fit on the SMs at once (shared memory bound)
-  const long long per_sm = std::max<long long>(1, std::min<long long>(16, (227 * 1024) / (long long)(smem + 1024)));
-  const unsigned grid = (unsigned)std::min<long long>(items, per_sm * sm_count);
+  const int threads = 32 * (p.coutp / 16);
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(pooled_conv_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_dependent(pooled_conv_kernel, dim3(grid), dim3(32 * (p.coutp / 16)), smem, st, p);
+  // persistent CTAs: as many as fit on the SMs at once
+  int per_sm = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pooled_conv_kernel,
+                                                                      threads, smem);
+  if (e != cudaSuccess) return e;
+  const long long want = items;
+  const unsigned grid = (unsigned)std::max<long long>(
+      1, std::min<long long>(want, (long long)std::max(per_sm, 1) * sm_count));
+  return launch_dependent(pooled_conv_kernel, dim3(grid), dim3(threads), smem, st, p);
 }
 
 constexpr size_t kGramSmem = 2 * kGramSlabFloats * sizeof(float);
@@ -1019,19 +1011,15 @@ cudaError_t gram_reduce_launch(const float* part, const int* box_cta0_host, int 
   return cudaGetLastError();
 }
 
-cudaError_t pool_finalize_launch(const PoolFinParams& p, bool dependent, cudaStream_t st) {
-  size_t smem = (((size_t)p.Cin * p.k[0] * p.k[1] * p.k[2] + 3) & ~(size_t)3) * 4;
-  if (p.lrs) smem += (size_t)p.lag_nrange[0] * p.lag_nrange[1] * p.lag_nrange[2] * kLagSlots * 4;
+cudaError_t pool_finalize_launch(const PoolFinParams& p, cudaStream_t st) {
+  const size_t smem = (((size_t)p.Cin * p.k[0] * p.k[1] * p.k[2] + 3) & ~(size_t)3) * 4;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(pool_finalize_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  if (!dependent) {
-    pool_finalize_kernel<<<p.Cout, 256, smem, st>>>(p);
-    return cudaGetLastError();
-  }
-  return launch_dependent(pool_finalize_kernel, dim3(p.Cout), dim3(256), smem, st, p);
+  pool_finalize_kernel<<<p.Cout, 256, smem, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace tc3d

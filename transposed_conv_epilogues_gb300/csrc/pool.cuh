@@ -80,12 +80,13 @@ cudaError_t lag_set_smem();
 cudaError_t lag_launch(const LagParams& p, int cin, cudaStream_t st);
 
 // Pooled convolution on CUDA cores (pool.cu): stride 2, at most 3 taps per
-// axis, Cin <= 4, Cout <= 64; y = conv(x, w2) + b2 over P0 x P1 x P2 outputs,
-// input position 2 q + e - pad.  A CTA takes (n, q0, 4 rows of q1, 16 of q2)
-// with one warp per 16 channels; its input box and the weights come in by TMA.
+// axis, Cin <= 4, Cout <= 64; y = s2 conv(x, w2) + b2 over P0 x P1 x P2
+// outputs, input position 2 q + e - pad.  A CTA takes items (n, q0, 4 rows of
+// q1, 16 of q2) with one warp per 16 channels; the input boxes and the weights
+// come in by TMA.
 constexpr int kPooledMaxCin = 4;
 constexpr int kPooledMaxCout = 64;
-constexpr int kPooledRows = 4;     // q1 outputs per CTA (per thread)
+constexpr int kPooledRows = 4;     // q1 outputs per item (per lane)
 constexpr int kPooledQ2 = 16;      // q2 outputs per CTA (one per lane pair)
 constexpr int kPooledBoxCols = 36; // columns of the input box (33 used + alignment shift)
 constexpr int kPooledBoxRows = 2 * kPooledRows + 1;
@@ -94,6 +95,8 @@ struct PooledParams {
   const float* w2;   // [ci][e0][e1][e2][coutp], 3 taps per axis (zero past Ke)
   const float* b2;   // [Cout] or nullptr
   const float* s2;   // [Cout] scale of the sums (y = s2 * acc + b2), or nullptr (1)
+  unsigned* ctr;     // item counter, zero at launch (CTAs take items from it), or nullptr
+                     // (CTA b takes items b, b + grid, ...)
   float* y;          // [N][Cout][P0][P1][P2]
   int* err;
   unsigned long long timeout_cycles;
@@ -117,8 +120,6 @@ struct PoolFinParams {
   const double* gcls;   // batch statistics: per class combined Gram [ncls][kGramEntries];
                         // nullptr in evaluation mode and in lag form
   const float* lrs;     // batch statistics in lag form: box sums [nbox][kLagSlots]
-  int lag_nseg[3];
-  int lag_nrange[3], lag_range[3][4][2], lag_ridx[3][2][kMaxAxisTaps];
   unsigned wkmask[3][kMaxAxisTaps];  // per axis and summed tap e: bit k set iff W[k] adds in
   // per class c and entry i of its patch (rows off[c] .. off[c + 1] - 1 of
   // all classes): the patch index d, the index of its weight in a channel's
@@ -132,6 +133,7 @@ struct PoolFinParams {
   float* b2;            // [Cout]
   float* s2;            // lag form with the pooled layout: [Cout] scale / 64, which the
                         // pooled conv applies (w2 then holds unscaled sums); else nullptr
+  unsigned* pool_ctr;   // the pooled conv's item counter, zeroed here (or nullptr)
   float eps;
   double count;         // outputs per channel, N * O0 * O1 * O2
   double inv_count;     // 1 / count
@@ -158,8 +160,8 @@ cudaError_t gram_reduce_launch(const float* part, const int* box_cta0_host, int 
 // s2 (or, without s2, the weights w2 with the scale folded in)
 cudaError_t lag_finalize_launch(const PoolFinParams& p, const float* part, int ctas, int nent,
                                 cudaStream_t st);
-// dependent: launched after the lag reduction with programmatic dependent
-// launch (the first kernel of a call is launched normally)
-cudaError_t pool_finalize_launch(const PoolFinParams& p, bool dependent, cudaStream_t st);
+// evaluation mode, or batch statistics from the Gram path's class Grams (a
+// normal launch: the first kernel of a call, or after the Gram reduction)
+cudaError_t pool_finalize_launch(const PoolFinParams& p, cudaStream_t st);
 
 }  // namespace tc3d
