@@ -331,8 +331,11 @@ def test_plans_of_workloads(lib):
     c3 = plan("convT_s2p1d2")  # only the all-odd class has taps: 1 of 8, 27 taps
     assert c3["nR"] == 1 and c3["nEmpty"] == 7 and c3["M"] == [16, 32, 32]
     assert all(ax["classes"] == [1] and sorted(ax["kidx"][0]) == [0, 1, 2] for ax in c3["axes"])
+    # the engine writes the rows of the odd (z, y) pair; the bias fill the others
+    assert c3["fill_slab"] == 1 and c3["fill_rows"] == 1
     c4 = plan("convT_bn_avgpool")
     assert c4["fused"] == 1 and c4["nR"] == 8 and c4["M"] == [32, 32, 32]
+    assert c4["fill_rows"] == 0
     c5 = plan("conv_maxpool_lse_relu")
     assert c5["Q"] == [2, 2, 8] and c5["n_tile"] == 64
     for n in BY_NAME:
@@ -342,3 +345,20 @@ def test_plans_of_workloads(lib):
     # dense channels-last conv through the engine
     assert plan("dwconv_k3")["direct"] == 1 and plan("dwconv_k3_ndhwc")["direct"] == 1
     assert plan("conv_k3_ndhwc")["direct"] == 0 and plan("conv_k3_ndhwc")["ndhwc"] == 1
+
+
+@pytest.mark.parametrize("s, d, want", [
+    ((2, 2, 2), (2, 2, 2), 1),   # one class with taps, stride 2 along x, 4 row pairs
+    ((1, 2, 2), (1, 2, 2), 1),   # 2 row pairs (y only)
+    ((2, 1, 2), (2, 1, 2), 1),   # 2 row pairs (z only)
+    ((1, 1, 2), (1, 1, 2), 0),   # one row pair: the engine writes every row
+    ((2, 2, 1), (2, 2, 1), 0),   # stride 1 along x: the general one-class store
+    ((2, 2, 2), (1, 1, 1), 0),   # every class has taps
+])
+def test_fill_rows_plan(lib, s, d, want):
+    """Row mode of the bias fill: exactly when the engine stores through the
+    one-class stride-2-along-x path with more than one (z, y) class pair."""
+    pl = tc.plan_describe(1, (1, 3, 4, 5, 6), (3, 4, 3, 3, 3), s, 1, d)
+    assert pl["status"] == 0 and pl["fill_rows"] == want
+    if want:
+        assert pl["fill_slab"] == 1 and pl["nR"] == 1

@@ -194,16 +194,15 @@ void fill_params(const Plan& pl, EngineParams* ep) {
     ep->box[a] = pl.box[a];
   }
   {
-    // class tables of the one-class store path: at most 8 classes, whose
-    // offsets from a row's first output fit in an int
+    // class tables of the one-class store path (the plan checked that the
+    // offsets from a row's first output fit in an int)
     const int F = pl.s_out[0] * pl.s_out[1] * pl.s_out[2];
     const long long o12 = (long long)pl.O[1] * pl.O[2];
-    ep->cls_fast = pl.nR == 1 && F <= 8;
+    ep->cls_fast = pl.cls_fast;
     for (int f = 0; f < 8 && f < F; ++f) {
       const int r2 = f % pl.s_out[2], r1 = (f / pl.s_out[2]) % pl.s_out[1],
                 r0 = f / (pl.s_out[2] * pl.s_out[1]);
       const long long off = r0 * o12 + (long long)r1 * pl.O[2] + r2;
-      if (off > INT32_MAX) ep->cls_fast = 0;
       ep->cls_off[f] = (int)std::min<long long>(off, INT32_MAX);
       ep->cls_r[f] = r0 | (r1 << 8) | (r2 << 16);
       if (pl.nR == 1 && r0 == pl.r_axis[0][0] && r1 == pl.r_axis[1][0] && r2 == pl.r_axis[2][0])
@@ -354,13 +353,21 @@ int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cuda
 
 int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cudaStream_t st) {
   if (!pl.fill_slab) return TC3D_OK;
-  const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
-  int zlo[3];
-  for (int a = 0; a < 3; ++a) zlo[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
-  return fill_slab_launch(y, bias, pl.pb.N, pl.pb.Cout, O, zlo, (unsigned)d->sm_count, st) ==
-                 cudaSuccess
-             ? TC3D_OK
-             : TC3D_ERR_CUDA;
+  FillParams fp;
+  fp.y = y;
+  fp.bias = bias;
+  fp.NC = (int)(pl.pb.N * pl.pb.Cout);
+  fp.Cout = (int)pl.pb.Cout;
+  for (int a = 0; a < 3; ++a) {
+    fp.O[a] = (int)pl.O[a];
+    fp.zl[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
+  }
+  // the engine's rows: the (r0, r1) pair of its one class with taps
+  fp.s0 = pl.fill_rows ? pl.s_out[0] : 0;
+  fp.s1 = pl.fill_rows ? pl.s_out[1] : 0;
+  fp.r0 = pl.fill_rows ? pl.r_axis[0][0] : 0;
+  fp.r1 = pl.fill_rows ? pl.r_axis[1][0] : 0;
+  return fill_slab_launch(fp, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
 }
 
 int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, const float* bias,
@@ -916,6 +923,7 @@ std::string describe(const Plan& pl) {
     append(s, ", \"nR\": %lld", pl.nR);
     append(s, ", \"nEmpty\": %lld", pl.nEmpty);
     append(s, ", \"fill_slab\": %lld", pl.fill_slab);
+    append(s, ", \"fill_rows\": %lld", pl.fill_rows);
     append(s, ", \"xslack\": %lld", pl.xslack);
     append(s, ", \"ocb\": %lld", pl.ocb);
     append(s, ", \"n_tile\": %lld", pl.n_tile);

@@ -945,16 +945,18 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               }
             }
           } else if (p.cls_fast && p.s_out[2] == 2) {
-            // one class with taps, stride 2 along x: dense stores.  The Q2
-            // lanes of a row group hold consecutive m2 with equal (m0, m1),
-            // so for a class pair (r0, r1) the group's outputs at x = 2 m2
-            // + r2 form one run of 2 Q2 floats.  The warp's 64 values of a
-            // pair are written by 2 stores of 32 consecutive floats per
-            // run: writer lane l of store k takes flattened position
-            // i = 32 k + l, i.e. run g = i / (2 Q2) at x offset i % (2 Q2),
-            // whose value sits in source lane g Q2 + (i % (2 Q2)) / 2.
-            const int npair = F >> 1;  // class pairs (r0, r1)
+            // one class with taps, stride 2 along x: dense stores of the
+            // rows of its class pair (r0, r1) only (both x classes: the
+            // value and the bias); the rows of the other pairs are the bias
+            // fill's.  The Q2 lanes of a row group hold consecutive m2 with
+            // equal (m0, m1), so the group's outputs at x = 2 m2 + r2 form
+            // one run of 2 Q2 floats.  The warp's 64 values are written by 2
+            // stores of 32 consecutive floats per run: writer lane l of
+            // store k takes flattened position i = 32 k + l, i.e. run g =
+            // i / (2 Q2) at x offset i % (2 Q2), whose value sits in source
+            // lane g Q2 + (i % (2 Q2)) / 2.
             const int star01 = p.cls_star >> 1, star2 = p.cls_star & 1;
+            const int rstar = p.cls_r[2 * star01], offstar = p.cls_off[2 * star01];
             int src[2], xodd[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -967,7 +969,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             for (int a = 0; a < p.n_acc; ++a) {
               const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
               float* pk[2];
-              uint32_t mk[2];  // bit c: class pair c of this writer is inside
+              bool mk[2];  // this writer's output of the pair lies inside
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 int t[3];
@@ -976,15 +978,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 const bool rv = m0 < p.M[0] && m1 < p.M[1] && m2 < p.M[2];
                 const int zb0 = p.s_out[0] * m0, zb1 = p.s_out[1] * m1, xb = 2 * m2 + xodd[k];
                 pk[k] = p.y + ((long long)tc.n * p.Cout + oc0) * ovol + (long long)zb0 * o12 +
-                        (long long)zb1 * p.O[2] + xb;
-                mk[k] = 0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const int r = p.cls_r[2 * c];
-                  if (c < npair && rv && xb < p.O[2] && zb0 + (r & 255) < p.O[0] &&
-                      zb1 + ((r >> 8) & 255) < p.O[1])
-                    mk[k] |= 1u << c;
-                }
+                        (long long)zb1 * p.O[2] + xb + offstar;
+                mk[k] = rv && xb < p.O[2] && zb0 + (rstar & 255) < p.O[0] &&
+                        zb1 + ((rstar >> 8) & 255) < p.O[1];
               }
               for (int cc = 0; cc < p.n_tile; cc += 32) {
                 uint32_t v[32];
@@ -1001,14 +997,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                   const float val = __uint_as_float(v[jj]) + b;
                   const float v0 = __shfl_sync(0xffffffffu, val, src[0]);
                   const float v1 = __shfl_sync(0xffffffffu, val, src[1]);
-                  const float s0 = xodd[0] == star2 ? v0 : b;
-                  const float s1 = xodd[1] == star2 ? v1 : b;
-#pragma unroll
-                  for (int c = 0; c < 4; ++c) {
-                    const int off = p.cls_off[2 * c];
-                    if ((mk[0] >> c) & 1u) y0[off] = c == star01 ? s0 : b;
-                    if ((mk[1] >> c) & 1u) y1[off] = c == star01 ? s1 : b;
-                  }
+                  if (mk[0]) *y0 = xodd[0] == star2 ? v0 : b;
+                  if (mk[1]) *y1 = xodd[1] == star2 ? v1 : b;
                   y0 += ovol;
                   y1 += ovol;
                 }
@@ -1455,47 +1445,93 @@ __global__ void bn_pool4_kernel(const float* t, float* y, int N, int Cout, int O
   }
 }
 
-// three disjoint boxes: z0 >= zlo0 | z0 < zlo0, z1 >= zlo1 | z0 < zlo0, z1 < zlo1, z2 >= zlo2
-// Bias fill of the outputs past the last row with taps on some axis (rows m
-// >= M of the transposed-conv row grid hold only tap-less classes).  Per
-// (n, c) slice, with zl = s_out * M clipped to O:
-//   rows (z, y) with z >= zl0, or y >= zl1: the whole x range;
-//   the other rows: x in [zl2, O2).
-// Block row blockIdx.y takes slices; whole rows go one per warp with the
-// lanes along x, the short x tails one element per thread.  Blocks are small
-// (128 threads, at most 32 registers each) so that one fits on an SM beside
-// an engine CTA: the fill runs concurrently with the engine.
-__global__ void __launch_bounds__(128, 16) fill_slab_kernel(float* y, const float* bias, int NC,
-                                                        int Cout, int O0, int O1, int O2, int zl0,
-                                                        int zl1, int zl2) {
-  const int n_zrows = (O0 - zl0) * O1;           // rows of the z >= zl0 planes
-  const int n_full = n_zrows + zl0 * (O1 - zl1);  // rows filled over the whole x range
-  const int wtail = O2 - zl2;
-  const int n_tail = wtail > 0 ? zl0 * zl1 * wtail : 0;
-  const long long ovol = (long long)O0 * O1 * O2;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int nc = blockIdx.y; nc < NC; nc += gridDim.y) {
-    float* ys = y + (long long)nc * ovol;
-    const float b = bias ? __ldg(bias + nc % Cout) : 0.f;
-    for (int r = blockIdx.x * 4 + warp; r < n_full; r += gridDim.x * 4) {
-      int z, yy;
-      if (r < n_zrows) {
-        z = zl0 + r / O1;
-        yy = r - (z - zl0) * O1;
-      } else {
-        const int r2 = r - n_zrows, w1 = O1 - zl1;
-        z = r2 / w1;
-        yy = zl1 + (r2 - z * w1);
-      }
-      float* row = ys + ((long long)z * O1 + yy) * O2;
-      for (int x = lane; x < O2; x += 32) row[x] = b;
-    }
-    for (int i = blockIdx.x * 128 + threadIdx.x; i < n_tail; i += gridDim.x * 128) {
-      const int r = i / wtail, x = zl2 + (i - r * wtail);
-      const int z = r / zl1, yy = r - z * zl1;
-      ys[((long long)z * O1 + yy) * O2 + x] = b;
+// Bias fill of the outputs the engine does not write.  Per (n, c) slice,
+// with zl = s_out * M clipped to O (rows m >= M of the transposed-conv row
+// grid hold only tap-less classes):
+//   planes z >= zl0, rows y >= zl1: the whole x range;
+//   in row mode (s0 > 0: the engine writes only the rows of the class pair
+//   (r0, r1) of its one class with taps): planes with z % s0 != r0 and rows
+//   with y % s1 != r1, the whole x range;
+//   the engine's rows: x in [zl2, O2).
+// Work unit: one plane of one slice, one warp.  Spans go out
+// as bulk copies (TMA engine) from a per-warp shared buffer holding the
+// bias, with scalar stores for the ends off the 16-byte grid; scattered rows
+// take one lane each.  Blocks are small (4 warps of 32 registers, 8 KB of
+// shared memory) so that one fits on an SM beside an engine CTA: the fill
+// runs concurrently with the engine, and costs it few issue slots.
+constexpr int kFillWarps = 4;
+constexpr int kFillBuf = 512;  // floats of a warp's bias buffer
+
+// [p, p + n) from buffer src (a bulk copy per kFillBuf floats, issued by
+// lanes in turn; scalar ends)
+__device__ __forceinline__ void fill_span(float* p, long long n, float b, uint32_t src, int lane) {
+  const int to16 = (int)((4 - ((reinterpret_cast<uintptr_t>(p) >> 2) & 3)) & 3);
+  const int head = n < to16 ? (int)n : to16;
+  if (lane < head) p[lane] = b;
+  p += head;
+  n -= head;
+  const long long mid = n & ~3LL;
+  if (lane < (int)(n - mid)) p[mid + lane] = b;
+  const long long chunks = (mid + kFillBuf - 1) / kFillBuf;
+  for (long long c = lane; c < chunks; c += 32) {
+    const long long o = c * kFillBuf;
+    const long long len = mid - o < kFillBuf ? mid - o : kFillBuf;
+    bulk_s2g(p + o, src, (uint32_t)(len * 4));
+  }
+}
+
+// rows y_j = s j + r (j < nrows) of a plane, x in [x0, O2): lane per row
+__device__ __forceinline__ void fill_rows_run(float* plane, int nrows, int s, int r, int x0, int O2,
+                                              float b, uint32_t src, int lane) {
+  for (int j = lane; j < nrows; j += 32) {
+    float* row = plane + (long long)(s * j + r) * O2 + x0;
+    const int n = O2 - x0;
+    const int to16 = (int)((4 - ((reinterpret_cast<uintptr_t>(row) >> 2) & 3)) & 3);
+    const int head = n < to16 ? n : to16;
+    for (int i = 0; i < head; ++i) row[i] = b;
+    const int rest = n - head, mid = rest & ~3;
+    for (int i = head + mid; i < n; ++i) row[i] = b;
+    for (int o = 0; o < mid; o += kFillBuf) {
+      const int len = mid - o < kFillBuf ? mid - o : kFillBuf;
+      bulk_s2g(row + head + o, src, (uint32_t)(len * 4));
     }
   }
+}
+
+__global__ void __launch_bounds__(32 * kFillWarps, 16) fill_slab_kernel(const __grid_constant__ FillParams p) {
+  __shared__ __align__(128) float buf[kFillWarps][kFillBuf];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u = (long long)blockIdx.x * kFillWarps + warp;
+  if (u >= (long long)p.NC * p.O[0]) return;
+  const int nc = (int)(u / p.O[0]), z = (int)(u - (long long)nc * p.O[0]);
+  const float b = p.bias ? __ldg(p.bias + nc % p.Cout) : 0.f;
+  for (int i = lane; i < kFillBuf; i += 32) buf[warp][i] = b;
+  fence_proxy_async_smem();
+  __syncwarp();
+  const uint32_t src = smem_u32(&buf[warp][0]);
+  const int O1 = p.O[1], O2 = p.O[2];
+  float* plane = p.y + ((long long)nc * p.O[0] + z) * ((long long)O1 * O2);
+  if (z >= p.zl[0] || (p.s0 > 0 && z % p.s0 != p.r0)) {
+    fill_span(plane, (long long)O1 * O2, b, src, lane);
+  } else {
+    const int zl1 = p.zl[1];
+    // the rows y < zl1 of the fill (y % s1 != r1): for each of the s1 - 1
+    // residues a run of rows with stride s1
+    if (p.s0 > 0)
+      for (int rr = 0; rr < p.s1; ++rr)
+        if (rr != p.r1 && rr < zl1)
+          fill_rows_run(plane, (zl1 - rr + p.s1 - 1) / p.s1, p.s1, rr, 0, O2, b, src, lane);
+    // the engine's rows past x = zl2
+    if (p.zl[2] < O2) {
+      const int s = p.s0 > 0 ? p.s1 : 1, r = p.s0 > 0 ? p.r1 : 0;
+      if (r < zl1) fill_rows_run(plane, (zl1 - r + s - 1) / s, s, r, p.zl[2], O2, b, src, lane);
+    }
+    if (zl1 < O1) fill_span(plane + (long long)zl1 * O2, (long long)(O1 - zl1) * O2, b, src, lane);
+  }
+  // the copies have read the buffer before the warp leaves (their writes
+  // complete with the grid)
+  bulk_commit();
+  bulk_wait_read();
 }
 
 __global__ void wait_timeout_kernel(int* err, unsigned long long timeout_cycles) {
@@ -1588,14 +1624,17 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
   return cudaGetLastError();
 }
 
-cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
-                             const int zlo[3], unsigned blocks, cudaStream_t st) {
-  // blocks: the CTA count to use (one per SM), spread over slices first
-  const int NC = N * Cout;
-  const unsigned rows = std::max(1u, std::min(blocks, (unsigned)std::min(NC, 65535)));
-  const unsigned per_slice = std::max(1u, blocks / rows);
-  fill_slab_kernel<<<dim3(per_slice, rows), 128, 0, st>>>(y, bias, NC, Cout, O[0], O[1], O[2],
-                                                           zlo[0], zlo[1], zlo[2]);
+cudaError_t fill_slab_launch(const FillParams& p, cudaStream_t st) {
+  // a warp per (slice, plane)
+  const long long units = (long long)p.NC * p.O[0];
+  const long long grid = (units + kFillWarps - 1) / kFillWarps;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // the largest shared-memory carveout, the engine's: an SM holds CTAs of
+  // one carveout at a time, so only then can a fill CTA join an engine CTA
+  const cudaError_t e = cudaFuncSetAttribute(fill_slab_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  fill_slab_kernel<<<(unsigned)grid, 32 * kFillWarps, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -161,10 +161,17 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
                               const int O[3], const int P[3], const float* gamma,
                               const float* beta, float eps, float2* stat, unsigned blocks,
                               cudaStream_t st);
-// bias (or 0) into the outputs at z_a >= zlo[a] for any axis a (outputs of
-// rows past the GEMM row grid; all of them in classes without taps)
-cudaError_t fill_slab_launch(float* y, const float* bias, int N, int Cout, const int O[3],
-                             const int zlo[3], unsigned blocks, cudaStream_t st);
+// bias (or 0) into the outputs at z_a >= zl[a] for any axis a (outputs of
+// rows past the GEMM row grid; all of them in classes without taps) and,
+// with s0 > 0, into every output row (z, y) with z % s0 != r0 or y % s1 !=
+// r1 (rows of tap-less class pairs)
+struct FillParams {
+  float* y;           // [N * Cout][O0][O1][O2]
+  const float* bias;  // [Cout] or nullptr (0)
+  int NC, Cout, O[3], zl[3];
+  int s0, s1, r0, r1;  // s0 == 0: no row mode
+};
+cudaError_t fill_slab_launch(const FillParams& p, cudaStream_t st);
 cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_cycles, cudaStream_t st);
 
 // device address of the library's error word on the current device

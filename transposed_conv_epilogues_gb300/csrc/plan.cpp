@@ -224,6 +224,17 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     }
   }
   pl.nR = pl.nRaxis[0] * pl.nRaxis[1] * pl.nRaxis[2];
+  {
+    // the one-class store path: at most 8 classes, whose offsets from a
+    // row's first output fit in an int; along x with stride 2 it writes only
+    // the rows of its class pair, and the bias fill the others
+    const int F = pl.s_out[0] * pl.s_out[1] * pl.s_out[2];
+    const int64_t maxoff = (int64_t)(pl.s_out[0] - 1) * pl.O[1] * pl.O[2] +
+                           (int64_t)(pl.s_out[1] - 1) * pl.O[2] + (pl.s_out[2] - 1);
+    pl.cls_fast = pl.nR == 1 && F <= 8 && maxoff <= INT32_MAX;
+    pl.fill_rows = pl.cls_fast && pl.s_out[2] == 2 && pl.s_out[0] * pl.s_out[1] > 1;
+    if (pl.fill_rows) pl.fill_slab = 1;
+  }
   if (is_bn_op(pb.op)) {
     // fused BatchNorm + 4x4x4 pooling: a row is a 2x2x2 output block with all
     // 8 parity classes carrying taps, so a 4^3 window is 2x2x2 rows

@@ -80,6 +80,12 @@ struct Plan {
   // outputs at z_a >= s_out*M (all of them in tap-less classes) are written
   // by a separate bias fill; fill_slab says whether any exist
   int fill_slab;
+  // one class with taps whose store takes the dense stride-2-along-x path
+  // (cls_fast with s_out[2] == 2): the engine writes only the output rows of
+  // that class's (r0, r1) pair, the bias fill all others (fill_rows; then
+  // fill_slab is set too)
+  int cls_fast;
+  int fill_rows;
 
   // GEMM N: per column block ocb output channels x nR classes, oc-major
   int ocb, n_tile, nb_per_group, n_colblocks;

@@ -774,6 +774,13 @@ cudaError_t lag_finalize_launch(const PoolFinParams& p, const float* part, int c
   const size_t smem_r = (size_t)lag_reduce_smem_ints(nent) * 4;
   const size_t smem_c =
       (size_t)lag_channel_smem_floats(p.Cin, p.k[0] * p.k[1] * p.k[2], nrows, ntri) * 4;
+  // both kernels share SMs with the lag kernel, whose shared-memory carveout
+  // is the largest: an SM holds CTAs of one carveout at a time
+  for (const void* f : {(const void*)lag_reduce_kernel, (const void*)lag_channel_kernel}) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   if (smem_r > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(lag_reduce_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
