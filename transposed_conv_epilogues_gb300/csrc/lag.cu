@@ -33,6 +33,9 @@ namespace tc3d {
 namespace {
 
 constexpr int kLagThreads = kLagRows * 32;
+// registers a thread: the finalize kernels launched while this one runs
+// need 4096 of the SM's 65536 beside its 256 threads
+constexpr int kLagMaxRegs = 232;
 constexpr int kLagRing = 3;                   // chunk slots per warp
 constexpr int kLagPlane = kLagBoxRows * kLagBoxCols;  // floats of one channel's window plane
 // a chunk slot holds one box: [Cin][kLagChunk planes][3 rows][40 columns];
@@ -351,7 +354,7 @@ __device__ __forceinline__ int seg_of(const LagParams& p, int a, int z) {
 }
 
 template <int CIN>
-__global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_constant__ LagParams p) {
+__global__ void __maxnreg__(kLagMaxRegs) lag_stats_kernel(const __grid_constant__ LagParams p) {
   constexpr int NS = lag_nslots(CIN);
   // float index of the 128-byte aligned base
   const int a0 = (int)(((128u - (smem_u32(lag_dsm) & 127u)) & 127u) >> 2);
@@ -481,27 +484,45 @@ __global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_
     for (int s = 0; s < NS; ++s) red[threadIdx.x * kLagRedStride + s] = acc[s];
   }
   for (int e = threadIdx.x; e < kLagOutFloats; e += kLagThreads) outa[e] = 0.f;
+  // runs of lanes (columns) of one segment: run i is lanes [lrun[i], lrun[i +
+  // 1]) of segment lseg[i] (a segment may recur: columns past x take the
+  // wide one)
+  __shared__ int lrun[33], lseg[32], nlrun;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int l = 0; l < 32; ++l)
+      if (l == 0 || segl[l] != segl[l - 1]) {
+        lrun[n] = l;
+        lseg[n] = segl[l];
+        ++n;
+      }
+    lrun[n] = 32;
+    nlrun = n;
+  }
   __syncthreads();
   {
-    // segments are runs of consecutive lanes: a running sum, written out at
-    // each change of segment (each (region, slot) cell has one writer)
+    // thread (h, k) adds slot k over the lanes of warps 4h .. 4h + 3, run by
+    // run, with independent partial sums (each (region, slot) cell of a half
+    // has one writer)
     const int h = threadIdx.x >> 7, k = threadIdx.x & 127;
     if (k < NS) {
       float* oh = outa + (size_t)h * kLagMaxReg2 * kLagSlots + k;
       for (int wv = 4 * h; wv < 4 * h + 4; ++wv) {
         const int base = segw[wv] * p.nseg[2];
-        int cur = segl[0];
-        float run = 0.f;
-        for (int l = 0; l < 32; ++l) {
-          const int sl = segl[l];
-          if (sl != cur) {
-            oh[(base + cur) * kLagSlots] += run;
-            run = 0.f;
-            cur = sl;
+        const float* col = red + (size_t)wv * 32 * kLagRedStride + k;
+        for (int i = 0; i < nlrun; ++i) {
+          const int l1 = lrun[i + 1];
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          int l = lrun[i];
+          for (; l + 4 <= l1; l += 4) {
+            a0 += col[l * kLagRedStride];
+            a1 += col[(l + 1) * kLagRedStride];
+            a2 += col[(l + 2) * kLagRedStride];
+            a3 += col[(l + 3) * kLagRedStride];
           }
-          run += red[(wv * 32 + l) * kLagRedStride + k];
+          for (; l < l1; ++l) a0 += col[l * kLagRedStride];
+          oh[(base + lseg[i]) * kLagSlots] += (a0 + a1) + (a2 + a3);
         }
-        oh[(base + cur) * kLagSlots] += run;
       }
     }
   }
@@ -510,51 +531,45 @@ __global__ void __launch_bounds__(kLagThreads, 1) lag_stats_kernel(const __grid_
   // its segment s0): the sum of its regions inside the box.  Per slot k:
   // R[s1][s2] = both halves; T[s1][b2] = sum of R over range b2 of axis 2;
   // box (b0, b1, b2) = [s0 in range b0] * sum of T over range b1 of axis 1.
-  {
+  // The ranges as bit masks of segments, the sums unrolled over the maxima.
+  if (threadIdx.x < 128) {
+    const int k = threadIdx.x;
     const int ns1 = p.nseg[1], ns2 = p.nseg[2];
     const int nr0 = p.nrange[0], nr1 = p.nrange[1], nr2 = p.nrange[2];
-    __shared__ int rng[3][4][2];
-    if (threadIdx.x < 24)
-      rng[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2] =
-          p.range[threadIdx.x / 8][(threadIdx.x / 2) % 4][threadIdx.x % 2];
-    __syncthreads();
-    float* dst = p.part + (size_t)blockIdx.x * p.nbox * kLagSlots;
-    const int k = threadIdx.x & 127;
-    if (threadIdx.x < 128) {
-      float T[kLagMaxSeg][4];
+    unsigned m1[4], m2[4];
+    bool in0[4];
 #pragma unroll
-      for (int s1 = 0; s1 < kLagMaxSeg; ++s1)
+    for (int b = 0; b < 4; ++b) {
+      m1[b] = b < nr1 ? (1u << p.range[1][b][1]) - (1u << p.range[1][b][0]) : 0u;
+      m2[b] = b < nr2 ? (1u << p.range[2][b][1]) - (1u << p.range[2][b][0]) : 0u;
+      in0[b] = b < nr0 && s0 >= p.range[0][b][0] && s0 < p.range[0][b][1];
+    }
+    float* dst = p.part + (size_t)blockIdx.x * p.nbox * kLagSlots + k;
 #pragma unroll
-        for (int b2 = 0; b2 < 4; ++b2) T[s1][b2] = 0.f;
-      if (k < NS) {
+    for (int b2 = 0; b2 < 4; ++b2) {
+      if (b2 >= nr2) break;
+      float T[kLagMaxSeg];
 #pragma unroll
-        for (int s1 = 0; s1 < kLagMaxSeg; ++s1) {
-          if (s1 >= ns1) break;
+      for (int s1 = 0; s1 < kLagMaxSeg; ++s1) {
+        float t = 0.f;
 #pragma unroll
-          for (int s2 = 0; s2 < kLagMaxSeg; ++s2) {
-            if (s2 >= ns2) break;
-            const int r12 = s1 * ns2 + s2;
-            const float v = outa[r12 * kLagSlots + k] + outa[(kLagMaxReg2 + r12) * kLagSlots + k];
-#pragma unroll
-            for (int b2 = 0; b2 < 4; ++b2)
-              if (b2 < nr2 && s2 >= rng[2][b2][0] && s2 < rng[2][b2][1]) T[s1][b2] += v;
-          }
+        for (int s2 = 0; s2 < kLagMaxSeg; ++s2) {
+          const int r12 = s1 * ns2 + s2;
+          if (k < NS && s1 < ns1 && s2 < ns2 && ((m2[b2] >> s2) & 1u))
+            t += outa[r12 * kLagSlots + k] + outa[(kLagMaxReg2 + r12) * kLagSlots + k];
         }
+        T[s1] = t;
       }
-      for (int b0 = 0; b0 < nr0; ++b0) {
-        const bool in0 = k < NS && s0 >= rng[0][b0][0] && s0 < rng[0][b0][1];
-        for (int b1 = 0; b1 < nr1; ++b1) {
 #pragma unroll
-          for (int b2 = 0; b2 < 4; ++b2) {
-            if (b2 >= nr2) break;
-            float v = 0.f;
-            if (in0) {
+      for (int b1 = 0; b1 < 4; ++b1) {
+        if (b1 >= nr1) break;
+        float v = 0.f;
 #pragma unroll
-              for (int s1 = 0; s1 < kLagMaxSeg; ++s1)
-                if (s1 >= rng[1][b1][0] && s1 < rng[1][b1][1]) v += T[s1][b2];
-            }
-            dst[((b0 * nr1 + b1) * nr2 + b2) * kLagSlots + k] = v;
-          }
+        for (int s1 = 0; s1 < kLagMaxSeg; ++s1) v += ((m1[b1] >> s1) & 1u) ? T[s1] : 0.f;
+#pragma unroll
+        for (int b0 = 0; b0 < 4; ++b0) {
+          if (b0 >= nr0) break;
+          dst[((b0 * nr1 + b1) * nr2 + b2) * kLagSlots] = in0[b0] ? v : 0.f;
         }
       }
     }
@@ -567,6 +582,15 @@ size_t lag_smem_bytes() { return kLagSmem; }
 
 cudaError_t lag_set_smem() {
   cudaError_t e = cudaSuccess;
+  // the largest shared-memory carveout: the finalize kernels launched while
+  // this one runs take the SMs' leftover shared memory, and an SM holds CTAs
+  // of one carveout at a time
+  for (const void* f : {(const void*)lag_stats_kernel<1>, (const void*)lag_stats_kernel<2>,
+                        (const void*)lag_stats_kernel<3>}) {
+    const cudaError_t ec = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                (int)cudaSharedmemCarveoutMaxShared);
+    if (ec != cudaSuccess) e = ec;
+  }
   const cudaError_t e1 = cudaFuncSetAttribute(lag_stats_kernel<1>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLagSmem);
   const cudaError_t e2 = cudaFuncSetAttribute(lag_stats_kernel<2>,

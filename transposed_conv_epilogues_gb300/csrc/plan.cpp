@@ -636,9 +636,12 @@ static void plan_lag(const Plan& bn, PoolPlan& pp) {
       lag_reduce_smem_ints(pp.lag_nbox * kLagSlots) * 4 > 192 * 1024)
     return;
   // work split: the jobs of axis-0 segment s (one per block of 8 rows and 32
-  // columns) cost about N (2 len(s) + 1) each (steps, plus the planes every
-  // run of consecutive planes loads first); CTAs in proportion, at least
-  // one per job, then spare CTAs to the segment whose CTAs carry most
+  // columns) cost about N (2 len(s) + 3.5) each, in units of half a step: a
+  // step per plane, and per run of consecutive planes (one per sample) the
+  // planes it loads first and the wait for its first chunk, which no earlier
+  // work hides (measured on GB300: a run costs about 1.7 steps); CTAs in
+  // proportion, at least one per job, then spare CTAs to the segment whose
+  // CTAs carry most
   pp.lag_nb1 = (int)ceil_div(pb.S[1], kLagRows);
   pp.lag_nb2 = (int)ceil_div(pb.S[2], kLagCols);
   const int64_t jobs_per_seg = (int64_t)pp.lag_nb1 * pp.lag_nb2;
@@ -646,7 +649,7 @@ static void plan_lag(const Plan& bn, PoolPlan& pp) {
   double cost[kLagMaxSeg], total = 0.0;
   for (int s = 0; s < pp.lag_nseg[0]; ++s) {
     const int len = pp.lag_seg[0][s + 1] - pp.lag_seg[0][s];
-    cost[s] = (double)pb.N * (2.0 * len + 1.0);
+    cost[s] = (double)pb.N * (2.0 * len + 3.5);
     total += cost[s] * (double)jobs_per_seg;
   }
   int64_t grid = 0;

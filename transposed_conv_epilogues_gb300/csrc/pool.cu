@@ -979,6 +979,12 @@ cudaError_t pooled_launch(const PooledParams& p, int sm_count, cudaStream_t st) 
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  // the largest carveout, as the finalize CTAs it joins on the SMs
+  {
+    const cudaError_t e = cudaFuncSetAttribute(pooled_conv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   // persistent CTAs: as many as fit on the SMs at once
   int per_sm = 0;
   const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pooled_conv_kernel,
