@@ -488,40 +488,44 @@ __global__ void __maxnreg__(kLagMaxRegs) lag_stats_kernel(const __grid_constant_
   // 1]) of segment lseg[i] (a segment may recur: columns past x take the
   // wide one)
   __shared__ int lrun[33], lseg[32], nlrun;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int l = 0; l < 32; ++l)
-      if (l == 0 || segl[l] != segl[l - 1]) {
-        lrun[n] = l;
-        lseg[n] = segl[l];
-        ++n;
-      }
-    lrun[n] = 32;
-    nlrun = n;
+  if (warp == 0) {
+    const bool start = lane == 0 || segl[lane] != segl[lane - 1];
+    const unsigned m = __ballot_sync(0xffffffffu, start);
+    if (start) {
+      const int i = __popc(m & ((1u << lane) - 1u));
+      lrun[i] = lane;
+      lseg[i] = segl[lane];
+    }
+    if (lane == 0) {
+      lrun[__popc(m)] = 32;
+      nlrun = __popc(m);
+    }
   }
   __syncthreads();
   {
     // thread (h, k) adds slot k over the lanes of warps 4h .. 4h + 3, run by
-    // run, with independent partial sums (each (region, slot) cell of a half
-    // has one writer)
+    // run, 8 loads in flight (each (region, slot) cell of a half has one
+    // writer)
     const int h = threadIdx.x >> 7, k = threadIdx.x & 127;
     if (k < NS) {
       float* oh = outa + (size_t)h * kLagMaxReg2 * kLagSlots + k;
       for (int wv = 4 * h; wv < 4 * h + 4; ++wv) {
-        const int base = segw[wv] * p.nseg[2];
+        const int base = segw[wv] * kLagMaxSeg;  // region (s1, s2) at s1 kLagMaxSeg + s2
         const float* col = red + (size_t)wv * 32 * kLagRedStride + k;
         for (int i = 0; i < nlrun; ++i) {
           const int l1 = lrun[i + 1];
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
           int l = lrun[i];
-          for (; l + 4 <= l1; l += 4) {
-            a0 += col[l * kLagRedStride];
-            a1 += col[(l + 1) * kLagRedStride];
-            a2 += col[(l + 2) * kLagRedStride];
-            a3 += col[(l + 3) * kLagRedStride];
+          float a[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) a[u] = 0.f;
+          for (; l + 8 <= l1; l += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] += col[(l + u) * kLagRedStride];
           }
-          for (; l < l1; ++l) a0 += col[l * kLagRedStride];
-          oh[(base + lseg[i]) * kLagSlots] += (a0 + a1) + (a2 + a3);
+#pragma unroll
+          for (int u = 0; u < 7; ++u)
+            if (l + u < l1) a[u] += col[(l + u) * kLagRedStride];
+          oh[(base + lseg[i]) * kLagSlots] += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
         }
       }
     }
@@ -534,7 +538,6 @@ __global__ void __maxnreg__(kLagMaxRegs) lag_stats_kernel(const __grid_constant_
   // The ranges as bit masks of segments, the sums unrolled over the maxima.
   if (threadIdx.x < 128) {
     const int k = threadIdx.x;
-    const int ns1 = p.nseg[1], ns2 = p.nseg[2];
     const int nr0 = p.nrange[0], nr1 = p.nrange[1], nr2 = p.nrange[2];
     unsigned m1[4], m2[4];
     bool in0[4];
@@ -544,6 +547,16 @@ __global__ void __maxnreg__(kLagMaxRegs) lag_stats_kernel(const __grid_constant_
       m2[b] = b < nr2 ? (1u << p.range[2][b][1]) - (1u << p.range[2][b][0]) : 0u;
       in0[b] = b < nr0 && s0 >= p.range[0][b][0] && s0 < p.range[0][b][1];
     }
+    // the region sums, loaded unconditionally (the region table has room
+    // for kLagMaxSeg^2 regions; cells past (ns1, ns2) are zero)
+    float R[kLagMaxSeg][kLagMaxSeg];
+#pragma unroll
+    for (int s1 = 0; s1 < kLagMaxSeg; ++s1)
+#pragma unroll
+      for (int s2 = 0; s2 < kLagMaxSeg; ++s2) {
+        const int r = s1 * kLagMaxSeg + s2;
+        R[s1][s2] = outa[r * kLagSlots + k] + outa[(kLagMaxReg2 + r) * kLagSlots + k];
+      }
     float* dst = p.part + (size_t)blockIdx.x * p.nbox * kLagSlots + k;
 #pragma unroll
     for (int b2 = 0; b2 < 4; ++b2) {
@@ -553,11 +566,7 @@ __global__ void __maxnreg__(kLagMaxRegs) lag_stats_kernel(const __grid_constant_
       for (int s1 = 0; s1 < kLagMaxSeg; ++s1) {
         float t = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < kLagMaxSeg; ++s2) {
-          const int r12 = s1 * ns2 + s2;
-          if (k < NS && s1 < ns1 && s2 < ns2 && ((m2[b2] >> s2) & 1u))
-            t += outa[r12 * kLagSlots + k] + outa[(kLagMaxReg2 + r12) * kLagSlots + k];
-        }
+        for (int s2 = 0; s2 < kLagMaxSeg; ++s2) t += ((m2[b2] >> s2) & 1u) ? R[s1][s2] : 0.f;
         T[s1] = t;
       }
 #pragma unroll
