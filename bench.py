@@ -155,6 +155,7 @@ KERNEL_SOURCES = {
     "engine": ["engine.cu", "engine.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
     "lag": ["lag.cu", "pool.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
     "pooled": ["pool.cu", "pool.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
+    "fill": ["fill.cu", "engine.cuh", "ptx.cuh", "plan.h", "plan.cpp"],
     "direct": ["direct.cu", "direct.cuh", "plan.h", "plan.cpp"],
 }
 
