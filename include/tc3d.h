@@ -174,10 +174,10 @@ int tc3d_convT_bneval_avgpool(const float* x, const float* w, const float* bias,
  *  - Problems whose workspace (tc3d_workspace_bytes) exceeds that size are
  *    rejected with TC3D_ERR_WORKSPACE before anything is launched.
  *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.  The address is kept for the life of the process, so it
- *    assumes the device's context is not torn down and re-created in between
- *    (no cudaDeviceReset of that device while the library is in use).
+ *    per device, with that device current).  The address is kept for the
+ *    life of the process, so it assumes the device's context is not torn
+ *    down and re-created in between (no cudaDeviceReset of that device while
+ *    the library is in use).
  *  - All calls share the one array: calls that overlap on the GPU (other
  *    streams, other host threads) race and give wrong results; serialise
  *    them.  Each call rewrites every scratch byte it reads, so nothing needs

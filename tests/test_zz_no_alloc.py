@@ -42,7 +42,7 @@ def _problem(seed, xs, ws):
     return [torch.from_numpy(a).cuda() for a in (x, w, b)]
 
 
-def _call_noalloc(tc, x, w, b, y, pad):
+def _call_noalloc(tc, x, w, b, y, pad, groups=1):
     I3 = ctypes.c_int * 3
     N, Cin, S0, S1, S2 = x.shape
     Cout, _, k0, k1, k2 = w.shape
@@ -50,7 +50,7 @@ def _call_noalloc(tc, x, w, b, y, pad):
     return tc.load().tc3d_conv_maxpool_lse_relu_noalloc(
         ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()),
         ctypes.c_void_p(b.data_ptr()), ctypes.c_void_p(y.data_ptr()), N, Cin, S0, S1, S2, Cout,
-        k0, k1, k2, I3(1, 1, 1), I3(pad, pad, pad), I3(1, 1, 1), I3(0, 0, 0), 1, stream)
+        k0, k1, k2, I3(1, 1, 1), I3(pad, pad, pad), I3(1, 1, 1), I3(0, 0, 0), groups, stream)
 
 
 def test_noalloc_matches_workspace_entry_point_two_calls(tc):
@@ -78,3 +78,17 @@ def test_noalloc_rejects_problems_beyond_its_scratch(tc):
     assert _call_noalloc(tc, x, w, b, y, 1) == tc.TC3D_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert bool((y == 3.0).all())
+
+
+def test_noalloc_grouped_matches_workspace_entry_point(tc):
+    """A depthwise problem (groups = Cin = Cout) through the same scratch."""
+    x, w, b = _problem(300, (2, 8, 10, 12, 16), (8, 1, 3, 3, 3))
+    ref = tc.conv_maxpool_lse_relu(x, w, b, 1, 1, groups=8)
+    y = torch.full_like(ref, float("nan"))
+    rc = _call_noalloc(tc, x, w, b, y, 1, groups=8)
+    assert rc == tc.TC3D_OK, tc.status_string(rc)
+    torch.cuda.synchronize()
+    g = y.double().cpu().numpy()
+    r = ref.double().cpu().numpy()
+    assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r))
+    assert tc.last_device_error() == tc.TC3D_OK

@@ -362,11 +362,13 @@ int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cud
     fp.O[a] = (int)pl.O[a];
     fp.zl[a] = (int)std::min<int64_t>(pl.O[a], (int64_t)pl.s_out[a] * pl.M[a]);
   }
-  // the engine's rows: the (r0, r1) pair of its one class with taps
+  // the engine's rows: the (r0, r1) pair of its one class with taps; with
+  // stride 2 along y it also writes the other y class's rows of its planes
+  const bool ybeside = pl.s_out[1] == 2;
   fp.s0 = pl.fill_rows ? pl.s_out[0] : 0;
-  fp.s1 = pl.fill_rows ? pl.s_out[1] : 0;
+  fp.s1 = pl.fill_rows ? (ybeside ? 1 : pl.s_out[1]) : 0;
   fp.r0 = pl.fill_rows ? pl.r_axis[0][0] : 0;
-  fp.r1 = pl.fill_rows ? pl.r_axis[1][0] : 0;
+  fp.r1 = pl.fill_rows && !ybeside ? pl.r_axis[1][0] : 0;
   return fill_slab_launch(fp, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
 }
 

@@ -946,9 +946,10 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             }
           } else if (p.cls_fast && p.s_out[2] == 2) {
             // one class with taps, stride 2 along x: dense stores of the
-            // rows of its class pair (r0, r1) only (both x classes: the
-            // value and the bias); the rows of the other pairs are the bias
-            // fill's.  The Q2 lanes of a row group hold consecutive m2 with
+            // rows of its class pair (r0, r1) (both x classes: the value and
+            // the bias) and, with stride 2 along y, of the other y class's
+            // row beside it (the bias); the other rows are the bias fill's.
+            // The Q2 lanes of a row group hold consecutive m2 with
             // equal (m0, m1), so the group's outputs at x = 2 m2 + r2 form
             // one run of 2 Q2 floats.  The warp's 64 values are written by 2
             // stores of 32 consecutive floats per run: writer lane l of
@@ -957,6 +958,10 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             // lane g Q2 + (i % (2 Q2)) / 2.
             const int star01 = p.cls_star >> 1, star2 = p.cls_star & 1;
             const int rstar = p.cls_r[2 * star01], offstar = p.cls_off[2 * star01];
+            // the other y class of the pair's plane: row offset and class
+            const bool ybeside = p.s_out[1] == 2;
+            const int ry = (rstar >> 8) & 255, roth = 1 - ry;
+            const long long offoth = (long long)(roth - ry) * p.O[2];
             int src[2], xodd[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -969,7 +974,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
             for (int a = 0; a < p.n_acc; ++a) {
               const uint32_t taddr = dbase + (uint32_t)(a * p.acc_cols);
               float* pk[2];
-              bool mk[2];  // this writer's output of the pair lies inside
+              bool mk[2], mo[2];  // this writer's output of the pair (of the row beside) lies inside
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 int t[3];
@@ -979,8 +984,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                 const int zb0 = p.s_out[0] * m0, zb1 = p.s_out[1] * m1, xb = 2 * m2 + xodd[k];
                 pk[k] = p.y + ((long long)tc.n * p.Cout + oc0) * ovol + (long long)zb0 * o12 +
                         (long long)zb1 * p.O[2] + xb + offstar;
-                mk[k] = rv && xb < p.O[2] && zb0 + (rstar & 255) < p.O[0] &&
-                        zb1 + ((rstar >> 8) & 255) < p.O[1];
+                const bool in = rv && xb < p.O[2] && zb0 + (rstar & 255) < p.O[0];
+                mk[k] = in && zb1 + ry < p.O[1];
+                mo[k] = ybeside && in && zb1 + roth < p.O[1];
               }
               for (int cc = 0; cc < p.n_tile; cc += 32) {
                 uint32_t v[32];
@@ -999,6 +1005,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
                   const float v1 = __shfl_sync(0xffffffffu, val, src[1]);
                   if (mk[0]) *y0 = xodd[0] == star2 ? v0 : b;
                   if (mk[1]) *y1 = xodd[1] == star2 ? v1 : b;
+                  if (mo[0]) y0[offoth] = b;
+                  if (mo[1]) y1[offoth] = b;
                   y0 += ovol;
                   y1 += ovol;
                 }

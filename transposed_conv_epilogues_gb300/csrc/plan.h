@@ -82,8 +82,9 @@ struct Plan {
   int fill_slab;
   // one class with taps whose store takes the dense stride-2-along-x path
   // (cls_fast with s_out[2] == 2): the engine writes only the output rows of
-  // that class's (r0, r1) pair, the bias fill all others (fill_rows; then
-  // fill_slab is set too)
+  // that class's (r0, r1) pair (and, with stride 2 along y, the rows of the
+  // other y class in the same planes), the bias fill all others (fill_rows;
+  // then fill_slab is set too)
   int cls_fast;
   int fill_rows;
 
