@@ -140,18 +140,19 @@ def test_conv_maxpool_lse_relu_small(tc, case):
 
 BN_CASES = [
     # x shape, w shape, stride, pad, dil, output_padding, groups, gamma/beta
-    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # fused (algebraic in eval)
+    ((2, 3, 8, 8, 8), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),        # lag form (the workload's form)
     ((2, 7, 9, 8, 10), (7, 5, 3, 3, 3), 2, 1, 1, (0, 1, 1), 1, True),  # fused, ragged
     ((2, 4, 6, 7, 8), (4, 3, 3, 3, 3), 2, 1, 1, 0, 2, True),          # fused, groups
     ((1, 5, 10, 12, 9), (5, 40, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # fused, 3 column blocks
-    ((4, 3, 24, 24, 24), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),     # fused, more tiles than CTAs
+    ((4, 3, 24, 24, 24), (3, 16, 3, 3, 3), 2, 1, 1, 0, 1, False),     # lag form, many pooled items
     ((4, 5, 24, 24, 24), (5, 16, 3, 3, 3), 2, 1, 1, 0, 1, True),     # fused, 5 channels, many tiles
-    # the algebraic path (patch Gram statistics + summed-weight pooled conv):
-    # batch statistics where the fused epilogue cannot run (one parity class
-    # per axis); running statistics always (the eval test reuses these)
+    # the algebraic path (patch Gram or lag-form statistics + summed-weight
+    # pooled conv): batch statistics where the fused epilogue cannot run (one
+    # parity class per axis); running statistics always (the eval test reuses
+    # these)
     ((2, 3, 8, 7, 9), (3, 4, 1, 1, 1), 2, 0, 1, (1, 0, 1), 1, True),  # k 1
     ((2, 4, 7, 8, 6), (4, 5, 2, 2, 2), 2, 0, 2, 1, 1, True),          # k 2, dilation 2
-    ((3, 1, 20, 22, 24), (1, 6, 1, 1, 1), 2, 0, 1, 1, 1, False),      # many thin-box units
+    ((3, 1, 20, 22, 24), (1, 6, 1, 1, 1), 2, 0, 1, 1, 1, False),      # k 1, lag form
     ((2, 2, 9, 7, 10), (2, 4, 3, 3, 3), 2, 0, 1, 0, 1, True),         # pad 0
     ((1, 4, 5, 6, 7), (4, 3, 3, 3, 3), 2, 1, 1, (1, 0, 1), 1, True),  # 32-entry patch
     ((2, 1, 9, 8, 7), (1, 4, 2, 3, 5), 2, (0, 1, 2), (1, 1, 3), 1, 1, True),  # widened pad
