@@ -553,6 +553,27 @@ def test_workload_convT_bn_avgpool_full(tc):
     assert np.all(np.abs(y.mean(axis=(0, 2, 3, 4))) < 0.05)
 
 
+def test_workload_convT_bn_avgpool_uniform01_affine(tc):
+    """The same workload with torch.rand-style inputs (all positive: the
+    transposed conv's mean is far from 0, so the statistics difference
+    E[t^2] - mean^2 cancels) and a non-trivial gamma / beta, on sampled
+    outputs plus two whole (sample, channel) blocks."""
+    wl = BY_NAME["convT_bn_avgpool"]
+    x, w, b = wl.make_inputs(x_dist="uniform01")
+    c = wl.cout
+    g = inputs.uniform(4401, (c,), 0.5, 1.5)
+    be = inputs.uniform(4402, (c,), -0.5, 0.5)
+    y = tc.convT_bn_avgpool(_dev(x), _dev(w), _dev(b), _dev(g), _dev(be), wl.eps,
+                            **wl.kwargs()).cpu().numpy()
+    flat = y.ravel()
+    per_nc = int(np.prod(y.shape[2:]))
+    idx = inputs.sample_indices(4403, flat.size, 20000)
+    blocks = [np.arange(per_nc, dtype=np.int64) + (n * c + co) * per_nc for n, co in ((0, 0), (63, 15))]
+    idx = np.concatenate([idx] + blocks)
+    ref = orc.convT_bn_avgpool_at(x, w, b, idx, g, be, wl.eps, **wl.kwargs())
+    check(flat[idx], ref, wl.name + " uniform01")
+
+
 def test_workload_convT_bneval_avgpool_sampled(tc):
     """The transposed-conv + BN + pool workload in evaluation mode."""
     wl, x, w, b = _wl("convT_bn_avgpool")
