@@ -109,6 +109,14 @@ CONVT_CASES = [
     ((1, 3, 2, 3, 40), (3, 40, 3, 3, 3), 2, 1, 2, 0, 1, True),
     # one parity class with taps, stride 1 along x
     ((1, 3, 4, 5, 6), (3, 4, 3, 3, 3), (2, 2, 1), 1, (2, 2, 1), 0, 1, True),
+    # no engine tiles (the only class with taps lies past the output): every
+    # output is the bias, written by the stand-alone fill
+    ((2, 3, 2, 2, 2), (3, 4, 1, 1, 1), 2, 1, 1, 0, 1, True),
+    ((2, 3, 2, 5, 6), (3, 4, 1, 3, 3), 2, (1, 1, 0), 1, 0, 1, True),
+    # the bias fill inside the engine over many slices and planes (units
+    # taken from the shared counter by every CTA), with and without bias
+    ((3, 8, 9, 10, 12), (8, 24, 3, 3, 3), 2, 1, 2, 0, 1, True),
+    ((3, 8, 9, 10, 12), (8, 24, 3, 3, 3), 2, 1, 2, (1, 1, 1), 1, False),
 ]
 
 
@@ -403,9 +411,9 @@ def test_deterministic_repeat(tc):
 
 
 def test_fill_stream_does_not_couple_callers(tc):
-    """A transposed conv forks its bias slab fill onto an auxiliary stream of
-    its caller's stream.  Work another caller queued on another stream must
-    not hold it up: stream B sleeps (a bounded spin kernel) before its own
+    """A transposed conv with a bias fill enqueues all its work on the
+    caller's stream.  Work another caller queued on another stream must not
+    hold it up: stream B sleeps (a bounded spin kernel) before its own
     transposed conv; the call on stream A, queued after it, still completes
     while B sleeps."""
     x, w, b = make((2, 6, 5, 7, 8), (6, 10, 3, 3, 3), 10)   # k3 s2 p1 d2: a bias slab
@@ -433,10 +441,10 @@ def test_fill_stream_does_not_couple_callers(tc):
 
 
 def test_cuda_graph_capture_replays(tc):
-    """Every entry point enqueues only stream-ordered work: the transposed
-    conv's bias slab fill forks onto the library's auxiliary stream and joins
-    back through events.  So a call can be captured into a CUDA graph and
-    replayed, giving the same bits as a direct call."""
+    """Every entry point enqueues only stream-ordered work on the caller's
+    stream (the transposed conv's bias fill runs inside the engine).  So a
+    call can be captured into a CUDA graph and replayed, giving the same bits
+    as a direct call."""
     calls = []
     x, w, b = make((2, 8, 7, 9, 8), (5, 8, 3, 3, 1), 5)                 # conv, view mode
     calls.append((tc.OP_CONV3D, (_dev(x), _dev(w), _dev(b)), dict(stride=1, padding=(1, 1, 0))))

@@ -19,7 +19,7 @@ BUILD = ROOT / "_build"
 LIB = PKG / "libtc3d.so"
 
 SOURCES = ["engine.cu", "api.cu", "plan.cpp", "noalloc.cu", "pool.cu", "direct.cu", "lag.cu", "fill.cu"]
-HEADERS = ["engine.cuh", "plan.h", "ptx.cuh", "pool.cuh", "direct.cuh"]
+HEADERS = ["engine.cuh", "fill.cuh", "plan.h", "ptx.cuh", "pool.cuh", "direct.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

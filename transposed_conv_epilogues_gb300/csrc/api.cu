@@ -40,44 +40,11 @@ struct DeviceState {
   bool gram_smem_set = false;
   bool direct_smem_set = false;
   bool lag_smem_set = false;
-  // auxiliary streams for the bias slab fill, which runs beside the engine:
-  // one per caller stream (fork / join through two events of its own), so a
-  // fill never waits behind work another caller queued; calls enqueue under
-  // g_fork_mu
-  struct Aux {
-    cudaStream_t caller = nullptr;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-  };
-  static constexpr int kMaxAux = 32;
-  Aux aux[kMaxAux];
-  int n_aux = 0;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
-std::mutex g_fork_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// The auxiliary stream and events of caller stream st (created on its first
-// use; nullptr once kMaxAux caller streams have one: the fill then runs on
-// st itself).  Call with g_fork_mu held.
-DeviceState::Aux* aux_for(DeviceState* d, cudaStream_t st) {
-  for (int i = 0; i < d->n_aux; ++i)
-    if (d->aux[i].caller == st) return &d->aux[i];
-  if (d->n_aux == DeviceState::kMaxAux) return nullptr;
-  DeviceState::Aux a;
-  a.caller = st;
-  if (cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
-    cudaGetLastError();  // leave no error behind for the next launch check
-    if (a.aux) cudaStreamDestroy(a.aux);
-    if (a.fork) cudaEventDestroy(a.fork);
-    return nullptr;
-  }
-  d->aux[d->n_aux] = a;
-  return &d->aux[d->n_aux++];
-}
 
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -319,10 +286,13 @@ bool encode_pooled_map(const Problem& pb, const float* x, PooledParams* pq) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cudaStream_t st) {
+// fill_ctr: the engine's bias-fill counter, zeroed by the pack kernel (or nullptr)
+int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cudaStream_t st,
+                unsigned long long* fill_ctr = nullptr) {
   PackParams pp;
   std::memset(&pp, 0, sizeof(pp));
   pp.w = w;
+  pp.zero_ctr = fill_ctr;
   pp.out = wpack;
   pp.transposed = pl.transposed;
   pp.cin_g = pl.cin_g;
@@ -351,11 +321,13 @@ int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cuda
   return pack_launch(pp, (unsigned)blocks, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
 }
 
-int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cudaStream_t st) {
-  if (!pl.fill_slab) return TC3D_OK;
+// The bias fill of the outputs no engine tile writes (a transposed conv's
+// tap-less classes and rows past its row grid)
+FillParams make_fill(const Plan& pl, const float* bias, float* y) {
   FillParams fp;
   fp.y = y;
   fp.bias = bias;
+  fp.ctr = nullptr;
   fp.NC = (int)(pl.pb.N * pl.pb.Cout);
   fp.Cout = (int)pl.pb.Cout;
   for (int a = 0; a < 3; ++a) {
@@ -369,15 +341,26 @@ int launch_fill(const Plan& pl, const float* bias, float* y, DeviceState* d, cud
   fp.s1 = pl.fill_rows ? (ybeside ? 1 : pl.s_out[1]) : 0;
   fp.r0 = pl.fill_rows ? pl.r_axis[0][0] : 0;
   fp.r1 = pl.fill_rows && !ybeside ? pl.r_axis[1][0] : 0;
-  return fill_slab_launch(fp, st) == cudaSuccess ? TC3D_OK : TC3D_ERR_CUDA;
+  return fp;
 }
 
 int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, const float* bias,
                   float* y, float2* partials, DeviceState* d, cudaStream_t st,
-                  const float2* bn_affine = nullptr) {
-  if (pl.tiles == 0) return TC3D_OK;
+                  const float2* bn_affine = nullptr, unsigned long long* fill_ctr = nullptr) {
+  // the store epilogue's fill warp does the bias fill; without tiles the
+  // stand-alone fill kernel does it
+  const bool fill = epi == EPI_STORE && pl.fill_slab;
+  if (pl.tiles == 0)
+    return !fill || fill_slab_launch(make_fill(pl, bias, y), st) == cudaSuccess ? TC3D_OK
+                                                                               : TC3D_ERR_CUDA;
   EngineParams ep;
   fill_params(pl, &ep);
+  ep.fill_on = fill ? 1 : 0;
+  if (fill) {
+    if (!fill_ctr) return TC3D_ERR_UNSUPPORTED;
+    ep.fill = make_fill(pl, bias, y);
+    ep.fill.ctr = fill_ctr;
+  }
   ep.x = x;
   ep.wpack = wpack;
   ep.bias = bias;
@@ -795,30 +778,12 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
   }
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* wpack = reinterpret_cast<float*>(wsb + pl.ws_wpack_off);
-  rc = launch_pack(pl, w, wpack, d->sm_count, st);
+  // the bias fill (a transposed conv's tap-less outputs) runs inside the engine
+  unsigned long long* ctr =
+      pl.fill_slab ? reinterpret_cast<unsigned long long*>(wsb + pl.ws_ctr_off) : nullptr;
+  rc = launch_pack(pl, w, wpack, d->sm_count, st, ctr);
   if (rc) return rc;
-  if (!is_bn_op(op)) {
-    if (!pl.fill_slab) return launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
-    // The slab fill writes only outputs the engine does not, so it runs beside
-    // the engine on the auxiliary stream: fork after the work queued so far
-    // on st, join before anything queued on st later.
-    std::lock_guard<std::mutex> lk(g_fork_mu);
-    DeviceState::Aux* a = aux_for(d, st);
-    if (!a) {
-      rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
-      return rc ? rc : launch_fill(pl, bias, y, d, st);
-    }
-    if (cudaEventRecord(a->fork, st) != cudaSuccess) return TC3D_ERR_CUDA;
-    rc = launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st);
-    if (rc) return rc;
-    if (cudaStreamWaitEvent(a->aux, a->fork, 0) != cudaSuccess) return TC3D_ERR_CUDA;
-    rc = launch_fill(pl, bias, y, d, a->aux);
-    if (rc) return rc;
-    if (cudaEventRecord(a->join, a->aux) != cudaSuccess ||
-        cudaStreamWaitEvent(st, a->join, 0) != cudaSuccess)
-      return TC3D_ERR_CUDA;
-    return TC3D_OK;
-  }
+  if (!is_bn_op(op)) return launch_engine(pl, pl.epi, x, wpack, bias, y, nullptr, d, st, nullptr, ctr);
 
   float2* stat = reinterpret_cast<float2*>(wsb + pl.ws_stat_off);
   const long long pvol = (long long)pl.P[0] * pl.P[1] * pl.P[2];
@@ -832,9 +797,7 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
       return TC3D_ERR_CUDA;
     if (pl.fused) return launch_engine(pl, EPI_BN_POOL, x, wpack, bias, y, nullptr, d, st, stat);
     float* full = reinterpret_cast<float*>(wsb + pl.ws_full_off);
-    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st);
-    if (rc) return rc;
-    rc = launch_fill(pl, bias, full, d, st);
+    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st, nullptr, ctr);
     if (rc) return rc;
     const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
     const int P[3] = {(int)pl.P[0], (int)pl.P[1], (int)pl.P[2]};
@@ -855,9 +818,7 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
   } else {
     float* full = reinterpret_cast<float*>(wsb + pl.ws_full_off);
     double* part2 = reinterpret_cast<double*>(wsb + pl.ws_part_off);
-    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st);
-    if (rc) return rc;
-    rc = launch_fill(pl, bias, full, d, st);
+    rc = launch_engine(pl, EPI_STORE, x, wpack, bias, full, nullptr, d, st, nullptr, ctr);
     if (rc) return rc;
     const int O[3] = {(int)pl.O[0], (int)pl.O[1], (int)pl.O[2]};
     const int P[3] = {(int)pl.P[0], (int)pl.P[1], (int)pl.P[2]};

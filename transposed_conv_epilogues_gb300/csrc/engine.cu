@@ -21,10 +21,14 @@
 //                            the odd ones, so that one issuer's barrier wait
 //                            and commit overlap the other's queued MMAs.
 //   warps 4.. (epilogue)     tcgen05.ld of D and the fused epilogue
+//   The store epilogue's warps also do the bias fill of a transposed conv's
+//   outputs that no tile writes: a part of it per tile iteration, and what
+//   is left after their last tile.
 //
 // Every mbarrier wait is bounded; on time-out the CTA sets an error word and
 // all roles return, TMEM is freed, the kernel exits.
 #include "engine.cuh"
+#include "fill.cuh"
 #include "ptx.cuh"
 
 namespace tc3d {
@@ -523,6 +527,53 @@ __device__ __forceinline__ void view_conversion_role(const EngineParams& p, cons
   }
 }
 
+// The bias fill inside the engine.  The epilogue warps of all CTAs take the
+// fill's (slice, plane) units one at a time from a shared counter.  During
+// the tile loop a warp does a paced quota, its even share of the units
+// spread over the CTA's tile iterations (a burst of fill stores at the start
+// would hold up the engine's own loads and evict its input from L2); after
+// its last tile it takes units until none are left, so CTAs that finish
+// their tiles early do more of the fill.
+struct EngineFill {
+  const FillParams* f;
+  long long units, share, done;
+  bool left;  // units may remain
+
+  __device__ __forceinline__ void init(const EngineParams& p, int nparts) {
+    f = &p.fill;
+    units = p.fill_on ? (long long)f->NC * f->O[0] : 0;
+    share = units / ((long long)gridDim.x * nparts);
+    done = 0;
+    left = units > 0;
+  }
+  // take a unit and fill it (whole warp); false when none was left
+  __device__ __forceinline__ bool step(int lane) {
+    unsigned long long idx = 0;
+    if (lane == 0) idx = atomicAdd(f->ctr, 1ull);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx >= (unsigned long long)units) {
+      left = false;
+      return false;
+    }
+    const int nc = (int)(idx / (unsigned long long)f->O[0]);
+    const int z = (int)(idx - (unsigned long long)nc * f->O[0]);
+    const float b = f->bias ? __ldg(f->bias + nc % f->Cout) : 0.f;
+    fill_plane(*f, nc, z, b, lane);
+    ++done;
+    return true;
+  }
+  // the quota up to fraction k / n of the share
+  __device__ __forceinline__ void upto(long long k, long long n, int lane,
+                                       const volatile int* abortf) {
+    const long long target = share * k / n;
+    while (left && done < target && !*abortf) step(lane);
+  }
+  // every unit still left
+  __device__ __forceinline__ void drain(int lane, const volatile int* abortf) {
+    while (left && !*abortf) step(lane);
+  }
+};
+
 }  // namespace
 
 template <int EPI, bool VIEW>
@@ -874,6 +925,12 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     }
     // running statistics: the affine map is known, no partial sums
     const bool bn_eval = EPI == EPI_BN_POOL && p.bn_affine != nullptr;
+    EngineFill fill;
+    fill.init(p, WarpCfg<EPI>::kEpiWarps);
+    // tile iterations of this CTA (the fill's pace)
+    const long long n_it =
+        (long long)((p.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) *
+        p.n_colblocks;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(p, tile);
       // pool-LSE running state per accumulator (channels this lane holds)
@@ -890,6 +947,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
         // channels 8g..8g+7).  A single group (pool + logsumexp) takes every
         // tile too.  Otherwise, with two accumulator buffers group g takes
         // buffer g; with one, group 0 takes every tile.
+        if constexpr (EPI == EPI_STORE) fill.upto(it_d + 1, n_it + 1, lane, abortf);
         constexpr bool kAllTiles =
             EPI == EPI_BN_POOL || WarpCfg<EPI>::kEpiWarps == kEpiGroup;
         if (!kAllTiles && (p.dbuf == 2 ? ((it_d & 1) != egroup) : (egroup != 0))) continue;
@@ -1242,6 +1300,7 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
         if (lane == 0) mbar_arrive(bars.d_empty(dslot));
       }
     }
+    if constexpr (EPI == EPI_STORE) fill.drain(lane, abortf);
     if constexpr (EPI == EPI_BN_POOL) {
       if (ok && p.n_colblocks == 1 && !bn_eval) {
         // slot: CTA-major, then lane quarter; each channel's slots are all
@@ -1277,6 +1336,7 @@ template __global__ void engine_kernel<EPI_STORE, true>(const __grid_constant__ 
 // the two K-halves of a row group 128 bytes apart, row groups 256 apart).
 // ---------------------------------------------------------------------------
 __global__ void pack_weights_kernel(const __grid_constant__ PackParams p) {
+  if (p.zero_ctr && blockIdx.x == 0 && threadIdx.x == 0) *p.zero_ctr = 0ull;
   const long long per_step = 2LL * p.n_tile * 8;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.total;
        i += (long long)gridDim.x * blockDim.x) {

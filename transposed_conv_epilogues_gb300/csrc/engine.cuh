@@ -16,8 +16,11 @@ namespace tc3d {
 //   warp 3        MMA issuer of the odd accumulators (idle with one)
 //   warps 4..     epilogue: one group of 4 warps (TMEM lane quarter = warp % 4),
 //                 or two groups that alternate accumulator buffers when the
-//                 epilogue uses two buffers (stores, BatchNorm pooling)
+//                 epilogue uses two buffers (stores, BatchNorm pooling);
+//                 the store epilogue also does the bias fill of the outputs
+//                 no tile writes (a transposed conv's tap-less classes)
 //   last 8 warps  conversion: raw fp32 -> (x, x - trunc(x)) in TMEM
+// (20 warps at most: an SM sub-partition's 16K registers hold 5 warps of 96.)
 constexpr int kWarpRaw = 0;
 constexpr int kWarpB = 1;
 constexpr int kWarpMMA = 2;
@@ -64,6 +67,20 @@ __host__ __device__ __forceinline__ int fast_div(const FastDiv& f, int n) {
 constexpr int kMaxRawStages = 3;
 constexpr int kMaxBStages = 16;
 constexpr int kMaxAStages = 16;  // TMEM A-stage ring: one K-step of all accumulators per stage
+
+// Bias fill of a transposed conv: bias (or 0) into the outputs at z_a >=
+// zl[a] for any axis a (outputs of rows past the GEMM row grid; all of them
+// in classes without taps) and, with s0 > 0, into every output row (z, y)
+// with z % s0 != r0 or y % s1 != r1 (rows of tap-less class pairs)
+struct FillParams {
+  float* y;           // [N * Cout][O0][O1][O2]
+  const float* bias;  // [Cout] or nullptr (0)
+  int NC, Cout, O[3], zl[3];
+  int s0, s1, r0, r1;  // s0 == 0: no row mode
+  // inside the engine: the next unit to take, shared by all CTAs (zeroed by
+  // the weight pre-pack before the engine starts)
+  unsigned long long* ctr;
+};
 
 struct EngineParams {
   CUtensorMap xmap;  // 5-D map over x (dims S2, S1, S0, C, N), used when use_tma
@@ -119,6 +136,11 @@ struct EngineParams {
   // folded into shift; the epilogue then stores final values and no partial
   // sums.  nullptr: batch statistics.
   const float2* bn_affine;
+
+  // store epilogue: the bias fill of the outputs no tile writes, done by the
+  // epilogue warps (fill_on = 0: none)
+  FillParams fill;
+  int fill_on;
 };
 
 struct PackParams {
@@ -134,6 +156,7 @@ struct PackParams {
   int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
   int octet_major;  // 1: K-step j of a chunk is channel octet j / nUtot at tap j % nUtot
   long long total;  // floats in the packed buffer
+  unsigned long long* zero_ctr;  // set to 0 when non-null (the engine's bias-fill counter)
 };
 
 // host-side launch wrappers (engine.cu; kernels are launched from the
@@ -161,16 +184,7 @@ cudaError_t bn_unfused_launch(const float* full, float* y, double* part2, int N,
                               const int O[3], const int P[3], const float* gamma,
                               const float* beta, float eps, float2* stat, unsigned blocks,
                               cudaStream_t st);
-// bias (or 0) into the outputs at z_a >= zl[a] for any axis a (outputs of
-// rows past the GEMM row grid; all of them in classes without taps) and,
-// with s0 > 0, into every output row (z, y) with z % s0 != r0 or y % s1 !=
-// r1 (rows of tap-less class pairs)
-struct FillParams {
-  float* y;           // [N * Cout][O0][O1][O2]
-  const float* bias;  // [Cout] or nullptr (0)
-  int NC, Cout, O[3], zl[3];
-  int s0, s1, r0, r1;  // s0 == 0: no row mode
-};
+// the stand-alone fill (grids without engine tiles)
 cudaError_t fill_slab_launch(const FillParams& p, cudaStream_t st);
 cudaError_t wait_timeout_launch(int* err, unsigned long long timeout_cycles, cudaStream_t st);
 

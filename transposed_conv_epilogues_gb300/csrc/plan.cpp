@@ -485,6 +485,10 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     pl.ws_wpack_off = off;
     pl.ws_wpack_bytes = (int64_t)pl.n_colblocks * pl.n_chunks * pl.ksteps_chunk * 64 * pl.n_tile;
     off = round_up(off + pl.ws_wpack_bytes, 256);
+    if (pl.fill_slab) {
+      pl.ws_ctr_off = off;
+      off = round_up(off + 8, 256);
+    }
     if (is_bn_op(pb.op)) {
       pl.ws_part_off = off;
       // batch statistics: fused, enough slots for any grid; unfused, per

@@ -127,6 +127,7 @@ struct Plan {
 
   // workspace (bytes, each region 256-aligned)
   int64_t ws_wpack_off, ws_wpack_bytes;
+  int64_t ws_ctr_off;                   // bias fill: the engine's unit counter (8 bytes)
   int64_t ws_part_off, ws_part_bytes;   // BN partials (batch statistics only): fused
                                         // [Cout][slots] float2, else [N][Cout] double2
   int64_t ws_stat_off, ws_stat_bytes;   // BN scale/shift [Cout] float2
