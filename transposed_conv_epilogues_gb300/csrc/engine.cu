@@ -651,6 +651,9 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above touches no global memory; everything below may read
+  // what the previous kernel of the stream (the weight pre-pack) wrote
+  grid_dependency_wait();
   const int dcols = p.n_acc * p.acc_cols;  // columns of one D buffer
   const uint32_t a_col0 = (uint32_t)(p.dbuf * dcols);
 
@@ -1336,6 +1339,9 @@ template __global__ void engine_kernel<EPI_STORE, true>(const __grid_constant__ 
 // the two K-halves of a row group 128 bytes apart, row groups 256 apart).
 // ---------------------------------------------------------------------------
 __global__ void pack_weights_kernel(const __grid_constant__ PackParams p) {
+  // the engine that follows may start its set-up now; it waits for this
+  // grid's completion before it reads the packed weights or the counter
+  grid_launch_dependents();
   if (p.zero_ctr && blockIdx.x == 0 && threadIdx.x == 0) *p.zero_ctr = 0ull;
   const long long per_step = 2LL * p.n_tile * 8;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.total;
@@ -1536,23 +1542,24 @@ cudaError_t engine_set_smem(int kid, int bytes) {
   }
 }
 
+// The engine is launched as a dependent of the weight pre-pack before it:
+// its launch and set-up overlap the pre-pack's tail.
 cudaError_t engine_launch(int kid, const EngineParams& p, unsigned grid, size_t smem,
                           cudaStream_t st) {
   switch (kid) {
     case EPI_STORE:
-      engine_kernel<EPI_STORE, false><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
-      break;
+      return launch_dependent(engine_kernel<EPI_STORE, false>, dim3(grid),
+                              dim3(WarpCfg<EPI_STORE>::kThreads), smem, st, p);
     case EPI_POOL_LSE:
-      engine_kernel<EPI_POOL_LSE, false><<<grid, WarpCfg<EPI_POOL_LSE>::kThreads, smem, st>>>(p);
-      break;
+      return launch_dependent(engine_kernel<EPI_POOL_LSE, false>, dim3(grid),
+                              dim3(WarpCfg<EPI_POOL_LSE>::kThreads), smem, st, p);
     case EPI_BN_POOL:
-      engine_kernel<EPI_BN_POOL, false><<<grid, WarpCfg<EPI_BN_POOL>::kThreads, smem, st>>>(p);
-      break;
+      return launch_dependent(engine_kernel<EPI_BN_POOL, false>, dim3(grid),
+                              dim3(WarpCfg<EPI_BN_POOL>::kThreads), smem, st, p);
     default:
-      engine_kernel<EPI_STORE, true><<<grid, WarpCfg<EPI_STORE>::kThreads, smem, st>>>(p);
-      break;
+      return launch_dependent(engine_kernel<EPI_STORE, true>, dim3(grid),
+                              dim3(WarpCfg<EPI_STORE>::kThreads), smem, st, p);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t pack_launch(const PackParams& pp, unsigned blocks, cudaStream_t st) {

@@ -12,25 +12,6 @@
 
 namespace tc3d {
 
-// Launch a kernel that may start before the previous kernel of the stream
-// ends (programmatic dependent launch); the kernel waits for it with
-// grid_dependency_wait before reading what it wrote.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 // Gram CTA: 32q threads per 8x8 Gram block, q = max(1, 8 / blocks), so
 // 256 threads for up to 8 blocks and 320 for the 10 blocks of a 32-entry patch
 constexpr int kGramMaxThreads = 320;
