@@ -113,6 +113,13 @@ CONVT_CASES = [
     # output is the bias, written by the stand-alone fill
     ((2, 3, 2, 2, 2), (3, 4, 1, 1, 1), 2, 1, 1, 0, 1, True),
     ((2, 3, 2, 5, 6), (3, 4, 1, 3, 3), 2, (1, 1, 0), 1, 0, 1, True),
+    # row mode of the fill with other strides: y stride 4 (rows y % 4 != r1
+    # filled a warp per row for long rows, a lane per row for short ones),
+    # and y stride 1 with z stride 3 or 4 (whole planes z % s0 != r0)
+    ((1, 3, 4, 5, 20), (3, 4, 3, 3, 3), (1, 4, 2), 1, (1, 4, 2), 0, 1, True),
+    ((2, 3, 3, 4, 6), (3, 5, 3, 3, 3), (1, 4, 2), 1, (1, 4, 2), (0, 3, 1), 1, True),
+    ((1, 2, 3, 4, 18), (2, 4, 3, 3, 3), (3, 1, 2), (1, 0, 1), (3, 1, 2), 0, 1, True),
+    ((2, 4, 3, 5, 7), (4, 6, 2, 2, 2), (4, 1, 2), (1, 1, 1), (4, 1, 2), (2, 0, 1), 1, False),
     # the bias fill inside the engine over many slices and planes (units
     # taken from the shared counter by every CTA), with and without bias
     ((3, 8, 9, 10, 12), (8, 24, 3, 3, 3), 2, 1, 2, 0, 1, True),
