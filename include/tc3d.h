@@ -44,8 +44,10 @@
  *  - workspace: caller-owned device memory of at least the size
  *    tc3d_workspace_bytes reports for the same arguments, 256-byte aligned.
  *    It holds the tensor-core-packed weights (and, for the fused BatchNorm,
- *    the per-tile partial sums).  The library never allocates or frees
- *    device memory and never frees caller pointers.
+ *    the per-tile partial sums; for a transposed conv with outputs that
+ *    hold only the bias, the counter that shares their fill among CTAs).
+ *    The library never allocates or frees device memory and never frees
+ *    caller pointers.
  *  - All work is enqueued on `stream`; nothing synchronises.  Input and
  *    output buffers must not overlap each other or the workspace.
  *  - Return value: TC3D_OK (0) or a negative TC3D_ERR_* code.  Argument
