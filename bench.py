@@ -308,15 +308,18 @@ def run_ours(args):
     # bias fill runs inside the engine; + BatchNorm finalize and apply for
     # batch statistics; + the running-statistics affine for evaluation mode)
     # (the convT_bneval path: finalize + pack + pooled conv; grouped convs
-    # with few channels per group: one direct launch; channels-last through
-    # the engine: transpose + pack + engine + transpose)
+    # with few channels per group: one direct launch; channels-last convs
+    # the engine's channels-last mode does not take: transpose + pack +
+    # engine + transpose)
     def launches(wl):
         if wl.op in ("conv3d", "conv3d_ndhwc"):
             pl = tc.plan_describe(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
                                   wl.dilation, wl.output_padding, wl.groups)
             if pl.get("direct"):
                 return 1
-            return 4 if wl.op == "conv3d_ndhwc" else 2
+            # channels-last outside the engine's channels-last mode: + the two
+            # layout transposes
+            return 4 if wl.op == "conv3d_ndhwc" and not pl.get("cl") else 2
         if wl.op in ("convT_bn_avgpool", "convT_bneval_avgpool"):
             pl = tc.plan_describe(op_of[wl.op], wl.x_shape, wl.w_shape, wl.stride, wl.padding,
                                   wl.dilation, wl.output_padding, wl.groups)

@@ -170,7 +170,9 @@ def test_convT_bneval_avgpool_argument_errors(lib):
 
 def test_direct_and_ndhwc_plans(lib):
     """Grouped convs with few channels per group take the direct kernel;
-    channels-last shapes and workspace through the transposes."""
+    dense channels-last convs the engine's channels-last mode (workspace: the
+    packed weights only); grouped ones that are not direct the route through
+    two layout transposes (workspace: + NCDHW copies of x and y)."""
     dw = tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8)
     assert dw["direct"] == 1 and dw["ndhwc"] == 0
     assert tc.plan_describe(0, (2, 8, 7, 9, 8), (12, 4, 3, 3, 3), 1, 1, 1, 0, 2)["direct"] == 0
@@ -179,11 +181,16 @@ def test_direct_and_ndhwc_plans(lib):
     assert tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 8), 1, 1, 1, 0, 8)["direct"] == 0
     assert tc.plan_describe(0, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 3, 1, 1, 0, 8)["direct"] == 0
     nd = tc.plan_describe(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)
-    assert nd["ndhwc"] == 1 and nd["direct"] == 0
+    assert nd["ndhwc"] == 1 and nd["direct"] == 0 and nd["cl"] == 1 and nd["view"] == 0
     assert tc.out_shape(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1) == (2, 9, 10, 12, 7)
     dense = tc.workspace_bytes(5, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1)
-    assert dense >= tc.workspace_bytes(0, (2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1) + \
-        4 * (2 * 5 * 9 * 10 * 12 + 2 * 7 * 9 * 10 * 12)
+    assert dense < 4 * (2 * 5 * 9 * 10 * 12 + 2 * 7 * 9 * 10 * 12)
+    # grouped, 8 x 8 channels per group: not direct, not channels-last mode
+    g2 = tc.plan_describe(5, (2, 16, 9, 10, 12), (16, 8, 3, 3, 3), 1, 1, 1, 0, 2)
+    assert g2["ndhwc"] == 1 and g2["direct"] == 0 and g2["cl"] == 0
+    assert tc.workspace_bytes(5, (2, 16, 9, 10, 12), (16, 8, 3, 3, 3), 1, 1, 1, 0, 2) >= \
+        tc.workspace_bytes(0, (2, 16, 9, 10, 12), (16, 8, 3, 3, 3), 1, 1, 1, 0, 2) + \
+        4 * (2 * 16 * 9 * 10 * 12 + 2 * 16 * 9 * 10 * 12)
     assert tc.workspace_bytes(5, (2, 8, 9, 10, 13), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
 
 
@@ -230,11 +237,14 @@ def test_direct_forms(lib):
 
 
 def test_ndhwc_transpose_route_limits(lib):
-    """The channels-last route through the engine transposes with batch in
-    the grid's y dimension: a batch above 65535 is rejected on the host."""
+    """The channels-last route through two layout transposes puts the batch
+    in the transpose grid's y dimension: a batch above 65535 is rejected on
+    the host.  The engine's channels-last mode has no such limit."""
     with pytest.raises(tc.Tc3dError) as e:
-        tc.workspace_bytes(5, (70000, 5, 4, 4, 4), (7, 5, 3, 3, 3), 1, 1)
+        tc.workspace_bytes(5, (70000, 16, 4, 4, 4), (16, 8, 3, 3, 3), 1, 1, 1, 0, 2)
     assert e.value.status == tc.TC3D_ERR_UNSUPPORTED
+    assert tc.plan_describe(5, (70000, 5, 4, 4, 4), (7, 5, 3, 3, 3), 1, 1)["cl"] == 1
+    assert tc.workspace_bytes(5, (70000, 5, 4, 4, 4), (7, 5, 3, 3, 3), 1, 1) > 0
     # the direct kernel (few channels per group) has no such limit
     assert tc.workspace_bytes(5, (70000, 8, 4, 4, 4), (8, 1, 3, 3, 3), 1, 1, 1, 0, 8) == 256
 
@@ -345,6 +355,8 @@ def test_plans_of_workloads(lib):
     # dense channels-last conv through the engine
     assert plan("dwconv_k3")["direct"] == 1 and plan("dwconv_k3_ndhwc")["direct"] == 1
     assert plan("conv_k3_ndhwc")["direct"] == 0 and plan("conv_k3_ndhwc")["ndhwc"] == 1
+    k3 = plan("conv_k3_ndhwc")
+    assert k3["cl"] == 1 and k3["cin_chunk"] == 16 and k3["cl_cb"] == 20
 
 
 @pytest.mark.parametrize("s, d, want", [
@@ -362,3 +374,29 @@ def test_fill_rows_plan(lib, s, d, want):
     assert pl["status"] == 0 and pl["fill_rows"] == want
     if want:
         assert pl["fill_slab"] == 1 and pl["nR"] == 1
+
+
+@pytest.mark.parametrize("cin", [3, 8, 12, 16, 32, 40])
+@pytest.mark.parametrize("xext", [16, 64])
+def test_channels_last_chunks(lib, cin, xext):
+    """The engine's channels-last mode: a raw box of cl_cb = cin_chunk + 4
+    channels per position (cl_cb / 4 odd: 16-byte loads of consecutive
+    positions start in distinct bank groups), GEMM-K tap-major in chunks of
+    8, 16, 24 or 32 channels, the fewest K-steps over all chunks among those
+    whose raw stage fits (at most 96 KB)."""
+    pl = tc.plan_describe(5, (2, cin, 6, 8, xext), (16, cin, 3, 3, 3), 1, 1)
+    assert pl["status"] == 0 and pl["cl"] == 1 and pl["view"] == 0
+    cc = pl["cin_chunk"]
+    assert cc in (8, 16, 24, 32) and pl["cl_cb"] == cc + 4 and (pl["cl_cb"] // 4) % 2 == 1
+    assert pl["ksteps_chunk"] == (cc // 8) * 27 and pl["n_chunks"] == -(-cin // cc)
+    assert pl["smem_bytes"] <= 227 * 1024
+    bvol = pl["box"][0] * pl["box"][1] * pl["box"][2]
+    assert pl["raw_stage_bytes"] >= bvol * pl["cl_cb"] * 4
+    steps = pl["n_chunks"] * pl["ksteps_chunk"]
+    for c2 in (8, 16, 24, 32):
+        if c2 <= -(-cin // 8) * 8 and bvol * (c2 + 4) * 4 <= 96 * 1024:
+            assert steps <= -(-cin // c2) * (c2 // 8) * 27
+    # the box has no x slack: channels, not x, are the innermost axis
+    assert pl["box"][2] == pl["T"][2] + 2
+    # transposed convs keep the NCDHW planning
+    assert tc.plan_describe(3, (2, cin, 6, 8, xext), (cin, 16, 3, 3, 3), 2, 1)["cl"] == 0

@@ -309,9 +309,20 @@ def test_direct_grouped_conv(tc, case):
 
 NDHWC_CASES = DIRECT_CASES[:3] + DIRECT_CASES[5:6] + [
     ((1, 3, 7, 35, 133), (6, 1, 2, 3, 3), (1, 1, 2), (0, 1, 1), 1, 3),
-    # not for the direct kernel: through the engine with layout transposes
+    ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1),           # (k,k,1), direct
+    # not for the direct kernel: the engine's channels-last mode (5 channels,
+    # not a multiple of 4: plain loads of the box instead of TMA)
     ((2, 5, 9, 10, 12), (7, 5, 3, 3, 3), 1, 1, 1, 1),
-    ((2, 3, 11, 9, 5), (4, 3, 3, 3, 1), 1, (1, 1, 0), 1, 1),           # (k,k,1): merged form
+    # channels-last mode through TMA: a ragged output-channel chunk (24),
+    # strides and dilation 2 (4 chunks of 8 channels), channels past Cin
+    # zero-filled by the load (12 in a 16-channel chunk), a ragged last chunk
+    # (40 = 5 x 8)
+    ((2, 16, 7, 9, 20), (24, 16, 3, 3, 3), 1, 1, 1, 1),
+    ((2, 32, 5, 9, 14), (64, 32, 3, 3, 3), (2, 1, 2), 1, (1, 2, 1), 1),
+    ((2, 12, 6, 5, 9), (20, 12, 2, 3, 1), 1, (0, 1, 0), 1, 1),
+    ((1, 40, 4, 7, 12), (8, 40, 3, 1, 3), 1, 1, 1, 1),
+    # grouped, 4 x 6 channels per group: through the engine with layout
+    # transposes
     ((1, 8, 6, 7, 9), (12, 4, 3, 2, 3), (1, 2, 1), 1, 1, 2),
     # the streaming form: ragged 32-channel blocks with a multiplier of 2,
     # pad 2 along z and stride 2 along x; k0 = 1; a multiplier of 16 and a
@@ -383,7 +394,8 @@ def test_conv3d_ndhwc_stream_misaligned(tc):
 # --------------------------------------------------------------------------
 def test_misaligned_input_uses_plain_loads(tc):
     """x starting 4 bytes past a 16-byte boundary cannot be a TMA source; the
-    plain-load producer must give the same result."""
+    plain-load producer must give the same result (NCDHW, and the
+    channels-last mode's own box layout)."""
     x, w, b = make((2, 4, 6, 7, 8), (5, 4, 3, 3, 3), 5)
     buf = torch.zeros(x.size + 1, dtype=torch.float32, device="cuda")
     buf[1:] = torch.from_numpy(x.ravel()).cuda()
@@ -391,6 +403,15 @@ def test_misaligned_input_uses_plain_loads(tc):
     assert xv.data_ptr() % 16 != 0
     y = tc.conv3d_fwd(xv, _dev(w), _dev(b), 1, 1).cpu().numpy()
     check(y, orc.conv3d(x, w, b, 1, 1), "misaligned x")
+    x, w, b = make((2, 16, 6, 7, 9), (24, 16, 3, 3, 3), 24, seed=75)
+    x_cl = np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))
+    assert tc.plan_describe(5, x.shape, w.shape, 1, 1)["cl"] == 1
+    buf = torch.zeros(x.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(x_cl.ravel()).cuda()
+    xv = buf[1:].view(x_cl.shape)
+    assert xv.data_ptr() % 16 != 0
+    y = tc.conv3d_fwd_ndhwc(xv, _dev(w), _dev(b), 1, 1).cpu().numpy()
+    check(y, orc.conv3d(x, w, b, 1, 1).transpose(0, 2, 3, 4, 1), "misaligned channels-last x")
 
 
 def test_guard_bands_untouched(tc):

@@ -36,7 +36,7 @@ struct DeviceState {
   int status = TC3D_OK;
   int sm_count = 0;
   int* err = nullptr;  // device address of the error word
-  bool smem_set[4] = {false, false, false, false};  // per kernel id
+  bool smem_set[5] = {false, false, false, false, false};  // per kernel id
   bool gram_smem_set = false;
   bool direct_smem_set = false;
   bool lag_smem_set = false;
@@ -188,6 +188,8 @@ void fill_params(const Plan& pl, EngineParams* ep) {
   ep->a_stages = pl.a_stages;
   ep->ks_stage = pl.ks_stage;
   ep->view = pl.view;
+  ep->cl = pl.cl;
+  ep->cl_cb = pl.cl_cb;
   ep->nslots = pl.nslots;
   ep->slot_bytes = (unsigned)pl.slot_bytes;
   ep->wide = pl.wide;
@@ -216,6 +218,30 @@ void fill_params(const Plan& pl, EngineParams* ep) {
 void encode_xmap(const Plan& pl, const float* x, EngineParams* ep) {
   const Problem& pb = pl.pb;
   ep->use_tma = 0;
+  if (pl.cl) {
+    // channels-last: x as (C, S2, S1, S0, N), box cl_cb x B2 x B1 x B0 x 1
+    if (!g_encode || !aligned(x, 16) || (pb.Cin % 4) != 0) return;
+    cuuint64_t dims[5] = {(cuuint64_t)pb.Cin, (cuuint64_t)pb.S[2], (cuuint64_t)pb.S[1],
+                          (cuuint64_t)pb.S[0], (cuuint64_t)pb.N};
+    cuuint64_t strides[4];
+    strides[0] = (cuuint64_t)pb.Cin * 4;
+    strides[1] = strides[0] * pb.S[2];
+    strides[2] = strides[1] * pb.S[1];
+    strides[3] = strides[2] * pb.S[0];
+    for (int i = 0; i < 4; ++i)
+      if (strides[i] >= (1ull << 40)) return;
+    cuuint32_t box[5] = {(cuuint32_t)pl.cl_cb, (cuuint32_t)pl.box[2], (cuuint32_t)pl.box[1],
+                         (cuuint32_t)pl.box[0], 1};
+    for (int i = 0; i < 5; ++i)
+      if (box[i] == 0 || box[i] > 256) return;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(&ep->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float*>(x),
+                          dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) ep->use_tma = 1;
+    return;
+  }
   if (!g_encode || !aligned(x, 16) || (pb.S[2] % 4) != 0) return;
   cuuint64_t dims[5] = {(cuuint64_t)pb.S[2], (cuuint64_t)pb.S[1], (cuuint64_t)pb.S[0],
                         (cuuint64_t)pb.Cin, (cuuint64_t)pb.N};
@@ -315,6 +341,7 @@ int launch_pack(const Plan& pl, const float* w, float* wpack, int sm_count, cuda
   pp.k_chunk = pl.k_chunk;
   pp.ksteps_chunk = pl.ksteps_chunk;
   pp.octet_major = pl.view;
+  pp.tap_major = pl.cl;
   pp.total = pl.ws_wpack_bytes / 4;
   long long blocks = (pp.total + 255) / 256;
   if (blocks > (long long)sm_count * 8) blocks = (long long)sm_count * 8;
@@ -371,7 +398,7 @@ int launch_engine(const Plan& pl, int epi, const float* x, const float* wpack, c
   encode_xmap(pl, x, &ep);
   const unsigned grid = (unsigned)engine_grid(pl, d->sm_count);
   ep.part_slots = (int)bn_part_slots(pl, grid);
-  const int kid = pl.view ? kEngineView : epi;
+  const int kid = pl.view ? kEngineView : pl.cl ? kEngineCl : epi;
   int rc = set_smem(d, kid);
   if (rc) return rc;
   return engine_launch(kid, ep, grid, (size_t)pl.smem_bytes, st) == cudaSuccess ? TC3D_OK
@@ -417,8 +444,23 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
               const int stride[3], const int pad[3], const int dil[3], const int out_pad[3],
               int groups, CallPlan* cp) {
   cp->ndhwc = op == OP_CONV_NDHWC;
-  int rc = plan_for(cp->ndhwc ? OP_CONV : op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad,
-                    dil, out_pad, groups, &cp->pl);
+  int rc;
+  if (cp->ndhwc) {
+    // channels-last: the engine's channels-last mode where it applies, else
+    // the NCDHW plan of the transposed copies
+    if (!stride || !pad || !dil) return TC3D_ERR_NULL;
+    Problem pb = make_problem(OP_CONV, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil,
+                              out_pad, groups);
+    pb.cl = 1;
+    rc = make_plan(pb, &cp->pl);
+    if (rc == TC3D_OK && !cp->pl.cl) {
+      pb.cl = 0;
+      rc = make_plan(pb, &cp->pl);
+    }
+  } else {
+    rc = plan_for(op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride, pad, dil, out_pad, groups,
+                  &cp->pl);
+  }
   if (rc) return rc;
   cp->upb = make_problem(cp->ndhwc ? OP_CONV : op, N, Cin, S0, S1, S2, Cout, k0, k1, k2, stride,
                          pad, dil, out_pad, groups);
@@ -437,7 +479,7 @@ int plan_call(int op, int N, int Cin, int S0, int S1, int S2, int Cout, int k0, 
   cp->ws_total = cp->pool ? cp->pp.ws_total : cp->pl.ws_total;
   if (cp->direct) {
     cp->ws_total = 256;  // nothing is staged
-  } else if (cp->ndhwc) {
+  } else if (cp->ndhwc && !cp->pl.cl) {
     // channels-last through the engine: x and y transposed to NCDHW copies
     // (the transpose grid: batch in y, 32 x 32 tiles in x)
     const int64_t sv = (int64_t)pb.S[0] * pb.S[1] * pb.S[2];
@@ -759,7 +801,7 @@ int run(int op, const float* x, const float* w, const float* bias, const BnArgs&
   if (rc) return rc;
   if (cp.pool) return run_pool(op, cp, x, w, bias, bn, y, ws, d, st);
   if (cp.direct) return run_direct(cp, x, w, bias, y, d, st);
-  if (cp.ndhwc) {
+  if (cp.ndhwc && !cp.pl.cl) {
     // channels-last through the engine: x -> NCDHW, the conv, y -> NDHWC
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     float* xt = reinterpret_cast<float*>(wsb + cp.ws_xt_off);
@@ -896,6 +938,8 @@ std::string describe(const Plan& pl) {
     append(s, ", \"a_stages\": %lld", pl.a_stages);
     append(s, ", \"ks_stage\": %lld", pl.ks_stage);
     append(s, ", \"view\": %lld", pl.view);
+    append(s, ", \"cl\": %lld", pl.cl);
+    append(s, ", \"cl_cb\": %lld", pl.cl_cb);
     append(s, ", \"reshaped\": %lld", pl.reshaped);
     append(s, ", \"nslots\": %lld", pl.nslots);
     append(s, ", \"slot_bytes\": %lld", pl.slot_bytes);

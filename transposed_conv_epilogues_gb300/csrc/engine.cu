@@ -576,7 +576,9 @@ struct EngineFill {
 
 }  // namespace
 
-template <int EPI, bool VIEW>
+// CL: the channels-last mode (store epilogue only), a template parameter so
+// that the NCDHW kernels compile without its branches
+template <int EPI, bool VIEW, bool CL>
 __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
     engine_kernel(const __grid_constant__ EngineParams p) {
   constexpr int kWarpConv0 = WarpCfg<EPI>::kConv0;
@@ -633,6 +635,19 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
       ktab[t] = (p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2] + xshift;
     }
+  } else if (CL) {
+    // channels-last: per K-step j of a chunk (tap j / (cin_chunk / 8), its
+    // channels 8 (j % (cin_chunk / 8)) .. + 7), the float offset of its first
+    // value from a row's own position in the raw box
+    int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
+    const int per_tap = p.cin_chunk / 8;
+    for (int j = threadIdx.x; j < p.ksteps_chunk; j += kThreads) {
+      const int t = j / per_tap, c8 = j - t * per_tap;
+      const int t0 = t / (p.nU[1] * p.nU[2]), t1 = (t / p.nU[2]) % p.nU[1], t2 = t % p.nU[2];
+      ktab[j] = ((p.u_rel[0][t0] * p.box[1] + p.u_rel[1][t1]) * p.box[2] + p.u_rel[2][t2]) *
+                    p.cl_cb +
+                8 * c8;
+    }
   } else {
     // GEMM-K table of one channel chunk: raw-box offset of (channel, tap) pair k
     int* ktab = reinterpret_cast<int*>(gbase + p.sm_ktab);
@@ -667,7 +682,8 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       const TileCoord tc = decode_tile(p, tile);
       const int zc = p.s_in[0] * tc.o[0] + p.u_min[0];
       const int yc = p.s_in[1] * tc.o[1] + p.u_min[1];
-      const int xc = (p.s_in[2] * tc.o[2] + p.u_min[2]) & ~3;
+      // the x start is rounded down to 16 bytes where x is the innermost axis
+      const int xc = (p.s_in[2] * tc.o[2] + p.u_min[2]) & (CL ? ~0 : ~3);
       bool ok = true;
       // column block cb belongs to group g (nb_per_group blocks per group)
       for (int cb = 0, g = 0, nb = 0; cb < p.n_colblocks && ok;
@@ -689,9 +705,34 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
           const uint32_t dst = sbase + p.sm_raw + stage * p.raw_stage_bytes;
           if (p.use_tma) {
             if (lane == 0) {
-              mbar_arrive_expect_tx(bars.raw_full(stage), (uint32_t)(p.cin_chunk * bvol * 4));
-              tma_load_5d(dst, &p.xmap, xc, yc, zc, ch0, tc.n, bars.raw_full(stage));
+              if (CL) {
+                mbar_arrive_expect_tx(bars.raw_full(stage), (uint32_t)(p.cl_cb * bvol * 4));
+                tma_load_5d(dst, &p.xmap, ch0, xc, yc, zc, tc.n, bars.raw_full(stage));
+              } else {
+                mbar_arrive_expect_tx(bars.raw_full(stage), (uint32_t)(p.cin_chunk * bvol * 4));
+                tma_load_5d(dst, &p.xmap, xc, yc, zc, ch0, tc.n, bars.raw_full(stage));
+              }
             }
+          } else if (CL) {
+            // channels-last box without TMA: element e is channel e % cl_cb
+            // of position e / cl_cb, copied by lane e % 32 (zero outside x)
+            const uint32_t dst0 = sbase + p.sm_raw + stage * p.raw_stage_bytes;
+            const int total = p.cl_cb * bvol;
+            for (int e = lane; e < total; e += 32) {
+              const int cl = e % p.cl_cb, pos = e / p.cl_cb;
+              const int i2 = pos % p.box[2], i1 = (pos / p.box[2]) % p.box[1];
+              const int i0 = pos / (p.box[2] * p.box[1]);
+              const int gx = xc + i2, gy = yc + i1, gz = zc + i0, ch = ch0 + cl;
+              const bool in = ch < p.C && gx >= 0 && gx < p.S[2] && gy >= 0 && gy < p.S[1] &&
+                              gz >= 0 && gz < p.S[0];
+              const float* src =
+                  in ? p.x + ((((long long)tc.n * p.S[0] + gz) * p.S[1] + gy) * p.S[2] + gx) * p.C + ch
+                     : p.x;
+              cp_async4_zfill(dst0 + 4u * (uint32_t)e, src, in);
+            }
+            cp_async_wait_all();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.raw_full(stage));
           } else {
             // Element e of the box (channel-major, x fastest) is copied by
             // lane e % 32 with a 4-byte cp.async (zero-filled outside the
@@ -820,12 +861,14 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
       row_local(p, a < p.n_acc ? a : 0, q, lane, t);
       row_base[a] = ((p.s_in[0] * t[0]) * p.box[1] + p.s_in[1] * t[1]) * p.box[2] +
                     p.s_in[2] * t[2];
+      if (CL) row_base[a] *= p.cl_cb;  // channels-last: positions of cl_cb floats
     }
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      // only the x origin of the tile matters here (its alignment shift)
+      // only the x origin of the tile matters here (its alignment shift; none
+      // in channels-last mode)
       const int b2 = tile - fast_div(p.ntile_div[2], tile) * p.ntile[2];
       const int xs = p.s_in[2] * (b2 * p.T[2]) + p.u_min[2];
-      const int xshift = xs - (xs & ~3);
+      const int xshift = CL ? 0 : xs - (xs & ~3);
       for (int cb = 0; cb < p.n_colblocks && ok; ++cb) {
         for (int c = 0; c < p.n_chunks && ok; ++c) {
           ok = __all_sync(0xffffffffu, mbar_wait(bars.raw_full(rstage), rphase, tmo, abortf));
@@ -852,26 +895,42 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
               const int kcount = min(p.ks_stage, p.ksteps_chunk - j0);
               for (int kk = half; kk < kcount; kk += 2) {
                 const int j = j0 + kk;
-                const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
-                const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
-                // GEMM-K entries past the chunk's valid ones (ragged last chunk,
-                // K padding) have zero weights; they read the row's own first
-                // raw element, which is already a term of the row's sum
-                const int kbase = j * 8;
-                const int kraw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                int kofs[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kofs[e] = kbase + e < valid_k ? kraw[e] : 0;
                 const uint32_t kcol = stage_col + (uint32_t)(kk * 16 * p.n_acc);
                 // the gathers of all accumulators first (independent loads in
                 // flight together), then the splits and TMEM stores
                 float xg[4][8];
+                if (CL) {
+                  // channels-last: the K-step's 8 values of a row are 8
+                  // consecutive channels of one position, two 16-byte loads
+                  // (channels past the valid ones are zero-filled by the load)
+                  const int off = ktab[j];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                  if (a >= p.n_acc) break;
-                  const float* rp = raw + row_base[a];
+                  for (int a = 0; a < 4; ++a) {
+                    if (a >= p.n_acc) break;
+                    const float4 v0 = *reinterpret_cast<const float4*>(raw + row_base[a] + off);
+                    const float4 v1 = *reinterpret_cast<const float4*>(raw + row_base[a] + off + 4);
+                    xg[a][0] = v0.x, xg[a][1] = v0.y, xg[a][2] = v0.z, xg[a][3] = v0.w;
+                    xg[a][4] = v1.x, xg[a][5] = v1.y, xg[a][6] = v1.z, xg[a][7] = v1.w;
+                  }
+                } else {
+                  const int4 ka = *reinterpret_cast<const int4*>(ktab + j * 8);
+                  const int4 kb = *reinterpret_cast<const int4*>(ktab + j * 8 + 4);
+                  // GEMM-K entries past the chunk's valid ones (ragged last
+                  // chunk, K padding) have zero weights; they read the row's
+                  // own first raw element, which is already a term of the
+                  // row's sum
+                  const int kbase = j * 8;
+                  const int kraw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                  int kofs[8];
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) xg[a][e] = rp[kofs[e]];
+                  for (int e = 0; e < 8; ++e) kofs[e] = kbase + e < valid_k ? kraw[e] : 0;
+#pragma unroll
+                  for (int a = 0; a < 4; ++a) {
+                    if (a >= p.n_acc) break;
+                    const float* rp = raw + row_base[a];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xg[a][e] = rp[kofs[e]];
+                  }
                 }
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
@@ -969,7 +1028,43 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 
         if constexpr (EPI == EPI_STORE) {
           const int F = p.s_out[0] * p.s_out[1] * p.s_out[2];
-          if (F == 1) {
+          if (CL) {
+            // channels-last y: a row's channels are contiguous, so each lane
+            // stores its own row's 32 channels of a chunk, as 16-byte vectors
+            // where the row's start allows
+            for (int cc = 0; cc < p.n_tile; cc += 32) {
+              const int oc_lane = cc + lane;
+              const float bl =
+                  (p.bias && oc_lane < ocb_valid) ? __ldg(p.bias + oc0 + oc_lane) : 0.f;
+              const int nvalid = min(32, ocb_valid - cc);
+#pragma unroll 1
+              for (int a = 0; a < p.n_acc; ++a) {
+                uint32_t v[32];
+                load_acc32(dbase + (uint32_t)(a * p.acc_cols + cc), lo_off, v);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                  v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __shfl_sync(0xffffffffu, bl, jj));
+                int mm[3];
+                const bool rv = row_global(p, tc.o, a, q, lane, mm);
+                if (!rv) continue;
+                float* yr = p.y +
+                            ((((long long)tc.n * p.O[0] + mm[0]) * p.O[1] + mm[1]) * p.O[2] + mm[2]) *
+                                p.Cout +
+                            oc0 + cc;
+                if (nvalid == 32 && (reinterpret_cast<uintptr_t>(yr) & 15) == 0) {
+#pragma unroll
+                  for (int g = 0; g < 8; ++g)
+                    reinterpret_cast<float4*>(yr)[g] =
+                        make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+                } else {
+#pragma unroll
+                  for (int jj = 0; jj < 32; ++jj)
+                    if (jj < nvalid) yr[jj] = __uint_as_float(v[jj]);
+                }
+              }
+            }
+          } else if (F == 1) {
             // a convolution (or a stride-1 transposed one): one output per
             // row and channel.  Column chunks outer, so that each chunk's
             // bias is loaded once for all accumulators; a full chunk stores
@@ -1328,10 +1423,11 @@ __global__ void __launch_bounds__(WarpCfg<EPI>::kThreads, 1)
 static_assert(WarpCfg<EPI_BN_POOL>::kEpiWarps == 2 * kEpiGroup && kBnSlotsPerCta == kEpiGroup,
               "BatchNorm pooling: two groups of 8 channels, one partial slot per lane quarter");
 
-template __global__ void engine_kernel<EPI_STORE, false>(const __grid_constant__ EngineParams p);
-template __global__ void engine_kernel<EPI_POOL_LSE, false>(const __grid_constant__ EngineParams p);
-template __global__ void engine_kernel<EPI_BN_POOL, false>(const __grid_constant__ EngineParams p);
-template __global__ void engine_kernel<EPI_STORE, true>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_STORE, false, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_POOL_LSE, false, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_BN_POOL, false, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_STORE, true, false>(const __grid_constant__ EngineParams p);
+template __global__ void engine_kernel<EPI_STORE, false, true>(const __grid_constant__ EngineParams p);
 
 // ---------------------------------------------------------------------------
 // weight pre-pack: W -> [colblock][chunk][kstep][w | w_lo][n_tile x 8] in the
@@ -1363,8 +1459,10 @@ __global__ void pack_weights_kernel(const __grid_constant__ PackParams p) {
     const int k = j * 8 + e;
     // GEMM-K index k of the chunk -> (channel, tap): channel-major, or, in
     // view mode, K-step j = (channel octet, tap) with the 8 channels inside
-    const int c_l = p.octet_major ? (j / p.nUtot) * 8 + e : k / p.nUtot;
-    const int t = p.octet_major ? j % p.nUtot : k % p.nUtot;
+    const int c_l = p.tap_major     ? k % p.cin_chunk
+                    : p.octet_major ? (j / p.nUtot) * 8 + e
+                                    : k / p.nUtot;
+    const int t = p.tap_major ? k / p.cin_chunk : p.octet_major ? j % p.nUtot : k % p.nUtot;
     const int icl = c * p.cin_chunk + c_l;
     const int ocg = nb * p.ocb + oc_l;  // output channel within the group
     if (oc_l < p.ocb && ocg < p.cout_g && k < p.k_chunk && icl < p.cin_g) {
@@ -1535,10 +1633,13 @@ __global__ void wait_timeout_kernel(int* err, unsigned long long timeout_cycles)
 cudaError_t engine_set_smem(int kid, int bytes) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
   switch (kid) {
-    case EPI_STORE: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, false>, a, bytes);
-    case EPI_POOL_LSE: return cudaFuncSetAttribute(engine_kernel<EPI_POOL_LSE, false>, a, bytes);
-    case EPI_BN_POOL: return cudaFuncSetAttribute(engine_kernel<EPI_BN_POOL, false>, a, bytes);
-    default: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, true>, a, bytes);
+    case EPI_STORE: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, false, false>, a, bytes);
+    case EPI_POOL_LSE:
+      return cudaFuncSetAttribute(engine_kernel<EPI_POOL_LSE, false, false>, a, bytes);
+    case EPI_BN_POOL:
+      return cudaFuncSetAttribute(engine_kernel<EPI_BN_POOL, false, false>, a, bytes);
+    case kEngineCl: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, false, true>, a, bytes);
+    default: return cudaFuncSetAttribute(engine_kernel<EPI_STORE, true, false>, a, bytes);
   }
 }
 
@@ -1548,16 +1649,19 @@ cudaError_t engine_launch(int kid, const EngineParams& p, unsigned grid, size_t 
                           cudaStream_t st) {
   switch (kid) {
     case EPI_STORE:
-      return launch_dependent(engine_kernel<EPI_STORE, false>, dim3(grid),
+      return launch_dependent(engine_kernel<EPI_STORE, false, false>, dim3(grid),
                               dim3(WarpCfg<EPI_STORE>::kThreads), smem, st, p);
     case EPI_POOL_LSE:
-      return launch_dependent(engine_kernel<EPI_POOL_LSE, false>, dim3(grid),
+      return launch_dependent(engine_kernel<EPI_POOL_LSE, false, false>, dim3(grid),
                               dim3(WarpCfg<EPI_POOL_LSE>::kThreads), smem, st, p);
     case EPI_BN_POOL:
-      return launch_dependent(engine_kernel<EPI_BN_POOL, false>, dim3(grid),
+      return launch_dependent(engine_kernel<EPI_BN_POOL, false, false>, dim3(grid),
                               dim3(WarpCfg<EPI_BN_POOL>::kThreads), smem, st, p);
+    case kEngineCl:
+      return launch_dependent(engine_kernel<EPI_STORE, false, true>, dim3(grid),
+                              dim3(WarpCfg<EPI_STORE>::kThreads), smem, st, p);
     default:
-      return launch_dependent(engine_kernel<EPI_STORE, true>, dim3(grid),
+      return launch_dependent(engine_kernel<EPI_STORE, true, false>, dim3(grid),
                               dim3(WarpCfg<EPI_STORE>::kThreads), smem, st, p);
   }
 }

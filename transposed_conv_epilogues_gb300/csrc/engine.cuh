@@ -125,6 +125,10 @@ struct EngineParams {
   int b_resident, b_stages;
   unsigned b_stage_bytes;
 
+  // channels-last mode: x [N][S0][S1][S2][C] and y [N][O0][O1][O2][Cout];
+  // the raw box is [position][cl_cb] (cl_cb = cin_chunk + 4 channels)
+  int cl, cl_cb;
+
   // view mode: A read by the tensor core from channels-last octet slots
   int view, nslots;
   unsigned slot_bytes;
@@ -155,14 +159,17 @@ struct PackParams {
   int ocb, n_tile, nb_per_group, n_colblocks;
   int cin_chunk, n_chunks, k_chunk, ksteps_chunk;
   int octet_major;  // 1: K-step j of a chunk is channel octet j / nUtot at tap j % nUtot
+  int tap_major;    // 1: GEMM-K index k of a chunk is tap k / cin_chunk, channel k % cin_chunk
   long long total;  // floats in the packed buffer
   unsigned long long* zero_ctr;  // set to 0 when non-null (the engine's bias-fill counter)
 };
 
 // host-side launch wrappers (engine.cu; kernels are launched from the
 // translation unit that defines them)
-// kernel id: the epilogue kind, or kEngineView for the view-mode store kernel
+// kernel id: the epilogue kind, or kEngineView for the view-mode store
+// kernel, kEngineCl for the channels-last one
 constexpr int kEngineView = 3;
+constexpr int kEngineCl = 4;
 cudaError_t engine_set_smem(int kid, int bytes);
 cudaError_t engine_launch(int kid, const EngineParams& p, unsigned grid, size_t smem,
                           cudaStream_t st);

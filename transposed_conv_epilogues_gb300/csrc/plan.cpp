@@ -337,33 +337,72 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
     if (pl.tiles >= ((int64_t)1 << 31)) return fail(TC3D_ERR_UNSUPPORTED);
   }
 
+  // ---- channels-last mode: a conv on NDHWC tensors (groups 1, one class)
+  // whose box and tap count fit.  The box's x start needs no 16-byte
+  // rounding there (channels are the innermost axis), so it has no slack.
+  pl.cl = 0;
+  if (pb.cl && pb.op == OP_CONV && pb.groups == 1 && pl.nR == 1 && nUtot <= kMaxKChunk / 8) {
+    Plan c = pl;
+    c.box[2] = (int)std::min<int64_t>(
+        (int64_t)c.s_in[2] * (c.T[2] - 1) + (c.u_max[2] - c.u_min[2]) + 1, 1 << 30);
+    c.xslack = 0;
+    const int64_t bvol = (int64_t)c.box[0] * c.box[1] * c.box[2];
+    const int64_t bstage = 64LL * c.n_tile;
+    const int64_t fixed = 4096 + 1024 + 1024;
+    // a chunk of 8, 16, 24 or 32 channels (not past the channel count) whose
+    // two raw stages fit beside the weight stages: the fewest K-steps over
+    // all chunks (a ragged last chunk is padded), then the widest
+    int64_t best_steps = INT64_MAX;
+    for (int cc = std::min(32, (int)round_up(c.cin_g, 8)); cc >= 8; cc -= 8) {
+      const int64_t raw = round_up(bvol * (cc + 4) * 4, 1024);
+      const int64_t ks = (int64_t)(cc / 8) * nUtot;
+      if (c.box[0] > 256 || c.box[1] > 256 || c.box[2] > 256 || raw > 96 * 1024 ||
+          cc * nUtot > kMaxKChunk)
+        continue;
+      if (2 * raw + 4 * bstage + fixed + round_up(ks * 32, 1024) > kMaxSmem) continue;
+      const int64_t steps = ceil_div(c.cin_g, cc) * ks;
+      if (steps >= best_steps) continue;
+      best_steps = steps;
+      c.cl = 1;
+      c.cl_cb = cc + 4;
+      c.cin_chunk = cc;
+      c.n_chunks = (int)ceil_div(c.cin_g, cc);
+      c.k_chunk = cc * nUtot;
+      c.ksteps_chunk = (int)ks;
+      c.raw_stage_bytes = raw;
+    }
+    if (c.cl) pl = c;
+  }
+
   // ---- channel chunk, smem budget
   {
     const int64_t bvol = (int64_t)pl.box[0] * pl.box[1] * pl.box[2];
     const int64_t raw_ch = bvol * 4;
     const int64_t bstage = 64LL * pl.n_tile;  // w + w_lo, n_tile x 8 tf32 each
     const int64_t fixed = 4096 + 1024 + 1024; // epilogue scratch, barriers, alignment
-    int best_cc = 0;
-    int64_t best_steps = INT64_MAX;
-    int max_cc = std::min(pl.cin_g, kMaxKChunk / nUtot);
-    if (max_cc < 1) return fail(TC3D_ERR_UNSUPPORTED);
-    for (int cc = 1; cc <= max_cc; ++cc) {
-      int64_t need = 2 * round_up(cc * raw_ch, 1024) + 4 * bstage + fixed +
-                     round_up(ceil_div((int64_t)cc * nUtot, 8) * 32, 1024);
-      if (need > kMaxSmem) break;
-      if (cc * raw_ch > 64 * 1024 && cc > 1) break;  // keep one stage modest
-      int64_t steps = ceil_div(pl.cin_g, cc) * ceil_div((int64_t)cc * nUtot, 8);
-      if (steps <= best_steps) {
-        best_steps = steps;
-        best_cc = cc;
+    if (!pl.cl) {
+      int best_cc = 0;
+      int64_t best_steps = INT64_MAX;
+      int max_cc = std::min(pl.cin_g, kMaxKChunk / nUtot);
+      if (max_cc < 1) return fail(TC3D_ERR_UNSUPPORTED);
+      for (int cc = 1; cc <= max_cc; ++cc) {
+        int64_t need = 2 * round_up(cc * raw_ch, 1024) + 4 * bstage + fixed +
+                       round_up(ceil_div((int64_t)cc * nUtot, 8) * 32, 1024);
+        if (need > kMaxSmem) break;
+        if (cc * raw_ch > 64 * 1024 && cc > 1) break;  // keep one stage modest
+        int64_t steps = ceil_div(pl.cin_g, cc) * ceil_div((int64_t)cc * nUtot, 8);
+        if (steps <= best_steps) {
+          best_steps = steps;
+          best_cc = cc;
+        }
       }
+      if (best_cc == 0) return fail(TC3D_ERR_UNSUPPORTED);
+      pl.cin_chunk = best_cc;
+      pl.n_chunks = (int)ceil_div(pl.cin_g, best_cc);
+      pl.k_chunk = best_cc * nUtot;
+      pl.ksteps_chunk = (int)ceil_div(pl.k_chunk, 8);
+      pl.raw_stage_bytes = round_up(best_cc * raw_ch, 1024);
     }
-    if (best_cc == 0) return fail(TC3D_ERR_UNSUPPORTED);
-    pl.cin_chunk = best_cc;
-    pl.n_chunks = (int)ceil_div(pl.cin_g, best_cc);
-    pl.k_chunk = best_cc * nUtot;
-    pl.ksteps_chunk = (int)ceil_div(pl.k_chunk, 8);
-    pl.raw_stage_bytes = round_up(best_cc * raw_ch, 1024);
     // An A-stage carries up to ks_stage K-steps of all accumulators (up to 24
     // MMAs) so that each stage's barrier wait / commit is amortised; a stage
     // never straddles two channel chunks.  Streamed weight stages match
@@ -414,7 +453,7 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
   // Channels are padded to octets with zeros.
   {
     const int S2 = pb.S[2];
-    const bool base_ok = pb.op == OP_CONV && pl.s_in[0] == 1 && pl.s_in[1] == 1 &&
+    const bool base_ok = pb.op == OP_CONV && !pl.cl && !pb.cl && pl.s_in[0] == 1 && pl.s_in[1] == 1 &&
                          pl.s_in[2] == 1 && pl.n_tile <= 128 && pl.nR == 1 &&
                          pl.n_colblocks == 1;
     const bool lines = base_ok && pl.nU[2] == 1 && pl.u_min[2] == 0 && pl.M[2] == S2 &&

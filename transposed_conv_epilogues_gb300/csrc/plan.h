@@ -49,6 +49,9 @@ struct Problem {
   // internal convolutions only: output extents below the formula's (0: the
   // formula's own); rows past them are not computed
   int out_ext[3];
+  // 1: x and y are channels-last (NDHWC); the plan then takes the engine's
+  // channels-last mode where it applies (Plan::cl)
+  int cl;
 };
 
 // Everything a launch needs, derived from a Problem.  Row space: for every
@@ -120,6 +123,13 @@ struct Plan {
   int view;
   int nslots;
   int64_t slot_bytes;
+  // channels-last mode (a conv on NDHWC x and y, groups 1): the raw box is
+  // [position][cl_cb] with cl_cb = cin_chunk + 4 channels (cl_cb / 4 odd, so
+  // 16-byte loads of consecutive positions hit distinct banks), GEMM-K runs
+  // tap-major, channel-minor, and a K-step (8 channels of one tap) is two
+  // 16-byte loads per row
+  int cl;
+  int cl_cb;
   // 1: planned in the merged (S1*S2) form of a (k,k,1) conv (see make_plan);
   // O_user are then the caller's output extents, O the merged ones
   int reshaped;
