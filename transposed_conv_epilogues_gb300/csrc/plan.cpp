@@ -340,36 +340,75 @@ static int make_plan_direct(const Problem& pb_in, Plan* out) {
   // ---- channels-last mode: a conv on NDHWC tensors (groups 1, one class)
   // whose box and tap count fit.  The box's x start needs no 16-byte
   // rounding there (channels are the innermost axis), so it has no slack.
+  // The tile found above is kept when its box fits the mode's stage budget;
+  // else a search of its own picks the tile (no x-store preference: a row's
+  // channels are one contiguous run whatever the tile).
   pl.cl = 0;
   if (pb.cl && pb.op == OP_CONV && pb.groups == 1 && pl.nR == 1 && nUtot <= kMaxKChunk / 8) {
-    Plan c = pl;
-    c.box[2] = (int)std::min<int64_t>(
-        (int64_t)c.s_in[2] * (c.T[2] - 1) + (c.u_max[2] - c.u_min[2]) + 1, 1 << 30);
-    c.xslack = 0;
-    const int64_t bvol = (int64_t)c.box[0] * c.box[1] * c.box[2];
-    const int64_t bstage = 64LL * c.n_tile;
+    const int64_t bstage = 64LL * pl.n_tile;
     const int64_t fixed = 4096 + 1024 + 1024;
-    // a chunk of 8, 16, 24 or 32 channels (not past the channel count) whose
-    // two raw stages fit beside the weight stages: the fewest K-steps over
-    // all chunks (a ragged last chunk is padded), then the widest
-    int64_t best_steps = INT64_MAX;
-    for (int cc = std::min(32, (int)round_up(c.cin_g, 8)); cc >= 8; cc -= 8) {
-      const int64_t raw = round_up(bvol * (cc + 4) * 4, 1024);
-      const int64_t ks = (int64_t)(cc / 8) * nUtot;
-      if (c.box[0] > 256 || c.box[1] > 256 || c.box[2] > 256 || raw > 96 * 1024 ||
-          cc * nUtot > kMaxKChunk)
-        continue;
-      if (2 * raw + 4 * bstage + fixed + round_up(ks * 32, 1024) > kMaxSmem) continue;
-      const int64_t steps = ceil_div(c.cin_g, cc) * ks;
-      if (steps >= best_steps) continue;
-      best_steps = steps;
-      c.cl = 1;
-      c.cl_cb = cc + 4;
-      c.cin_chunk = cc;
-      c.n_chunks = (int)ceil_div(c.cin_g, cc);
-      c.k_chunk = cc * nUtot;
-      c.ksteps_chunk = (int)ks;
-      c.raw_stage_bytes = raw;
+    auto cl_box = [&](int a, int t) {
+      return (int)std::min<int64_t>(
+          (int64_t)pl.s_in[a] * (t - 1) + (pl.u_max[a] - pl.u_min[a]) + 1, 1 << 30);
+    };
+    // the chunk of 8, 16, 24 or 32 channels (not past the channel count)
+    // whose two raw stages fit beside the weight stages: the fewest K-steps
+    // over all chunks (a ragged last chunk is padded), then the widest
+    auto fit = [&](Plan& c) {
+      for (int a = 0; a < 3; ++a) c.box[a] = cl_box(a, c.T[a]);
+      c.xslack = 0;
+      const int64_t bvol = (int64_t)c.box[0] * c.box[1] * c.box[2];
+      int64_t best_steps = INT64_MAX;
+      for (int cc = std::min(32, (int)round_up(c.cin_g, 8)); cc >= 8; cc -= 8) {
+        const int64_t raw = round_up(bvol * (cc + 4) * 4, 1024);
+        const int64_t ks = (int64_t)(cc / 8) * nUtot;
+        if (c.box[0] > 256 || c.box[1] > 256 || c.box[2] > 256 || raw > 96 * 1024 ||
+            cc * nUtot > kMaxKChunk)
+          continue;
+        if (2 * raw + 4 * bstage + fixed + round_up(ks * 32, 1024) > kMaxSmem) continue;
+        const int64_t steps = ceil_div(c.cin_g, cc) * ks;
+        if (steps >= best_steps) continue;
+        best_steps = steps;
+        c.cl = 1;
+        c.cl_cb = cc + 4;
+        c.cin_chunk = cc;
+        c.n_chunks = (int)ceil_div(c.cin_g, cc);
+        c.k_chunk = cc * nUtot;
+        c.ksteps_chunk = (int)ks;
+        c.raw_stage_bytes = raw;
+      }
+      return c.cl == 1;
+    };
+    Plan c = pl;
+    if (!fit(c)) {
+      const int lq = ilog2(4 * pl.n_acc);
+      double best = 1e300;
+      for (int q2 = 0; q2 <= 5; ++q2)
+        for (int q1 = 0; q1 + q2 <= 5; ++q1)
+          for (int p2 = 0; p2 <= lq; ++p2)
+            for (int p1 = 0; p1 + p2 <= lq; ++p1) {
+              const int Q[3] = {1 << (5 - q1 - q2), 1 << q1, 1 << q2};
+              const int P[3] = {1 << (lq - p1 - p2), 1 << p1, 1 << p2};
+              Plan t = pl;
+              double rows = 1, bv = 1;
+              for (int a = 0; a < 3; ++a) {
+                t.Q[a] = Q[a];
+                t.Pq[a] = P[a];
+                t.T[a] = Q[a] * P[a];
+                rows *= (double)round_up(pl.M[a], t.T[a]);
+                bv *= cl_box(a, t.T[a]);
+              }
+              const double cost = rows * (1.0 + 0.04 * bv / (128.0 * pl.n_acc));
+              if (cost < best && fit(t)) {
+                best = cost;
+                c = t;
+              }
+            }
+      if (c.cl) {
+        for (int a = 0; a < 3; ++a) c.ntile[a] = (int)ceil_div(c.M[a], c.T[a]);
+        c.tiles = (int64_t)pb.N * c.ntile[0] * c.ntile[1] * c.ntile[2];
+        if (c.tiles >= ((int64_t)1 << 31)) c.cl = 0;
+      }
     }
     if (c.cl) pl = c;
   }
