@@ -103,9 +103,11 @@ int tc3d_conv3d_fwd(const float* x, const float* w, const float* bias, float* y,
  * y [N, O0, O1, O2, Cout] (w and bias as for tc3d_conv3d_fwd).  Convs with
  * few channels per group (Cin/groups * Cout/groups <= 16, stride and
  * dilation 1 or 2 and at most 7 taps along the last axis) run in a direct
- * fp32 kernel that reads NDHWC natively; others transpose x to NCDHW in the
- * workspace, run the engine and transpose y back.  tc3d_workspace_bytes /
- * tc3d_out_shape take TC3D_OP_CONV3D_NDHWC (out_dims in NDHWC order). */
+ * fp32 kernel that reads NDHWC natively; dense convs (groups 1) run in the
+ * tensor-core engine's channels-last mode, which also reads and writes NDHWC
+ * directly; other grouped convs transpose x to NCDHW in the workspace, run
+ * the engine and transpose y back.  tc3d_workspace_bytes / tc3d_out_shape
+ * take TC3D_OP_CONV3D_NDHWC (out_dims in NDHWC order). */
 int tc3d_conv3d_fwd_ndhwc(const float* x, const float* w, const float* bias, float* y, int N,
                           int Cin, int S0, int S1, int S2, int Cout, int k0, int k1, int k2,
                           const int stride[3], const int pad[3], const int dilation[3],
