@@ -366,6 +366,10 @@ def test_plans_of_workloads(lib):
     ((1, 1, 2), (1, 1, 2), 0),   # one row pair: the engine writes every row
     ((2, 2, 1), (2, 2, 1), 0),   # stride 1 along x: the general one-class store
     ((2, 2, 2), (1, 1, 1), 0),   # every class has taps
+    ((1, 4, 2), (1, 4, 2), 1),   # y stride 4: rows y % 4 != r1 filled in row mode
+    ((3, 1, 2), (3, 1, 2), 1),   # z stride 3: whole planes z % 3 != r0
+    ((4, 1, 2), (4, 1, 2), 1),   # z stride 4
+    ((2, 3, 2), (2, 3, 2), 0),   # 12 classes: above the one-class store's 8
 ])
 def test_fill_rows_plan(lib, s, d, want):
     """Row mode of the bias fill: exactly when the engine stores through the
