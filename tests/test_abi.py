@@ -404,3 +404,23 @@ def test_channels_last_chunks(lib, cin, xext):
     assert pl["box"][2] == pl["T"][2] + 2
     # transposed convs keep the NCDHW planning
     assert tc.plan_describe(3, (2, cin, 6, 8, xext), (cin, 16, 3, 3, 3), 2, 1)["cl"] == 0
+
+
+def test_channels_last_tile_search(lib):
+    """A strided channels-last conv whose NCDHW-planned tile (x-long) gives a
+    box over the channels-last stage budget gets a tile of its own search:
+    the mode still applies, every raw stage fits in 96 KB and the plan's
+    shared memory in 227 KB; the tile covers the rows."""
+    xs, ws = (1, 32, 5, 6, 40), (64, 32, 3, 3, 3)
+    s, p, d = (1, 2, 2), (1, 0, 1), (2, 1, 1)
+    ncdhw = tc.plan_describe(0, xs, ws, s, p, d)
+    pl = tc.plan_describe(5, xs, ws, s, p, d)
+    assert pl["status"] == 0 and pl["cl"] == 1
+    assert pl["T"] != ncdhw["T"]
+    bvol = pl["box"][0] * pl["box"][1] * pl["box"][2]
+    assert bvol * pl["cl_cb"] * 4 <= 96 * 1024 and pl["smem_bytes"] <= 227 * 1024
+    for a in range(3):
+        st = s[a]
+        span = d[a] * (ws[2 + a] - 1)
+        assert pl["box"][a] == st * (pl["T"][a] - 1) + span + 1
+    assert pl["tiles"] == 1 * np.prod([-(-pl["M"][a] // pl["T"][a]) for a in range(3)])
